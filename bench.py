@@ -1,0 +1,578 @@
+#!/usr/bin/env python
+"""Benchmark of the linear-state prefix cache hot path on GB300.
+
+One step (workload "c1-serving-step": 36 GDN + 12 attention layers, 256 slots,
+conv [8192, 3] bf16, ssm [32, 128, 128] fp32, 4 KiB-rounded pages):
+  1. lsc_restore of 64 rows, all hits, on a prepare stream, signalling an event;
+  2. the forward stream waits on the event, then runs lsc_gdn_decode for the 64
+     restored rows on each of the 36 GDN layers (one decode token).
+value = algorithmic HBM bytes of the step / step time (GB/s); rows/s beside it.
+Also measured in the same run (rank 0, N = 1): the 256-row bf16 decode layer,
+the 512-row restore storm and the token-by-token resume prefill.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lsc|reference] [--no-parts]
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "restore & gather→GDN-step→scatter HBM GB/s (fraction of GB300 peak); rows/s"
+UNIT = "GB/s"
+FALLBACK_HBM = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["lsc", "reference"], default="lsc")
+    ap.add_argument("--no-parts", action="store_true", help="headline step only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+# ---------------------------------------------------------------- clocks
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- pools
+
+def make_pool(L, W, w, seed):
+    """Allocate and fill a pool on the current device; returns (buf, pool, views)."""
+    import torch
+    kinds = [L.LSC_LAYER_GDN if k == W.GDN else L.LSC_LAYER_ATTENTION for k in w.layers]
+    dt = {W.F32: L.LSC_F32, W.BF16: L.LSC_BF16}
+    desc = L.make_pool_desc(kinds, w.num_slots, w.conv_dim, w.conv_width, dt[w.conv_dtype], w.num_v_heads,
+                            w.head_v_dim, w.head_k_dim, dt[w.ssm_dtype], w.page_bytes)
+    nbytes = L.lsc_pool_required_bytes(desc)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    rc, pool = L.lsc_pool_create(desc, buf, nbytes)
+    if rc != L.LSC_OK:
+        raise RuntimeError(L.lsc_error_string(rc))
+    views = {}
+    for l in w.gdn_layers:
+        rc, v = L.lsc_pool_layer_view(pool, l)
+        assert rc == L.LSC_OK
+        views[l] = v
+        off = v.region - buf.data_ptr()
+        fill = [(0, v.conv_bytes // W.ESIZE[w.conv_dtype], w.conv_dtype),
+                (v.ssm_offset_bytes, v.ssm_bytes // W.ESIZE[w.ssm_dtype], w.ssm_dtype)]
+        W.fill_region_device(buf[off:off + v.region_bytes], w.num_slots, w.page_bytes, fill, w.pad_byte,
+                             seed * 1000 + l)
+    torch.cuda.synchronize()
+    return buf, pool, views
+
+
+def restore_bytes(view, n_hit, n_gdn, n_rows):
+    """Algorithmic bytes of a restore: read + write of both views per (hit, layer),
+    plus one has_initial_state byte per written row."""
+    return 2 * n_hit * n_gdn * (view.conv_bytes + view.ssm_bytes) + n_rows
+
+
+def decode_bytes(view, w, n):
+    """Algorithmic bytes of one decode launch over n rows: conv + ssm state read and
+    written, x, alpha, beta, out, idx, has_init per row; the conv weights once."""
+    es = 2 if w.conv_dtype == "bf16" else 4
+    per_row = (2 * (view.conv_bytes + view.ssm_bytes) + w.conv_dim * es + 2 * w.num_v_heads * 4
+               + w.num_v_heads * w.head_v_dim * 4 + 4 + 1)
+    return n * per_row + w.conv_dim * w.conv_width * es
+
+
+def kernel_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha"]:
+        return None
+    return d["bytes_per_launch"]
+
+
+# ---------------------------------------------------------------- our arm
+
+def serving_step_inputs(W, w, rows, seed=0):
+    n = len(rows.live)
+    xs, abs_ = [], []
+    for l in w.gdn_layers:
+        x, cw, a, b = W.decode_inputs(w, n, seed=seed, layer=l)
+        xs.append((x, cw))
+        abs_.append((a, b))
+    return xs, abs_
+
+
+def run_lsc(args):
+    import torch
+    import torch.distributed as dist
+    from linear_attention_state_lsc_gb300 import lsc as L
+    from linear_attention_state_lsc_gb300 import workloads as W
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    L.load()
+    hbm_peak, peak_src = peaks()
+
+    w = W.get("c1")
+    rows = W.restore_rows("c1", seed=rank)  # each rank is an independent replica
+    buf, pool, views = make_pool(L, W, w, seed=rank)
+    v0 = views[w.gdn_layers[0]]
+    n = len(rows.live)
+    n_gdn = len(w.gdn_layers)
+    ops = L.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
+
+    # device-resident inputs of the step
+    bf = torch.bfloat16
+    idx = torch.from_numpy(rows.live.astype(np.int32)).cuda()
+    hs = torch.empty(n, dtype=torch.uint8, device="cuda")
+    hs_prefill = torch.from_numpy(rows.hs_prefill.copy()).cuda()
+    xs, abs_ = serving_step_inputs(W, w, rows, seed=rank)
+    X = torch.stack([torch.from_numpy(x) for x, _ in xs]).to(bf).cuda()          # [36, n, C]
+    CW = torch.stack([torch.from_numpy(cw) for _, cw in xs]).to(bf).cuda()       # [36, C, W]
+    A = torch.stack([torch.from_numpy(a) for a, _ in abs_]).cuda()               # [36, n, Hv]
+    B = torch.stack([torch.from_numpy(b) for _, b in abs_]).cuda()
+    OUT = torch.empty((n_gdn, n, w.num_v_heads, w.head_v_dim), device="cuda")
+    dargs = [L.decode_args(n, w.num_k_heads, idx, hs, X[g], CW[g], A[g], B[g], OUT[g]) for g in range(n_gdn)]
+
+    prep = torch.cuda.Stream()
+    fwd = torch.cuda.current_stream()
+    ev_done = torch.cuda.Event()
+    ev_done.record(fwd)
+    torch.cuda.synchronize()
+    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] for k in ("r0", "r1", "d0", "d1")}
+
+    def step(i=None):
+        hs.copy_(hs_prefill)
+        prep.wait_stream(fwd)
+        if i is not None:
+            ev["r0"][i].record(prep)
+        rc, _ = L.lsc_restore(pool, ops, rows.nkv, rows.block_size, rows.initialized, hs, prep, ev_done)
+        assert rc == L.LSC_OK, L.lsc_error_string(rc)
+        if i is not None:
+            ev["r1"][i].record(prep)
+        fwd.wait_event(ev_done)
+        if i is not None:
+            ev["d0"][i].record(fwd)
+        for g, l in enumerate(w.gdn_layers):
+            rc = L.lsc_gdn_decode(pool, l, dargs[g], fwd)
+            assert rc == L.LSC_OK, L.lsc_error_string(rc)
+        if i is not None:
+            ev["d1"][i].record(fwd)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(fwd)
+    for i in range(args.steps):
+        step(i)
+    t1.record(fwd)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    if world > 1:
+        tt = torch.tensor([elapsed], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed = float(tt.item())
+        dist.barrier()
+    assert L.lsc_pool_status(pool, fwd) == L.LSC_OK
+
+    rb = restore_bytes(v0, n, n_gdn, n)
+    db = n_gdn * decode_bytes(v0, w, n)
+    step_bytes = rb + db
+    t_restore = statistics.mean(ev["r0"][i].elapsed_time(ev["r1"][i]) for i in range(args.steps)) / 1e3
+    t_decode = statistics.mean(ev["d0"][i].elapsed_time(ev["d1"][i]) for i in range(args.steps)) / 1e3 / n_gdn
+    restore_gbs = rb / t_restore / 1e9
+    decode_gbs = decode_bytes(v0, w, n) / t_decode / 1e9
+    value = world * step_bytes * args.steps / elapsed / 1e9
+    rows_per_s = world * n * args.steps / elapsed
+
+    roof_restore = {"bound": "hbm", "kernel": "restore_kernel", "achieved": round(restore_gbs, 1),
+                    "peak": hbm_peak, "unit": "GB/s", "frac": round(restore_gbs / hbm_peak, 4),
+                    "traffic": kernel_traffic("restore_kernel"), "bytes_per_launch": rb,
+                    "launch_ms": round(t_restore * 1e3, 4), "peak_source": peak_src}
+    roof_decode = {"bound": "hbm", "kernel": "decode_kernel<128,f32>", "achieved": round(decode_gbs, 1),
+                   "peak": hbm_peak, "unit": "GB/s", "frac": round(decode_gbs / hbm_peak, 4),
+                   "traffic": kernel_traffic("decode_kernel<128,f32,2>"), "bytes_per_launch": decode_bytes(v0, w, n),
+                   "launch_ms": round(t_decode * 1e3, 4), "peak_source": peak_src}
+    dominant = roof_restore if t_restore >= t_decode * n_gdn else roof_decode
+
+    # end to end through the public API with host buffers: per step, H2D of the
+    # step's inputs from pinned memory, the calls, D2H of the outputs
+    e2e = e2e_serving(args, L, torch, pool, w, rows, ops, n, n_gdn, X, CW, A, B, step_bytes, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32", "data": "synthetic",
+        "config": {"workload": "c1-serving-step", "layers": "36 GDN + 12 attention", "num_slots": w.num_slots,
+                   "rows": n, "restore": "64 rows all hits x 36 GDN layers",
+                   "decode": "1 token x 64 restored rows x 36 GDN layers",
+                   "conv": "[8192,3] bf16", "ssm": "[32,128,128] f32", "page_bytes": w.page_bytes,
+                   "l2": "inputs larger than L2 (9.9 GB restore, 9.9 GB decode per step)",
+                   "parallelism": f"replicas x{world}"},
+        "rows_per_s": round(rows_per_s, 1),
+        "step_bytes": step_bytes,
+        "roofline": dominant,
+        "roofline_other": roof_decode if dominant is roof_restore else roof_restore,
+        "clocks": ck,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (1 + n_gdn),
+    }
+    L.lsc_pool_destroy(pool)
+    del buf, X, OUT
+    torch.cuda.empty_cache()
+
+    if rank == 0 and world == 1 and not args.no_parts:
+        line["parts"] = measure_parts(L, W, torch, hbm_peak)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(budget_s=12.0)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_serving(args, L, torch, pool, w, rows, ops, n, n_gdn, X, CW, A, B, step_bytes, world):
+    hx = X.cpu().pin_memory()
+    ha = A.cpu().pin_memory()
+    hb = B.cpu().pin_memory()
+    hhs = torch.from_numpy(rows.hs_prefill.copy()).pin_memory()
+    hidx = torch.from_numpy(rows.live.astype(np.int32)).pin_memory()
+    hout = torch.empty((n_gdn, n, w.num_v_heads, w.head_v_dim), pin_memory=True)
+    dx, da, db = torch.empty_like(X), torch.empty_like(A), torch.empty_like(B)
+    dhs = torch.empty(n, dtype=torch.uint8, device="cuda")
+    didx = torch.empty(n, dtype=torch.int32, device="cuda")
+    dout = torch.empty((n_gdn, n, w.num_v_heads, w.head_v_dim), device="cuda")
+    dargs = [L.decode_args(n, w.num_k_heads, didx, dhs, dx[g], CW[g], da[g], db[g], dout[g]) for g in range(n_gdn)]
+    prep = torch.cuda.Stream()
+    fwd = torch.cuda.current_stream()
+    evd = torch.cuda.Event()
+    evd.record(fwd)
+    h2d = hx.numel() * hx.element_size() + ha.numel() * 4 + hb.numel() * 4 + n + 4 * n
+    d2h = hout.numel() * 4
+
+    def step():
+        dhs.copy_(hhs, non_blocking=True)
+        didx.copy_(hidx, non_blocking=True)
+        dx.copy_(hx, non_blocking=True)
+        da.copy_(ha, non_blocking=True)
+        db.copy_(hb, non_blocking=True)
+        prep.wait_stream(fwd)
+        rc, _ = L.lsc_restore(pool, ops, rows.nkv, rows.block_size, rows.initialized, dhs, prep, evd)
+        assert rc == L.LSC_OK
+        fwd.wait_event(evd)
+        for g, l in enumerate(w.gdn_layers):
+            assert L.lsc_gdn_decode(pool, l, dargs[g], fwd) == L.LSC_OK
+        hout.copy_(dout, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([el], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        el = float(tt.item())
+    return {"value": round(world * step_bytes * args.steps / el / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(el / args.steps * 1e3, 4), "clock": "host wall clock"}
+
+
+def measure_parts(L, W, torch, hbm_peak, reps=5):
+    parts = {}
+    fwd = torch.cuda.current_stream()
+
+    def timed(fn, k):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        e0.record(fwd)
+        for _ in range(k):
+            fn()
+        e1.record(fwd)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / k
+
+    # decode step at 256 rows, bf16 state, one launch per layer over 36 layers
+    w = W.get("c2")
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    n = 256
+    rng = np.random.default_rng(0)
+    idx = torch.from_numpy(rng.permutation(w.num_slots).astype(np.int32)).cuda()
+    has = torch.ones(n, dtype=torch.uint8, device="cuda")
+    x, cw, a, b = W.decode_inputs(w, n, seed=0, layer=0)
+    X = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    CW = torch.from_numpy(cw).to(torch.bfloat16).cuda()
+    A, B = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    out = torch.empty((n, w.num_v_heads, w.head_v_dim), device="cuda")
+    da = L.decode_args(n, w.num_k_heads, idx, has, X, CW, A, B, out)
+
+    def dec_all():
+        for l in w.gdn_layers:
+            assert L.lsc_gdn_decode(pool, l, da, fwd) == L.LSC_OK
+
+    t = timed(dec_all, reps) / len(w.gdn_layers)
+    v = views[w.gdn_layers[0]]
+    bytes_ = decode_bytes(v, w, n)
+    parts["decode_c2"] = {"workload": "c2: 256 rows, ssm bf16, page +512 B, one launch per layer x 36",
+                          "kernel": "decode_kernel<128,bf16,1>", "launch_ms": round(t * 1e3, 4),
+                          "bytes_per_launch": bytes_, "GB/s": round(bytes_ / t / 1e9, 1),
+                          "frac": round(bytes_ / t / 1e9 / hbm_peak, 4), "rows_per_s": round(n / t, 1),
+                          "traffic": kernel_traffic("decode_kernel<128,bf16,1>")}
+    L.lsc_pool_destroy(pool)
+    del buf
+    torch.cuda.empty_cache()
+
+    # restore storm
+    w = W.get("c3")
+    rows = W.restore_rows("c3")
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    ops = L.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
+    hs = torch.from_numpy(rows.hs_prefill.copy()).cuda()
+    rep = {}
+
+    def storm():
+        rc, r = L.lsc_restore(pool, ops, rows.nkv, rows.block_size, rows.initialized, hs, fwd, None)
+        assert rc == L.LSC_OK
+        rep["r"] = r
+
+    t = timed(storm, reps)
+    r = rep["r"]
+    v = views[w.gdn_layers[0]]
+    bytes_ = restore_bytes(v, r.n_hit, len(w.gdn_layers), r.n_hit + r.n_miss)
+    parts["restore_c3"] = {"workload": "c3: 512 rows over 1024 slots, 205 hit / 154 miss / 153 no-op, hot source",
+                           "kernel": "restore_kernel", "launch_ms": round(t * 1e3, 4), "bytes_per_launch": bytes_,
+                           "GB/s": round(bytes_ / t / 1e9, 1), "frac": round(bytes_ / t / 1e9 / hbm_peak, 4),
+                           "rows_per_s": round(512 / t, 1)}
+    L.lsc_pool_destroy(pool)
+    del buf, hs
+    torch.cuda.empty_cache()
+
+    # resume prefill: 64 sequences, 36 layers (one input set per layer is reused
+    # across layers to bound memory; every layer has its own state)
+    w = W.get("c4")
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    lengths = W.seq_lengths(64, 64, 2048, seed=0)
+    cu, q, k, vv, a, b = W.recurrent_inputs(w, lengths, seed=0, layer=0)
+    T = int(cu[-1])
+    rng = np.random.default_rng(4)
+    idx = torch.from_numpy(rng.permutation(w.num_slots)[:64].astype(np.int32)).cuda()
+    has = torch.from_numpy((rng.random(64) < 0.5).astype(np.uint8)).cuda()
+    dev = [torch.from_numpy(z).cuda() for z in (cu, q, k, vv, a, b)]
+    out = torch.empty((T, w.num_v_heads, w.head_v_dim), device="cuda")
+    ra = L.recurrent_args(64, w.num_k_heads, T, idx, has, *dev, out)
+
+    def rec_all():
+        for l in w.gdn_layers:
+            assert L.lsc_gdn_recurrent(pool, l, ra, fwd) == L.LSC_OK
+
+    t = timed(rec_all, 2)
+    nl = len(w.gdn_layers)
+    flops = 6.0 * T * w.num_v_heads * w.head_v_dim * w.head_k_dim * nl
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    fp32_peak = sms * 128 * 2 * 2070e6
+    parts["recurrent_c4"] = {"workload": f"c4: 64 sequences, {T} tokens, 36 layers, state [32,128,128] f32",
+                             "kernel": "recurrent_kernel<128,f32>", "ms_per_36_layers": round(t * 1e3, 3),
+                             "token_layers_per_s": round(T * nl / t, 1),
+                             "TFLOP/s": round(flops / t / 1e12, 2),
+                             "roofline": {"bound": "alu", "peak_TFLOP/s": round(fp32_peak / 1e12, 1),
+                                          "frac": round(flops / t / fp32_peak, 4),
+                                          "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 flop x 2070 MHz"},
+                             "flops_basis": "6 dk dv per (token, head): S k, the rank-1 update, S q"}
+    L.lsc_pool_destroy(pool)
+    del buf, out, dev
+    torch.cuda.empty_cache()
+    return parts
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(n_rows=None, seed=0):
+    """A bounded sample of the serving step on the host: the same pages, shapes
+    and layers as the c1 step, with n_rows restore+decode rows (2 n_rows slots);
+    by default one row per host thread (the oracle parallelises over rows)."""
+    import oracle
+    from linear_attention_state_lsc_gb300 import workloads as W
+    if n_rows is None:
+        n_rows = max(1, min(16, oracle.num_threads()))
+    w = W.get("c1")
+    w.num_slots = 2 * n_rows
+    kinds = [oracle.GDN if k == W.GDN else oracle.ATTENTION for k in w.layers]
+    pool = oracle.Pool(kinds, w.num_slots, w.conv_dim, w.conv_width, oracle.BF16, w.num_v_heads,
+                       w.head_v_dim, w.head_k_dim, oracle.F32, w.page_bytes)
+    _, Lo = oracle.layout(pool)
+    regions = {}
+    rng = np.random.default_rng(seed)
+    for l in w.gdn_layers:
+        regions[l] = rng.integers(0, 256, w.num_slots * w.page_bytes, dtype=np.uint8)
+        pages = regions[l].reshape(w.num_slots, w.page_bytes)
+        vals = rng.standard_normal((w.num_slots, Lo["ssm_elems"]), dtype=np.float32)
+        pages[:, Lo["ssm_offset"]:Lo["ssm_offset"] + Lo["ssm_bytes"]] = vals.view(np.uint8).reshape(w.num_slots, -1)
+        conv = W.to_dtype_bytes(rng.standard_normal((w.num_slots, Lo["conv_elems"]), dtype=np.float32), W.BF16)
+        pages[:, :Lo["conv_bytes"]] = conv
+    live = np.arange(n_rows, dtype=np.int32)
+    src = np.arange(n_rows, 2 * n_rows, dtype=np.int32)
+    nkv = np.full(n_rows, 64, np.int32)
+    init = np.zeros(n_rows, np.uint8)
+    inputs = [W.decode_inputs(w, n_rows, seed=seed, layer=l) for l in w.gdn_layers]
+    inputs = [(W.to_dtype_bytes(x, W.BF16), W.to_dtype_bytes(cw, W.BF16), a, b) for x, cw, a, b in inputs]
+    per_row = 2 * len(w.gdn_layers) * (Lo["conv_bytes"] + Lo["ssm_bytes"]) + 1
+    dec_row = 2 * (Lo["conv_bytes"] + Lo["ssm_bytes"]) + w.conv_dim * 2 + 2 * w.num_v_heads * 4 + \
+        w.num_v_heads * w.head_v_dim * 4 + 5
+    step_bytes = n_rows * per_row + len(w.gdn_layers) * (n_rows * dec_row + w.conv_dim * w.conv_width * 2)
+
+    def run():
+        hs = (nkv > 0).astype(np.uint8)
+        rc = oracle.restore(pool, regions, live, src, nkv, 64, init, hs)
+        assert rc == oracle.OK
+        for g, l in enumerate(w.gdn_layers):
+            x, cw, a, b = inputs[g]
+            rc, _ = oracle.gdn_decode(pool, regions[l], live, hs, x, cw, w.num_k_heads, a, b)
+            assert rc == oracle.OK
+
+    return run, step_bytes, n_rows, min(n_rows, oracle.num_threads())
+
+
+def cpu_baseline(budget_s=12.0):
+    import oracle.build as ob
+    ob.build()
+    run, step_bytes, n_rows, threads = oracle_sample()
+    run()
+    t = time.perf_counter()
+    k = 0
+    while time.perf_counter() - t < budget_s:
+        run()
+        k += 1
+    el = time.perf_counter() - t
+    return {"value": round(step_bytes * k / el / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "rows_per_s": round(n_rows * k / el, 3),
+            "sample": f"c1 serving step on {n_rows} rows (restore x 36 GDN layers + 36 decode layers), "
+                      f"{k} repetitions in {el:.1f} s, OpenMP over rows"}
+
+
+def run_reference(args):
+    rank, local, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo", init_method="env://")
+        if rank != 0:
+            dist.barrier()
+            dist.destroy_process_group()
+            return
+    import oracle.build as ob
+    ob.build()
+    run, step_bytes, n_rows, threads = oracle_sample()
+    for _ in range(args.warmup):
+        run()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    el = time.perf_counter() - t
+    value = step_bytes * args.steps / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic",
+            "config": {"workload": "c1-serving-step", "sample_rows": n_rows, "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"c1 serving step restricted to {n_rows} rows per step"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_lsc(a)

@@ -1,0 +1,200 @@
+// lsc_copy.cu -- byte-moving kernels of liblsc: the persistent cross-layer
+// restore, and the strided gather / scatter of slot state.
+//
+// Sources, cited by page title and section:
+//   [XN] "Linear-State Prefix Cache 内部机制" §4.1, §4.3 (restore copy and the
+//        has_initial_state write)
+//   [VA] "非连续 KV Cache" §3 (page stride, padding skipped by stride), §4-§5
+//        (gather_ssm_states / scatter_ssm_states_)
+//
+// All three kernels are HBM-bound copies.  They move 16-byte vectors with
+// coalesced loads and streaming stores, never touch bytes outside the conv and
+// ssm views of a page, and run as persistent grids sized from the SM count.
+#include <cuda_runtime.h>
+
+#include "lsc_internal.h"
+
+namespace lsc {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 8;  // 16 B vectors in flight per thread
+
+__device__ __forceinline__ void report(int32_t *status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Block-cooperative copy of nvec 16 B vectors: every thread issues kUnroll
+// loads before its stores, so a CTA keeps kThreads * kUnroll * 16 B in flight.
+__device__ __forceinline__ void copy_vec16(uint4 *__restrict__ d, const uint4 *__restrict__ s,
+                                           int64_t nvec) {
+  int64_t i = threadIdx.x;
+  const int64_t stride = blockDim.x;
+  for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) r[k] = __ldg(s + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) __stcs(d + i + k * stride, r[k]);
+  }
+  for (; i < nvec; i += stride) __stcs(d + i, __ldg(s + i));
+}
+
+// Copy len bytes with the widest access the two addresses allow; the tail that
+// does not fill a vector is copied byte by byte and stops exactly at len.
+__device__ __forceinline__ void copy_span(uint8_t *dst, const uint8_t *src, int64_t len) {
+  const uintptr_t a = (uintptr_t)dst | (uintptr_t)src;
+  int64_t done = 0;
+  if ((a & 15) == 0) {
+    const int64_t nv = len >> 4;
+    copy_vec16((uint4 *)dst, (const uint4 *)src, nv);
+    done = nv << 4;
+  } else if ((a & 3) == 0) {
+    const int64_t nw = len >> 2;
+    for (int64_t i = threadIdx.x; i < nw; i += blockDim.x)
+      ((uint32_t *)dst)[i] = __ldg((const uint32_t *)src + i);
+    done = nw << 2;
+  }
+  for (int64_t i = done + threadIdx.x; i < len; i += blockDim.x) dst[i] = src[i];
+}
+
+__device__ __forceinline__ void zero_span(uint8_t *dst, int64_t len) {
+  int64_t done = 0;
+  if (((uintptr_t)dst & 15) == 0) {
+    const int64_t nv = len >> 4;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) __stcs((uint4 *)dst + i, z);
+    done = nv << 4;
+  }
+  for (int64_t i = done + threadIdx.x; i < len; i += blockDim.x) dst[i] = 0;
+}
+
+// Persistent restore: one launch covers every (hit row, GDN layer, chunk) work
+// unit of the plan, plus the has_initial_state writes of the plan's rows.
+// Consecutive units are consecutive chunks of one page, so at any moment the
+// grid streams a contiguous stretch of each source page.
+__global__ void __launch_bounds__(kThreads) restore_kernel(const __grid_constant__ RestorePlan p) {
+  const int gthreads = gridDim.x * blockDim.x;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < p.n_hs; j += gthreads) {
+    const int32_t e = p.hs_ops[j];
+    p.hs[e >> 1] = (uint8_t)(e & 1);
+  }
+  const int64_t per_hit = (int64_t)p.num_gdn * p.chunks_per_slot;
+  const int64_t total = (int64_t)p.n_hits * per_hit;
+  for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
+    const int h = (int)(u / per_hit);
+    const int64_t rem = u - (int64_t)h * per_hit;
+    const int g = (int)(rem / p.chunks_per_slot);
+    int c = (int)(rem - (int64_t)g * p.chunks_per_slot);
+    const int s = c >= p.seg_chunks[0] ? 1 : 0;
+    if (s) c -= p.seg_chunks[0];
+    const int64_t off = p.seg_off[s] + (int64_t)c * p.chunk_bytes;
+    const int64_t left = p.seg_len[s] - (int64_t)c * p.chunk_bytes;
+    const int64_t len = left < p.chunk_bytes ? left : p.chunk_bytes;
+    uint8_t *layer = p.base + (int64_t)g * p.region_bytes;
+    const int2 hs = p.hit[h];
+    copy_span(layer + (int64_t)hs.x * p.page + off, layer + (int64_t)hs.y * p.page + off, len);
+  }
+}
+
+// Gather: unit = (row, chunk of the conv view or of the ssm view).
+__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ AccessParams p) {
+  const int cps = p.conv_chunks + p.ssm_chunks;
+  const int64_t total = (int64_t)p.n * cps;
+  for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
+    const int i = (int)(u / cps);
+    const int c = (int)(u - (int64_t)i * cps);
+    const int32_t slot = p.idx[i];
+    bool warm = slot >= 0 && (p.has_init == nullptr || p.has_init[i] != 0);
+    if (slot >= p.num_slots) {
+      warm = false;
+      if (threadIdx.x == 0 && c == 0) report(p.status, LSC_ERR_OUT_OF_RANGE);
+    }
+    int64_t off, len, page_off;
+    uint8_t *dst;
+    if (c < p.conv_chunks) {
+      off = (int64_t)c * p.chunk_bytes;
+      len = p.conv_bytes - off < p.chunk_bytes ? p.conv_bytes - off : p.chunk_bytes;
+      dst = p.conv_dense + (int64_t)i * p.conv_bytes + off;
+      page_off = off;
+    } else {
+      off = (int64_t)(c - p.conv_chunks) * p.chunk_bytes;
+      len = p.ssm_bytes - off < p.chunk_bytes ? p.ssm_bytes - off : p.chunk_bytes;
+      dst = p.ssm_dense + (int64_t)i * p.ssm_bytes + off;
+      page_off = p.ssm_off + off;
+    }
+    if (warm) copy_span(dst, p.layer + (int64_t)slot * p.page + page_off, len);
+    else zero_span(dst, len);
+  }
+}
+
+// Scatter: the inverse; negative or out-of-range indices write nothing.
+__global__ void __launch_bounds__(kThreads) scatter_kernel(const __grid_constant__ AccessParams p) {
+  const int cps = p.conv_chunks + p.ssm_chunks;
+  const int64_t total = (int64_t)p.n * cps;
+  for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
+    const int i = (int)(u / cps);
+    const int c = (int)(u - (int64_t)i * cps);
+    const int32_t slot = p.idx[i];
+    if (slot < 0) continue;
+    if (slot >= p.num_slots) {
+      if (threadIdx.x == 0 && c == 0) report(p.status, LSC_ERR_OUT_OF_RANGE);
+      continue;
+    }
+    int64_t off, len, page_off;
+    const uint8_t *src;
+    if (c < p.conv_chunks) {
+      off = (int64_t)c * p.chunk_bytes;
+      len = p.conv_bytes - off < p.chunk_bytes ? p.conv_bytes - off : p.chunk_bytes;
+      src = p.conv_dense + (int64_t)i * p.conv_bytes + off;
+      page_off = off;
+    } else {
+      off = (int64_t)(c - p.conv_chunks) * p.chunk_bytes;
+      len = p.ssm_bytes - off < p.chunk_bytes ? p.ssm_bytes - off : p.chunk_bytes;
+      src = p.ssm_dense + (int64_t)i * p.ssm_bytes + off;
+      page_off = p.ssm_off + off;
+    }
+    copy_span(p.layer + (int64_t)slot * p.page + page_off, src, len);
+  }
+}
+
+int blocks_per_sm(const void *kernel) {
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess || b < 1) {
+    cudaGetLastError();
+    b = 1;
+  }
+  return b;
+}
+
+int grid_for(const void *kernel, int num_sms, int64_t units) {
+  static int cached[3] = {0, 0, 0};
+  const int slot = kernel == (const void *)restore_kernel ? 0 : kernel == (const void *)gather_kernel ? 1 : 2;
+  if (!cached[slot]) cached[slot] = blocks_per_sm(kernel);
+  int64_t g = (int64_t)num_sms * cached[slot];
+  if (units < g) g = units;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+int restore_grid(int num_sms) { return grid_for((const void *)restore_kernel, num_sms, 1LL << 40); }
+
+cudaError_t launch_restore(const RestorePlan &plan, int grid, cudaStream_t stream) {
+  restore_kernel<<<grid, kThreads, 0, stream>>>(plan);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const AccessParams &p, int num_sms, cudaStream_t stream) {
+  const int64_t units = (int64_t)p.n * (p.conv_chunks + p.ssm_chunks);
+  gather_kernel<<<grid_for((const void *)gather_kernel, num_sms, units), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const AccessParams &p, int num_sms, cudaStream_t stream) {
+  const int64_t units = (int64_t)p.n * (p.conv_chunks + p.ssm_chunks);
+  scatter_kernel<<<grid_for((const void *)scatter_kernel, num_sms, units), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace lsc

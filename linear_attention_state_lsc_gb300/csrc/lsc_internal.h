@@ -1,0 +1,98 @@
+// lsc_internal.h -- shared between the host code and the kernels of liblsc.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lsc.h"
+
+namespace lsc {
+
+// Byte geometry of one GDN layer region; the same for every GDN layer.
+struct Geom {
+  uint8_t *base;         // pool base (GDN layer g starts at base + g * region_bytes)
+  int64_t page;          // physical page stride
+  int64_t region_bytes;  // num_slots * page
+  int64_t conv_bytes;    // conv view bytes, at page offset 0
+  int64_t ssm_off;       // ssm view page offset (16 B aligned)
+  int64_t ssm_bytes;
+  int32_t num_slots;
+  int32_t num_gdn;
+  int32_t conv_dim, conv_width, conv_dtype;
+  int32_t Hv, dv, dk, ssm_dtype;
+  int32_t *status;       // device error word
+};
+
+// ---- restore -------------------------------------------------------------
+// The whole plan travels as one by-value kernel parameter (<= 32764 bytes), so
+// the call needs no staging buffer and no host sync.
+constexpr int kPlanMaxHits = 2048;
+constexpr int kPlanMaxHs = 3584;
+
+struct RestorePlan {
+  uint8_t *base;
+  uint8_t *hs;             // device has_initial_state
+  int64_t region_bytes;
+  int64_t page;
+  int64_t seg_off[2];      // copied byte ranges of a page
+  int64_t seg_len[2];
+  int64_t chunk_bytes;     // work-unit size
+  int32_t seg_chunks[2];   // work units per segment
+  int32_t chunks_per_slot;
+  int32_t num_gdn;
+  int32_t n_hits;
+  int32_t n_hs;
+  int2 hit[kPlanMaxHits];  // (dst slot, src slot)
+  int32_t hs_ops[kPlanMaxHs];  // (row << 1) | value
+};
+static_assert(sizeof(RestorePlan) <= 32000, "restore plan exceeds the kernel parameter limit");
+
+cudaError_t launch_restore(const RestorePlan &plan, int grid, cudaStream_t stream);
+int restore_grid(int num_sms);
+
+// ---- gather / scatter ------------------------------------------------------
+struct AccessParams {
+  uint8_t *layer;          // region base of the GDN layer
+  int64_t page, conv_bytes, ssm_off, ssm_bytes, chunk_bytes;
+  int32_t num_slots, n, conv_chunks, ssm_chunks;
+  const int32_t *idx;
+  const uint8_t *has_init; // gather only, may be null
+  uint8_t *conv_dense;
+  uint8_t *ssm_dense;
+  int32_t *status;
+};
+cudaError_t launch_gather(const AccessParams &p, int num_sms, cudaStream_t stream);
+cudaError_t launch_scatter(const AccessParams &p, int num_sms, cudaStream_t stream);
+
+// ---- GDN decode and recurrence ----------------------------------------------
+struct DecodeParams {
+  uint8_t *layer;
+  int64_t page, ssm_off;
+  int32_t num_slots, conv_dim, conv_width, conv_bf16;
+  int32_t Hk, Hv, dv, group;
+  int32_t n;
+  const int32_t *idx;
+  const uint8_t *has_init;
+  const void *x;
+  const void *w;
+  const float *alpha, *beta;
+  float *out;
+  int32_t *status;
+};
+// returns LSC_OK, LSC_ERR_UNSUPPORTED or LSC_ERR_CUDA
+int launch_decode(const DecodeParams &p, int dk, int ssm_dtype, cudaStream_t stream);
+
+struct RecurrentParams {
+  uint8_t *layer;
+  int64_t page, ssm_off;
+  int32_t num_slots, Hk, Hv, dv, group, n_seq, total_tokens;
+  const int32_t *idx;
+  const uint8_t *has_init;
+  const int32_t *cu;
+  const float *q, *k, *v, *alpha, *beta;
+  float *out;
+  int32_t *status;
+};
+int launch_recurrent(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
+
+}  // namespace lsc

@@ -1,0 +1,276 @@
+"""ctypes binding of liblsc (include/lsc.h), same names as the C ABI.
+
+Argument marshalling only: every step of the hot path runs in the CUDA kernels
+of liblsc.so.  Pointers are plain integers; torch tensors, numpy arrays and
+None (NULL) are accepted wherever a pointer is expected.  Loading fails loudly
+when liblsc.so has not been built -- there is no fallback.
+"""
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblsc.so")
+
+# return codes (include/lsc.h)
+LSC_OK = 0
+LSC_SOFT_COLD = 1
+LSC_ERR_INVALID_ARG = -1
+LSC_ERR_OUT_OF_RANGE = -2
+LSC_ERR_DUP_DST = -3
+LSC_ERR_SRC_IS_DST = -4
+LSC_ERR_MISALIGNED = -5
+LSC_ERR_STATELESS_LAYER = -6
+LSC_ERR_UNSUPPORTED = -7
+LSC_ERR_CUDA = -8
+LSC_ERR_DEV_TIMEOUT = -9
+LSC_ERR_NO_MEMORY = -10
+LSC_ERR_LAYOUT = -11
+LSC_ERR_WRONG_DEVICE = -12
+
+LSC_LAYER_ATTENTION, LSC_LAYER_GDN = 0, 1
+LSC_F32, LSC_BF16, LSC_F16 = 0, 1, 2
+
+
+class LscError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        super().__init__(f"{what}: {lsc_error_string(code)} ({code})")
+
+
+class LinearStateCacheOp(C.Structure):
+    _fields_ = [("linear_state_id", C.c_int32), ("restore_src_slot_id", C.c_int32),
+                ("restore_prefix_hash", C.c_uint64), ("save_prefix_hash", C.c_uint64),
+                ("save_dst_slot_id", C.c_int32), ("reserved", C.c_int32)]
+
+
+# numpy view of an array of LinearStateCacheOp (same layout, 32 bytes)
+OP_DTYPE = np.dtype([("linear_state_id", "<i4"), ("restore_src_slot_id", "<i4"),
+                     ("restore_prefix_hash", "<u8"), ("save_prefix_hash", "<u8"),
+                     ("save_dst_slot_id", "<i4"), ("reserved", "<i4")], align=True)
+
+
+class lsc_pool_desc(C.Structure):
+    _fields_ = [("num_layers", C.c_int32), ("layer_kinds", C.POINTER(C.c_int32)),
+                ("num_slots", C.c_int32), ("conv_dim", C.c_int32), ("conv_width", C.c_int32),
+                ("conv_dtype", C.c_int32), ("num_v_heads", C.c_int32), ("head_v_dim", C.c_int32),
+                ("head_k_dim", C.c_int32), ("ssm_dtype", C.c_int32), ("page_bytes", C.c_int64)]
+
+
+class lsc_layer_view(C.Structure):
+    _fields_ = [("region", C.c_void_p), ("region_bytes", C.c_int64), ("gdn_index", C.c_int32),
+                ("conv_dtype", C.c_int32), ("ssm_dtype", C.c_int32),
+                ("conv", C.c_void_p), ("conv_shape", C.c_int64 * 3), ("conv_strides", C.c_int64 * 3),
+                ("conv_storage_offset", C.c_int64),
+                ("ssm", C.c_void_p), ("ssm_shape", C.c_int64 * 4), ("ssm_strides", C.c_int64 * 4),
+                ("ssm_storage_offset", C.c_int64),
+                ("page_bytes", C.c_int64), ("payload_bytes", C.c_int64), ("conv_bytes", C.c_int64),
+                ("ssm_offset_bytes", C.c_int64), ("ssm_bytes", C.c_int64)]
+
+
+class lsc_restore_report(C.Structure):
+    _fields_ = [("n_hit", C.c_int32), ("n_miss", C.c_int32), ("n_noop", C.c_int32),
+                ("soft_cold", C.c_int32), ("launches", C.c_int32), ("reserved", C.c_int32),
+                ("bytes_copied", C.c_int64)]
+
+
+class lsc_gdn_decode_args(C.Structure):
+    _fields_ = [("n", C.c_int32), ("num_k_heads", C.c_int32), ("idx", C.c_void_p),
+                ("has_init", C.c_void_p), ("x", C.c_void_p), ("conv_weight", C.c_void_p),
+                ("alpha", C.c_void_p), ("beta", C.c_void_p), ("out", C.c_void_p)]
+
+
+class lsc_gdn_recurrent_args(C.Structure):
+    _fields_ = [("n_seq", C.c_int32), ("num_k_heads", C.c_int32), ("total_tokens", C.c_int32),
+                ("reserved", C.c_int32), ("idx", C.c_void_p), ("has_init", C.c_void_p),
+                ("cu_seqlens", C.c_void_p), ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p),
+                ("alpha", C.c_void_p), ("beta", C.c_void_p), ("out", C.c_void_p)]
+
+
+_lib = None
+
+
+def load():
+    """Load liblsc.so (built by __graft_entry__.build()); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"liblsc.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = C.CDLL(LIB_PATH)
+    P, I32, I64 = C.c_void_p, C.c_int32, C.c_int64
+    sig = {
+        "lsc_pool_required_bytes": ([C.POINTER(lsc_pool_desc), C.POINTER(C.c_size_t)], C.c_int),
+        "lsc_pool_create": ([C.POINTER(lsc_pool_desc), P, C.c_size_t, C.POINTER(P)], C.c_int),
+        "lsc_pool_destroy": ([P], C.c_int),
+        "lsc_pool_layer_view": ([P, I32, C.POINTER(lsc_layer_view)], C.c_int),
+        "lsc_pool_num_slots": ([P], I32),
+        "lsc_pool_status": ([P, P, C.POINTER(I32)], C.c_int),
+        "lsc_restore_classify": ([P, P, I32, P, I32, P, P, C.POINTER(lsc_restore_report)], C.c_int),
+        "lsc_restore": ([P, P, I32, P, I32, P, P, P, P, C.POINTER(lsc_restore_report)], C.c_int),
+        "lsc_gather": ([P, I32, P, P, I32, P, P, P], C.c_int),
+        "lsc_scatter": ([P, I32, P, I32, P, P, P], C.c_int),
+        "lsc_gdn_decode": ([P, I32, C.POINTER(lsc_gdn_decode_args), P], C.c_int),
+        "lsc_gdn_recurrent": ([P, I32, C.POINTER(lsc_gdn_recurrent_args), P], C.c_int),
+        "lsc_error_string": ([C.c_int], C.c_char_p),
+        "lsc_build_info": ([], C.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def ptr(x):
+    """Integer address of a tensor / array / int; None -> 0 (NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr() or None
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(type(x))
+
+
+def _stream(s):
+    if s is None or isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None  # torch.cuda.Stream
+
+
+def _event(e):
+    if e is None or isinstance(e, int):
+        return e or None
+    return e.cuda_event or None  # torch.cuda.Event (must have been created/recorded once)
+
+
+def lsc_error_string(code):
+    return load().lsc_error_string(int(code)).decode()
+
+
+def lsc_build_info():
+    return load().lsc_build_info().decode()
+
+
+def make_pool_desc(layer_kinds, num_slots, conv_dim, conv_width, conv_dtype, num_v_heads,
+                   head_v_dim, head_k_dim, ssm_dtype, page_bytes):
+    kinds = (C.c_int32 * len(layer_kinds))(*layer_kinds)
+    d = lsc_pool_desc(len(layer_kinds), kinds, num_slots, conv_dim, conv_width, conv_dtype,
+                      num_v_heads, head_v_dim, head_k_dim, ssm_dtype, page_bytes)
+    d._keep = kinds
+    return d
+
+
+def lsc_pool_required_bytes(desc):
+    n = C.c_size_t(0)
+    rc = load().lsc_pool_required_bytes(C.byref(desc), C.byref(n))
+    if rc < 0:
+        raise LscError(rc, "lsc_pool_required_bytes")
+    return n.value
+
+
+def lsc_pool_create(desc, device_base=None, base_bytes=0):
+    """Returns (rc, pool handle or None)."""
+    h = C.c_void_p()
+    rc = load().lsc_pool_create(C.byref(desc), ptr(device_base), base_bytes, C.byref(h))
+    return rc, (h.value if rc == LSC_OK else None)
+
+
+def lsc_pool_destroy(pool):
+    return load().lsc_pool_destroy(pool)
+
+
+def lsc_pool_layer_view(pool, layer):
+    v = lsc_layer_view()
+    rc = load().lsc_pool_layer_view(pool, layer, C.byref(v))
+    return rc, v
+
+
+def lsc_pool_num_slots(pool):
+    return load().lsc_pool_num_slots(pool)
+
+
+def lsc_pool_status(pool, stream=None):
+    s = C.c_int32(0)
+    rc = load().lsc_pool_status(pool, _stream(stream), C.byref(s))
+    if rc < 0:
+        raise LscError(rc, "lsc_pool_status")
+    return s.value
+
+
+def ops_array(live, src, restore_hash=None, save_hash=None, save_slot=None):
+    """numpy array of LinearStateCacheOp records."""
+    n = len(live)
+    a = np.zeros(n, OP_DTYPE)
+    a["linear_state_id"] = live
+    a["restore_src_slot_id"] = src
+    a["restore_prefix_hash"] = 0 if restore_hash is None else restore_hash
+    a["save_prefix_hash"] = 0 if save_hash is None else save_hash
+    a["save_dst_slot_id"] = -1 if save_slot is None else save_slot
+    return a
+
+
+def _host(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def lsc_restore_classify(pool, ops, n_kv_cache_tokens, block_size, linear_state_initialized):
+    """Returns (rc, actions int8 [n] (0 no-op, 1 hit, 2 miss), lsc_restore_report)."""
+    assert ops.dtype == OP_DTYPE
+    nkv = _host(n_kv_cache_tokens, np.int32)
+    init = _host(linear_state_initialized, np.uint8)
+    act = np.zeros(len(ops), np.int8)
+    rep = lsc_restore_report()
+    rc = load().lsc_restore_classify(pool, ops.ctypes.data, len(ops), nkv.ctypes.data, block_size,
+                                     init.ctypes.data, act.ctypes.data, C.byref(rep))
+    return rc, act, rep
+
+
+def lsc_restore(pool, ops, n_kv_cache_tokens, block_size, linear_state_initialized,
+                has_initial_state, prepare_stream=None, done_event=None):
+    """ops / n_kv / initialized on the host; has_initial_state a device uint8
+    tensor (pre-filled).  Returns (rc, lsc_restore_report)."""
+    assert ops.dtype == OP_DTYPE
+    ops = np.ascontiguousarray(ops)
+    nkv = _host(n_kv_cache_tokens, np.int32)
+    init = _host(linear_state_initialized, np.uint8)
+    rep = lsc_restore_report()
+    rc = load().lsc_restore(pool, ops.ctypes.data, len(ops), nkv.ctypes.data, block_size,
+                            init.ctypes.data, ptr(has_initial_state), _stream(prepare_stream),
+                            _event(done_event), C.byref(rep))
+    return rc, rep
+
+
+def lsc_gather(pool, layer, idx, has_init, n, conv_dense, ssm_dense, stream=None):
+    return load().lsc_gather(pool, layer, ptr(idx), ptr(has_init), n, ptr(conv_dense),
+                             ptr(ssm_dense), _stream(stream))
+
+
+def lsc_scatter(pool, layer, idx, n, conv_dense, ssm_dense, stream=None):
+    return load().lsc_scatter(pool, layer, ptr(idx), n, ptr(conv_dense), ptr(ssm_dense),
+                              _stream(stream))
+
+
+def decode_args(n, num_k_heads, idx, has_init, x, conv_weight, alpha, beta, out):
+    return lsc_gdn_decode_args(n, num_k_heads, ptr(idx), ptr(has_init), ptr(x), ptr(conv_weight),
+                               ptr(alpha), ptr(beta), ptr(out))
+
+
+def lsc_gdn_decode(pool, layer, args, stream=None):
+    return load().lsc_gdn_decode(pool, layer, C.byref(args), _stream(stream))
+
+
+def recurrent_args(n_seq, num_k_heads, total_tokens, idx, has_init, cu_seqlens, q, k, v, alpha,
+                   beta, out):
+    return lsc_gdn_recurrent_args(n_seq, num_k_heads, total_tokens, 0, ptr(idx), ptr(has_init),
+                                  ptr(cu_seqlens), ptr(q), ptr(k), ptr(v), ptr(alpha), ptr(beta),
+                                  ptr(out))
+
+
+def lsc_gdn_recurrent(pool, layer, args, stream=None):
+    return load().lsc_gdn_recurrent(pool, layer, C.byref(args), _stream(stream))

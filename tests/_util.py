@@ -67,3 +67,19 @@ def payload_mask(w: W.Workload, L):
     for off, n, dt in views(w, L):
         m[off:off + n * W.ESIZE[dt]] = True
     return m
+
+
+LDT = {W.F32: 0, W.BF16: 1, W.F16: 2}
+
+
+def lib_desc(w: W.Workload, layers=None):
+    """Library pool description of a workload (include/lsc.h lsc_pool_desc)."""
+    from linear_attention_state_lsc_gb300 import lsc
+    kinds = [lsc.LSC_LAYER_GDN if k == W.GDN else lsc.LSC_LAYER_ATTENTION for k in (layers or w.layers)]
+    return lsc.make_pool_desc(kinds, w.num_slots, w.conv_dim, w.conv_width, LDT[w.conv_dtype],
+                              w.num_v_heads, w.head_v_dim, w.head_k_dim, LDT[w.ssm_dtype], w.page_bytes)
+
+
+def ops_of(rows):
+    from linear_attention_state_lsc_gb300 import lsc
+    return lsc.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)

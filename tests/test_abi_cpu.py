@@ -1,0 +1,242 @@
+"""C-ABI checks that need no GPU: the library loads and exports every symbol the
+header declares, the struct layouts agree, and the host logic (layout, views,
+row classification, validation, error codes, the layout log) matches the
+oracle.  No call here enqueues device work."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from linear_attention_state_lsc_gb300 import lsc as L
+from linear_attention_state_lsc_gb300 import workloads as W
+
+from _util import lib_desc, oracle_layout, oracle_pool, ops_of
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lsc.h")
+FAKE_BASE = 1 << 40  # 256 B aligned, never dereferenced: host-only pools
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lsc_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lsc):
+    names = declared_functions()
+    assert len(names) >= 14
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (lsc_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_struct_layouts(lsc):
+    assert ctypes.sizeof(L.LinearStateCacheOp) == 32 == L.OP_DTYPE.itemsize
+    assert L.OP_DTYPE.fields["save_dst_slot_id"][1] == ctypes.sizeof(ctypes.c_int32) * 2 + 16
+    assert ctypes.sizeof(L.lsc_restore_report) == 32
+    assert "sm_103a" in L.lsc_build_info()
+
+
+def test_error_strings(lsc):
+    for code in range(-12, 2):
+        s = L.lsc_error_string(code)
+        assert s and s != "unknown error", code
+    assert L.lsc_error_string(-99) == "unknown error"
+
+
+def host_pool(w, layers=None):
+    rc, pool = L.lsc_pool_create(lib_desc(w, layers), FAKE_BASE, 1 << 44)
+    assert rc == L.LSC_OK, L.lsc_error_string(rc)
+    return pool
+
+
+@pytest.mark.parametrize("name", ["c0", "c0p", "c1", "c2", "c3", "s1", "s2", "s3", "s4"])
+def test_layer_views_match_oracle_layout(lsc, name):
+    w = W.get(name) if name.startswith("c") else W.small(name)
+    Lo = oracle_layout(w)
+    pool = host_pool(w)
+    esc, ess = W.ESIZE[w.conv_dtype], W.ESIZE[w.ssm_dtype]
+    assert L.lsc_pool_required_bytes(lib_desc(w)) == Lo["num_gdn"] * Lo["region_bytes"]
+    g = 0
+    for l, kind in enumerate(w.layers):
+        rc, v = L.lsc_pool_layer_view(pool, l)
+        if kind == W.ATTN:
+            assert rc == L.LSC_ERR_STATELESS_LAYER
+            continue
+        assert rc == L.LSC_OK
+        assert v.gdn_index == g
+        assert v.region == FAKE_BASE + g * Lo["region_bytes"]
+        assert v.region_bytes == Lo["region_bytes"]
+        assert list(v.conv_shape) == [w.num_slots, w.conv_dim, w.conv_width - 1]
+        assert list(v.conv_strides) == [Lo["conv_stride_elems"], w.conv_width - 1, 1]
+        assert list(v.ssm_shape) == [w.num_slots, w.num_v_heads, w.head_v_dim, w.head_k_dim]
+        assert list(v.ssm_strides) == [Lo["ssm_stride_elems"], w.head_v_dim * w.head_k_dim, w.head_k_dim, 1]
+        assert v.ssm - v.region == Lo["ssm_offset"] and v.ssm_storage_offset * ess == Lo["ssm_offset"]
+        assert v.conv == v.region and v.conv_storage_offset == 0
+        assert v.payload_bytes == Lo["payload"] and v.conv_bytes == Lo["conv_bytes"]
+        assert v.ssm_bytes == Lo["ssm_bytes"]
+        g += 1
+    assert L.lsc_pool_layer_view(pool, len(w.layers))[0] == L.LSC_ERR_OUT_OF_RANGE
+    assert L.lsc_pool_num_slots(pool) == w.num_slots
+    assert L.lsc_pool_destroy(pool) == L.LSC_OK
+
+
+def test_worked_block_stride_example_through_the_library(lsc):
+    """vLLM-Ascend "非连续 KV Cache" §3.4: a 48-element fp16 view in a 128 B page
+    has a slot stride of 64 elements."""
+    d = L.make_pool_desc([L.LSC_LAYER_GDN], 4, 16, 4, L.LSC_F16, 1, 2, 2, L.LSC_F32, 128)
+    rc, pool = L.lsc_pool_create(d, FAKE_BASE, 4 * 128)
+    assert rc == L.LSC_OK
+    rc, v = L.lsc_pool_layer_view(pool, 0)
+    assert rc == L.LSC_OK
+    assert v.conv_strides[0] == 64 and v.conv_shape[1] * v.conv_shape[2] == 48
+    assert v.ssm_strides[0] == 32
+    L.lsc_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("page,code", [(100, L.LSC_ERR_LAYOUT), (130, L.LSC_ERR_LAYOUT), (136, L.LSC_ERR_MISALIGNED)])
+def test_pool_rejects_bad_pages(lsc, page, code):
+    d = L.make_pool_desc([L.LSC_LAYER_GDN], 4, 16, 4, L.LSC_F16, 1, 2, 2, L.LSC_F32, page)
+    assert L.lsc_pool_create(d, FAKE_BASE, 1 << 20)[0] == code
+
+
+def test_pool_rejects_bad_base_and_args(lsc):
+    w = W.get("c0")
+    assert L.lsc_pool_create(lib_desc(w), FAKE_BASE + 8, 1 << 20)[0] == L.LSC_ERR_MISALIGNED
+    assert L.lsc_pool_create(lib_desc(w), FAKE_BASE, 100)[0] == L.LSC_ERR_NO_MEMORY
+    bad = lib_desc(w)
+    bad.conv_width = 1
+    assert L.lsc_pool_create(bad, FAKE_BASE, 1 << 20)[0] == L.LSC_ERR_INVALID_ARG
+    bad = lib_desc(w)
+    bad.ssm_dtype = 7
+    assert L.lsc_pool_create(bad, FAKE_BASE, 1 << 20)[0] == L.LSC_ERR_INVALID_ARG
+
+
+def _classify_both(w, rows, layers=None):
+    pool = host_pool(w, layers)
+    rc_l, act_l, rep = L.lsc_restore_classify(pool, ops_of(rows), rows.nkv, rows.block_size, rows.initialized)
+    rc_o, act_o = oracle.classify(oracle_pool(w, layers), rows.live, rows.src, rows.nkv, rows.block_size,
+                                  rows.initialized)
+    L.lsc_pool_destroy(pool)
+    return rc_l, act_l, rep, rc_o, act_o
+
+
+@pytest.mark.parametrize("case", ["combos", "c0", "c1", "c3"])
+def test_classification_matches_oracle(lsc, case):
+    if case == "combos":
+        w = W.get("c0")
+        w.num_slots = 40
+        rows = W.combo_rows(40, 16, seed=9)
+    else:
+        w = W.get(case)
+        rows = W.restore_rows(case)
+    rc_l, act_l, rep, rc_o, act_o = _classify_both(w, rows)
+    assert rc_l == L.LSC_OK and rc_o == oracle.OK
+    np.testing.assert_array_equal(act_l, act_o)  # both use 0 no-op, 1 hit, 2 miss
+    assert rep.n_hit == (act_o == oracle.HIT).sum() and rep.n_miss == (act_o == oracle.MISS).sum()
+    assert rep.n_noop == (act_o == oracle.NOOP).sum()
+    Lo = oracle_layout(w)
+    assert rep.bytes_copied == rep.n_hit * Lo["num_gdn"] * (Lo["conv_bytes"] + Lo["ssm_bytes"])
+    if case == "c3":
+        assert (rep.n_hit, rep.n_miss, rep.n_noop) == (205, 154, 153)
+    if case == "c1":
+        assert rep.n_hit == 64
+
+
+ERRMAP = {oracle.REJECT_RANGE: L.LSC_ERR_OUT_OF_RANGE, oracle.REJECT_DUP_DST: L.LSC_ERR_DUP_DST,
+          oracle.REJECT_SRC_IS_DST: L.LSC_ERR_SRC_IS_DST, oracle.REJECT_ARG: L.LSC_ERR_INVALID_ARG}
+
+
+@pytest.mark.parametrize("case", ["range_dst", "range_src", "neg_dst", "dup_dst", "src_is_dst", "src_is_other_dst",
+                                  "dup_src_ok", "noop_out_of_range_ok"])
+def test_validation_matches_oracle(lsc, case):
+    w = W.get("c0")
+    live = np.array([1, 2, 3], np.int32)
+    src = np.array([10, 11, 12], np.int32)
+    nkv = np.array([16, 16, 16], np.int32)
+    init = np.zeros(3, np.uint8)
+    if case == "range_dst":
+        live[1] = 16
+    elif case == "range_src":
+        src[2] = 99
+    elif case == "neg_dst":
+        live[0] = -1
+    elif case == "dup_dst":
+        live[2] = live[0]
+    elif case == "src_is_dst":
+        src[1] = live[1]
+    elif case == "src_is_other_dst":
+        src[0] = live[2]
+    elif case == "dup_src_ok":
+        src[:] = 10
+    elif case == "noop_out_of_range_ok":
+        live[1], nkv[1] = 77, 17
+    rows = W._rows(live, src, nkv, init, 16, np.random.default_rng(0))
+    rc_l, _, _, rc_o, _ = _classify_both(w, rows)
+    assert rc_l == ERRMAP.get(rc_o, rc_o)
+    if case.endswith("_ok"):
+        assert rc_l == L.LSC_OK
+
+
+def test_restore_rejects_before_touching_the_device(lsc):
+    """On a host-only pool a valid call fails with LSC_ERR_CUDA (it would have to
+    enqueue), an invalid one with its validation error: validation runs first."""
+    w = W.get("c0")
+    pool = host_pool(w)
+    rows = W.restore_rows("c0")
+    ops = ops_of(rows)
+    rc, _ = L.lsc_restore(pool, ops, rows.nkv, 16, rows.initialized, FAKE_BASE)
+    assert rc == L.LSC_ERR_CUDA
+    ops2 = ops.copy()
+    ops2["linear_state_id"][3] = ops2["linear_state_id"][0]
+    assert L.lsc_restore(pool, ops2, rows.nkv, 16, rows.initialized, FAKE_BASE)[0] == L.LSC_ERR_DUP_DST
+    assert L.lsc_restore(pool, ops, rows.nkv, 0, rows.initialized, FAKE_BASE)[0] == L.LSC_ERR_INVALID_ARG
+    assert L.lsc_restore(pool, ops, rows.nkv, 16, rows.initialized, None)[0] == L.LSC_ERR_INVALID_ARG
+    assert L.lsc_gather(pool, 1, FAKE_BASE, None, 4, FAKE_BASE, FAKE_BASE) == L.LSC_ERR_STATELESS_LAYER
+    assert L.lsc_scatter(pool, 5, FAKE_BASE, 4, FAKE_BASE, FAKE_BASE) == L.LSC_ERR_OUT_OF_RANGE
+    L.lsc_pool_destroy(pool)
+
+
+def test_soft_cold_classification_without_gdn_layers(lsc):
+    w = W.get("c0")
+    w.num_slots = 40
+    rows = W.combo_rows(40, 16, seed=1)
+    pool = host_pool(w, [W.ATTN, W.ATTN, W.ATTN])
+    rc, act, rep = L.lsc_restore_classify(pool, ops_of(rows), rows.nkv, 16, rows.initialized)
+    assert rc == L.LSC_OK and rep.soft_cold == 1 and rep.bytes_copied == 0 and rep.n_hit > 0
+    assert L.lsc_pool_required_bytes(lib_desc(w, [W.ATTN] * 3)) == 0
+    L.lsc_pool_destroy(pool)
+
+
+def test_alloc_fault_injection_and_layout_log():
+    """LSC_FAULT=alloc makes pool creation fail cleanly; LSC_LOG=1 prints one
+    [lsc-pool] line per GDN layer with page size, shapes, strides, offsets and
+    contiguity (vLLM-Ascend "非连续 KV Cache" §7)."""
+    code = (
+        "import sys; sys.path.insert(0, %r); sys.path.insert(0, %r)\n"
+        "from linear_attention_state_lsc_gb300 import lsc as L, workloads as W\n"
+        "from _util import lib_desc\n"
+        "rc, p = L.lsc_pool_create(lib_desc(W.get('c0p')), 1 << 40, 1 << 30)\n"
+        "print('RC', rc)\n"
+    ) % (ROOT, os.path.join(ROOT, "tests"))
+    env = dict(os.environ, LSC_FAULT="alloc")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
+    assert "RC %d" % L.LSC_ERR_NO_MEMORY in r.stdout, r.stderr
+    env = dict(os.environ, LSC_LOG="1")
+    env.pop("LSC_FAULT", None)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
+    assert "RC 0" in r.stdout, r.stderr
+    lines = [l for l in r.stderr.splitlines() if l.startswith("[lsc-pool]")]
+    assert len(lines) == 2
+    assert "page_bytes=3072" in lines[0] and "conv shape=[16,64,3] stride=[768,3,1]" in lines[0]
+    assert "ssm shape=[16,2,16,16] stride=[768,256,16,1]" in lines[0] and "padding=256" in lines[0]
+    assert "contiguous=0" in lines[0] and "layer=2 gdn=1" in lines[1]
