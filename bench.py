@@ -34,7 +34,7 @@ FALLBACK_HBM = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["lsc", "reference"], default="lsc")
     ap.add_argument("--no-parts", action="store_true", help="headline step only")
@@ -72,7 +72,7 @@ class Clocks:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -233,13 +233,15 @@ def run_lsc(args):
         if i is not None:
             ev["d1"][i].record(fwd)
 
+    # the clock sampler runs from before the warm-up to after the timed region
+    # (all under load), so short timed regions still get samples
+    clocks = Clocks(local)
+    clocks.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clocks = Clocks(local)
-    clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -248,7 +250,11 @@ def run_lsc(args):
         step(i)
     t1.record(fwd)
     torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
     ck = clocks.stop()
+    ck["window"] = "warm-up + timed region + trailing untimed steps"
     elapsed = t0.elapsed_time(t1) / 1e3
     if world > 1:
         tt = torch.tensor([elapsed], device="cuda")

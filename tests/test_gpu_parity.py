@@ -33,6 +33,7 @@ def workload(name, **kw):
 
 
 def _payload(w):
+    w = dataclasses.replace(w, page_bytes=1 << 40)  # any page that holds the payload
     return oracle_layout(w)["payload"]
 
 
@@ -97,10 +98,10 @@ def test_restore_c0_four_rows(lsc):
 
 def test_restore_many_rows_several_launches(lsc):
     """More hit rows and has_initial_state writes than one launch's plan holds."""
-    w = workload("s4", num_slots=9000)
+    w = workload("s4", num_slots=12000)
     rng = np.random.default_rng(5)
     perm = rng.permutation(w.num_slots)
-    n = 4200
+    n = 8000
     live, spare = perm[:n], perm[n:]
     src = np.where(rng.random(n) < 0.6, spare[rng.integers(0, len(spare), n)], -1)
     nkv = 8 * rng.integers(0, 5, n)
