@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--impl", choices=["lsc", "reference"], default="lsc")
     ap.add_argument("--no-parts", action="store_true", help="headline step only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--ncu-case", choices=sorted(NCU_CASES), default=None,
+                    help="run only one kernel on a reduced pool (2 GDN layers), for profiler captures")
     return ap.parse_args()
 
 
@@ -576,9 +578,83 @@ def run_reference(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- profiler cases
+
+NCU_CASES = {
+    # name: (workload, rows, kernel)
+    "decode_f32": ("c1", 64, "decode"),      # serving-step decode: fp32 state, 64 rows, 277 MB per launch
+    "decode_bf16": ("c2", 256, "decode"),    # bf16 state, 256 rows, 571 MB per launch
+    "restore": ("c1", 64, "restore"),        # 64 hits x 2 layers, 549 MB per launch
+    "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer
+}
+
+
+def run_ncu_case(args):
+    """A reduced copy of one kernel's workload: the same shapes, page and rows,
+    2 GDN layers instead of 36, so that a profiler capture stays small."""
+    import torch
+    from linear_attention_state_lsc_gb300 import lsc as L
+    from linear_attention_state_lsc_gb300 import workloads as W
+    torch.cuda.set_device(0)
+    L.load()
+    name, n, kind = NCU_CASES[args.ncu_case]
+    w = W.get(name)
+    w.layers = [W.GDN, W.ATTN, W.GDN]
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    fwd = torch.cuda.current_stream()
+    rng = np.random.default_rng(0)
+    if kind == "restore":
+        rows = W.restore_rows("c1")
+        ops = L.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
+        hs = torch.from_numpy(rows.hs_prefill.copy()).cuda()
+
+        def launch(i):
+            rc, _ = L.lsc_restore(pool, ops, rows.nkv, rows.block_size, rows.initialized, hs, fwd, None)
+            assert rc == L.LSC_OK
+    elif kind == "decode":
+        idx = torch.from_numpy(rng.permutation(w.num_slots)[:n].astype(np.int32)).cuda()
+        has = torch.ones(n, dtype=torch.uint8, device="cuda")
+        x, cw, a, b = W.decode_inputs(w, n, seed=0, layer=0)
+        t = [torch.from_numpy(x).to(torch.bfloat16).cuda(), torch.from_numpy(cw).to(torch.bfloat16).cuda(),
+             torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()]
+        out = torch.empty((n, w.num_v_heads, w.head_v_dim), device="cuda")
+        da = L.decode_args(n, w.num_k_heads, idx, has, *t, out)
+
+        def launch(i):
+            assert L.lsc_gdn_decode(pool, w.gdn_layers[i % 2], da, fwd) == L.LSC_OK
+    else:
+        lengths = W.seq_lengths(n, 64, 512, seed=0)
+        cu, q, k, vv, a, b = W.recurrent_inputs(w, lengths, seed=0, layer=0)
+        T = int(cu[-1])
+        idx = torch.from_numpy(rng.permutation(w.num_slots)[:n].astype(np.int32)).cuda()
+        has = torch.ones(n, dtype=torch.uint8, device="cuda")
+        dev = [torch.from_numpy(z).cuda() for z in (cu, q, k, vv, a, b)]
+        out = torch.empty((T, w.num_v_heads, w.head_v_dim), device="cuda")
+        ra = L.recurrent_args(n, w.num_k_heads, T, idx, has, *dev, out)
+
+        def launch(i):
+            assert L.lsc_gdn_recurrent(pool, w.gdn_layers[i % 2], ra, fwd) == L.LSC_OK
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(fwd)
+    for i in range(args.steps):
+        launch(i)
+    e1.record(fwd)
+    torch.cuda.synchronize()
+    assert L.lsc_pool_status(pool, fwd) == L.LSC_OK
+    print(json.dumps({"ncu_case": args.ncu_case, "launches": args.steps,
+                      "ms_per_launch": round(e0.elapsed_time(e1) / args.steps, 4)}))
+    L.lsc_pool_destroy(pool)
+
+
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.ncu_case:
+        run_ncu_case(a)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_lsc(a)
