@@ -18,11 +18,13 @@
 #include <cuda_runtime.h>
 
 #include "lsc_internal.h"
+#include "lsc_ptx.h"
 
 namespace lsc {
 namespace {
 
 constexpr int kDecodeThreads = 256;
+constexpr int kDecodeMaxItems = 512;  // work items per CTA and launch
 constexpr int kMaxDv = 128;
 constexpr int kMaxTaps = 8;
 
@@ -49,7 +51,6 @@ __device__ __forceinline__ void st_conv(void *base, int64_t i, float v, bool bf1
 // 16-byte vectors of state elements <-> floats.
 template <typename TS> struct StateVec;
 template <> struct StateVec<float> {
-  static constexpr int kElems = 4;
   __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
     f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
     f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
@@ -59,7 +60,6 @@ template <> struct StateVec<float> {
   }
 };
 template <> struct StateVec<__nv_bfloat16> {
-  static constexpr int kElems = 8;
   __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -79,204 +79,394 @@ template <> struct StateVec<__nv_bfloat16> {
   }
 };
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
+// Fused decode as a persistent, warp-specialised, TMA-pipelined kernel.
+//
+// Work item = (row i, q/k head g): the G = Hv/Hk v heads that share q/k head g.
+// One CTA owns every conv channel of its item (q_g, k_g, and the v channels of
+// its G heads), so no two CTAs touch the same conv state.  CTA b processes items
+// b, b + grid, ... ; their state tiles (TR rows of one head, <= 32 KiB) stream
+// through a ring of NS shared-memory stages.
+//  * Producer warp (one lane): keeps NS tile loads in flight (cp.async.bulk, a
+//    `full` mbarrier per stage) and the conv inputs of the next two items in a
+//    double buffer; when the consumers release a stage (`empty` mbarrier) it
+//    bulk-stores the tile back through the page stride, waits for the store to
+//    leave shared memory, and refills the stage.
+//  * Consumer warps (kConsumers threads): conv update of the item, L2 norms,
+//    then each landed tile in place -- 8 threads per state row on 16-byte
+//    vectors: u = S_r.k, w = S_r.q, d = b (v_r - a u), S'_r = a S_r + d k,
+//    o_r = a w + d (k.q).
+// Only the conv and ssm views of a page are addressed.  Every mbarrier wait is
+// bounded: on expiry the CTA records LSC_ERR_DEV_TIMEOUT, the producer waits
+// (bounded) for every copy it issued, and the CTA returns.
+constexpr int kMaxStages = 8;
+constexpr int kConsumers = 512;
+constexpr int kDecodeBlock = kConsumers + 32;
+constexpr int64_t kTileBytes = 32 << 10;
 
-// Fused decode.  Grid (Hv, n); a cluster spans the `group` v heads that share
-// one q/k head, so every CTA of a cluster works on the same row.  CTA (h, i):
-//  1. issues the loads of its head's [dv x DK] state slice into registers (they
-//     complete while the conv runs);
-//  2. runs the conv update for the q and k channels of head group g and the v
-//     channels of head h, keeping y in shared memory; v channels' new conv state
-//     is written at once (this CTA owns them);
-//  3. waits on the cluster barrier -- every CTA of the cluster has now read the
-//     shared q/k channels' old conv state -- after which cluster rank 0 writes
-//     their new state;
-//  4. L2-normalises q and k, then updates its state rows and writes o.
-// Thread layout: TPR threads per state row, NV 16-byte vectors per thread;
-// vector j of a thread is column vector j*TPR + lane_in_row, so a warp's loads
-// use whole 32-byte sectors.
-template <int DK, typename TS, int PASSES>
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr int EPV = StateVec<TS>::kElems;
-  constexpr int VPR = DK / EPV;
-  constexpr int NV = VPR < 8 ? VPR : 8;
-  constexpr int TPR = VPR / NV;
-  constexpr int RPP = kDecodeThreads / TPR;
-  static_assert(VPR % NV == 0 && TPR >= 1 && TPR <= 32, "state row layout");
+template <int DK, typename TS>
+struct DecodeShape {
+  static constexpr int ES = (int)sizeof(TS);
+  static constexpr int EPV = 16 / ES;           // state elements per 16-byte vector
+  static constexpr int VPR = DK / EPV;          // vectors per state row
+  static constexpr int TPR = VPR < 8 ? VPR : 8; // threads per row
+  static constexpr int NV = VPR / TPR;          // vectors per thread per row
+  static constexpr int NC = NV * EPV;           // columns per thread
+  static constexpr int RPP = kConsumers / TPR;  // rows per pass
+};
 
-  __shared__ __align__(16) float ys[2 * DK + kMaxDv];
-  __shared__ float qk_stash[2 * DK * (kMaxTaps - 1)];
-  __shared__ float red[3][kDecodeThreads / 32];
+__host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-  const int tid = threadIdx.x;
-  const int h = blockIdx.x, i = blockIdx.y;
-  const int g = h / p.group;
-  const bool rank0 = (h % p.group) == 0;
-  const int32_t slot = p.idx[i];
-  const bool bad = slot >= p.num_slots;
-  const bool valid = slot >= 0 && !bad;
-  const bool warm = valid && (p.has_init == nullptr || p.has_init[i] != 0);
-  if (bad && tid == 0 && rank0) report(p.status, LSC_ERR_OUT_OF_RANGE);
-
-  uint8_t *page = valid ? p.layer + (int64_t)slot * p.page : nullptr;
-  TS *S = valid ? (TS *)(page + p.ssm_off) + (int64_t)h * p.dv * DK : nullptr;
-  const int r0 = tid / TPR, lr = tid % TPR;
-
-  // 1. state prefetch
-  uint4 sreg[PASSES][NV];
-#pragma unroll
-  for (int ps = 0; ps < PASSES; ++ps) {
-    const int r = r0 + ps * RPP;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      if (warm && r < p.dv) sreg[ps][j] = *(const uint4 *)(S + (int64_t)r * DK + (j * TPR + lr) * EPV);
-      else sreg[ps][j] = make_uint4(0, 0, 0, 0);
-    }
+// Tiling and dynamic shared-memory layout, computed identically on both sides.
+struct DecodeGeom {
+  int nch, TR, TPH, TPG, NS;
+  int64_t stage_stride, conv_buf, off_st, off_xs, off_ws, off_conv, ys_buf, off_ys, off_info, total;
+  __host__ __device__ DecodeGeom(int dk, int es, int dv, int G, int W, int esc, int ns) {
+    nch = 2 * dk + G * dv;
+    const int64_t row_bytes = (int64_t)dk * es;
+    TR = (int)(kTileBytes / row_bytes);
+    if (TR > dv) TR = dv;
+    if (TR < 1) TR = 1;
+    TPH = (dv + TR - 1) / TR;
+    TPG = G * TPH;
+    NS = ns;
+    stage_stride = align_up((int64_t)TR * row_bytes, 128);
+    off_st = 0;
+    off_xs = align_up((int64_t)nch * (W - 1) * esc, 16);
+    off_ws = off_xs + align_up((int64_t)nch * esc, 16);
+    conv_buf = align_up(off_ws + (int64_t)nch * W * esc, 128);
+    off_conv = (int64_t)NS * stage_stride;
+    ys_buf = align_up((int64_t)(nch + 2 * G) * 4, 128);
+    off_ys = off_conv + 2 * conv_buf;
+    off_info = off_ys + 2 * ys_buf;
+    total = off_info + 2 * 4 * kDecodeMaxItems;
   }
+};
 
-  // 2. causal conv1d update of this CTA's channels
-  const int C = p.conv_dim, W = p.conv_width;
-  const bool cbf = p.conv_bf16 != 0;
-  const int nch = 2 * DK + p.dv;
-  for (int cl = tid; cl < nch; cl += kDecodeThreads) {
-    const int c = cl < DK ? g * DK + cl
-                          : (cl < 2 * DK ? p.Hk * DK + g * DK + (cl - DK) : 2 * p.Hk * DK + h * p.dv + (cl - 2 * DK));
-    float win[kMaxTaps];
-    for (int j = 0; j < W - 1; ++j) win[j] = warm ? ld_conv(page, (int64_t)c * (W - 1) + j, cbf) : 0.f;
-    win[W - 1] = ld_conv(p.x, (int64_t)i * C + c, cbf);
-    float z = 0.f;
-    for (int j = 0; j < W; ++j) z = fmaf(ld_conv(p.w, (int64_t)c * W + j, cbf), win[j], z);
-    ys[cl] = z / (1.f + expf(-z));  // SiLU
-    if (valid) {
-      if (cl >= 2 * DK) {
-        for (int j = 0; j < W - 1; ++j) st_conv(page, (int64_t)c * (W - 1) + j, win[j + 1], cbf);
-      } else {
-        for (int j = 0; j < W - 1; ++j) qk_stash[cl * (W - 1) + j] = win[j + 1];
-      }
-    }
-  }
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
-  // 3. every CTA of the cluster has read the shared q/k conv state
-  cluster_sync_all();
-  if (valid && rank0) {
-    for (int cl = tid; cl < 2 * DK; cl += kDecodeThreads) {
-      const int c = cl < DK ? g * DK + cl : p.Hk * DK + g * DK + (cl - DK);
-      for (int j = 0; j < W - 1; ++j) st_conv(page, (int64_t)c * (W - 1) + j, qk_stash[cl * (W - 1) + j], cbf);
-    }
-  }
-
-  // 4a. L2 norms of q and k, and k . q
-  float sq = 0.f, sk = 0.f, sqk = 0.f;
-  for (int c = tid; c < DK; c += kDecodeThreads) {
-    const float a = ys[c], b = ys[DK + c];
-    sq = fmaf(a, a, sq);
-    sk = fmaf(b, b, sk);
-    sqk = fmaf(a, b, sqk);
-  }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    sq += __shfl_xor_sync(0xffffffffu, sq, m);
-    sk += __shfl_xor_sync(0xffffffffu, sk, m);
-    sqk += __shfl_xor_sync(0xffffffffu, sqk, m);
-  }
-  if ((tid & 31) == 0) {
-    red[0][tid >> 5] = sq;
-    red[1][tid >> 5] = sk;
-    red[2][tid >> 5] = sqk;
-  }
-  __syncthreads();
-  sq = sk = sqk = 0.f;
-#pragma unroll
-  for (int w = 0; w < kDecodeThreads / 32; ++w) {
-    sq += red[0][w];
-    sk += red[1][w];
-    sqk += red[2][w];
-  }
-  const float inv_q = 1.f / sqrtf(sq + 1e-6f);
-  const float inv_k = 1.f / sqrtf(sk + 1e-6f);
-  const float kq = sqk * inv_q * inv_k;
-  for (int c = tid; c < 2 * DK; c += kDecodeThreads) ys[c] *= c < DK ? inv_q : inv_k;
-  __syncthreads();
-
-  // 4b. delta rule on the register-resident rows
-  const float a = valid ? p.alpha[(int64_t)i * p.Hv + h] : 0.f;
-  const float b = valid ? p.beta[(int64_t)i * p.Hv + h] : 0.f;
-  const float *qs = ys, *ks = ys + DK;
-#pragma unroll
-  for (int ps = 0; ps < PASSES; ++ps) {
-    const int r = r0 + ps * RPP;
-    const bool rv = r < p.dv;
-    float u = 0.f, wq = 0.f;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      float s[EPV];
-      StateVec<TS>::unpack(sreg[ps][j], s);
-      const int c0 = (j * TPR + lr) * EPV;
-#pragma unroll
-      for (int e = 0; e < EPV; e += 4) {
-        const float4 k4 = *(const float4 *)(ks + c0 + e);
-        const float4 q4 = *(const float4 *)(qs + c0 + e);
-        u = fmaf(s[e], k4.x, u); u = fmaf(s[e + 1], k4.y, u); u = fmaf(s[e + 2], k4.z, u); u = fmaf(s[e + 3], k4.w, u);
-        wq = fmaf(s[e], q4.x, wq); wq = fmaf(s[e + 1], q4.y, wq); wq = fmaf(s[e + 2], q4.z, wq); wq = fmaf(s[e + 3], q4.w, wq);
-      }
-    }
-#pragma unroll
-    for (int m = TPR / 2; m >= 1; m >>= 1) {
-      u += __shfl_xor_sync(0xffffffffu, u, m);
-      wq += __shfl_xor_sync(0xffffffffu, wq, m);
-    }
-    const float vr = rv ? ys[2 * DK + r] : 0.f;
-    const float d = b * (vr - a * u);
-    const float o = fmaf(a, wq, d * kq);
-    if (valid && rv) {
-      TS *row = S + (int64_t)r * DK;
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        float s[EPV];
-        StateVec<TS>::unpack(sreg[ps][j], s);
-        const int c0 = (j * TPR + lr) * EPV;
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) s[e] = fmaf(a, s[e], d * ks[c0 + e]);
-        __stcs((uint4 *)(row + c0), StateVec<TS>::pack(s));
-      }
-    }
-    if (rv && lr == 0) p.out[((int64_t)i * p.Hv + h) * p.dv + r] = valid ? o : 0.f;
-  }
-}
-
-template <int DK, typename TS, int PASSES>
-cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.Hv, p.n, 1);
-  cfg.blockDim = dim3(kDecodeThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.group;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<DK, TS, PASSES>, p);
+__device__ __forceinline__ bool consumer_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "barrier.red.or.pred p, 1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kConsumers)
+      : "memory");
+  return r != 0;
 }
 
 template <int DK, typename TS>
-int dispatch_decode_passes(const DecodeParams &p, cudaStream_t s) {
-  constexpr int EPV = StateVec<TS>::kElems;
-  constexpr int VPR = DK / EPV;
-  constexpr int NV = VPR < 8 ? VPR : 8;
-  constexpr int RPP = kDecodeThreads / (VPR / NV);
-  const int passes = (p.dv + RPP - 1) / RPP;
-  cudaError_t e;
-  if (passes == 1) e = launch_decode_t<DK, TS, 1>(p, s);
-  else if constexpr (RPP * 2 >= kMaxDv && RPP < kMaxDv) {
-    if (passes == 2) e = launch_decode_t<DK, TS, 2>(p, s);
-    else return LSC_ERR_UNSUPPORTED;
-  } else return LSC_ERR_UNSUPPORTED;
-  if (e != cudaSuccess) { cudaGetLastError(); return LSC_ERR_CUDA; }
+__global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+  using Sh = DecodeShape<DK, TS>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], cfull[2];
+  __shared__ float red[3][kConsumers / 32];
+
+  const int tid = threadIdx.x;
+  const int W = p.conv_width, C = p.conv_dim, dv = p.dv, G = p.group, Hk = p.Hk;
+  const int esc = p.conv_bf16 ? 2 : 4;
+  const bool cbf = p.conv_bf16 != 0;
+  const bool tma_conv = p.conv_tma != 0;
+  const DecodeGeom D(DK, Sh::ES, dv, G, W, esc, p.stages);
+  const int NS = D.NS;
+  const int n_items = p.n * Hk;
+  const int b = blockIdx.x, grid = gridDim.x;
+  const int my_items = b < n_items ? (n_items - b + grid - 1) / grid : 0;
+  const int my_tiles = my_items * D.TPG;
+  int32_t *info_slot = reinterpret_cast<int32_t *>(smem + D.off_info);
+  int32_t *info_warm = info_slot + kDecodeMaxItems;
+
+  // rows of this CTA's items: slot (or -1) and warm, loaded once
+  for (int k = tid; k < my_items; k += kDecodeBlock) {
+    const int i = (b + k * grid) / Hk;
+    const int32_t slot = p.idx[i];
+    const bool ok = slot >= 0 && slot < p.num_slots;
+    if (slot >= p.num_slots) report(p.status, LSC_ERR_OUT_OF_RANGE);
+    info_slot[k] = ok ? slot : -1;
+    info_warm[k] = ok && (p.has_init == nullptr || p.has_init[i] != 0);
+  }
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&cfull[0], 1);
+    mbar_init(&cfull[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (tid >= kConsumers) {
+    // ------------------------------------------------------------ producer
+    if (tid != kConsumers) return;
+    int issued_tiles = 0, issued_convs = 0;
+    auto issue_conv = [&](int k) {
+      if (k >= my_items) return;
+      const int j = b + k * grid, i = j / Hk, g = j % Hk;
+      const int32_t slot = info_slot[k];
+      const bool warm = info_warm[k] != 0;
+      uint8_t *buf = smem + D.off_conv + (k & 1) * D.conv_buf;
+      const uint32_t bytes = (slot >= 0 && tma_conv) ? (uint32_t)(D.nch * ((warm ? W - 1 : 0) + 1 + W) * esc) : 0u;
+      mbar_arrive_expect_tx(&cfull[k & 1], bytes);
+      if (bytes) {
+        const uint8_t *page = p.layer + (int64_t)slot * p.page;
+        const int c0[3] = {g * DK, Hk * DK + g * DK, 2 * Hk * DK + g * G * dv};
+        const int cn[3] = {DK, DK, G * dv};
+        const int cl0[3] = {0, DK, 2 * DK};
+        for (int sgm = 0; sgm < 3; ++sgm) {
+          if (warm)
+            bulk_g2s(buf + D.off_st + (int64_t)cl0[sgm] * (W - 1) * esc, page + (int64_t)c0[sgm] * (W - 1) * esc,
+                     (uint32_t)(cn[sgm] * (W - 1) * esc), &cfull[k & 1]);
+          bulk_g2s(buf + D.off_xs + (int64_t)cl0[sgm] * esc, (const uint8_t *)p.x + ((int64_t)i * C + c0[sgm]) * esc,
+                   (uint32_t)(cn[sgm] * esc), &cfull[k & 1]);
+          bulk_g2s(buf + D.off_ws + (int64_t)cl0[sgm] * W * esc, (const uint8_t *)p.w + (int64_t)c0[sgm] * W * esc,
+                   (uint32_t)(cn[sgm] * W * esc), &cfull[k & 1]);
+        }
+      }
+      issued_convs = k + 1;
+    };
+    // global address of tile t's rows in the state view
+    auto tile_addr = [&](int t, uint32_t &bytes, bool &live, bool &load) -> uint8_t * {
+      const int k = t / D.TPG, rem = t % D.TPG, hl = rem / D.TPH, rb = rem % D.TPH;
+      const int j = b + k * grid, g = j % Hk;
+      const int rows = min(D.TR, dv - rb * D.TR);
+      bytes = (uint32_t)rows * DK * Sh::ES;
+      const int32_t slot = info_slot[k];
+      live = slot >= 0;
+      load = live && info_warm[k] != 0;
+      if (!live) return nullptr;
+      return p.layer + (int64_t)slot * p.page + p.ssm_off +
+             (((int64_t)(g * G + hl) * dv + (int64_t)rb * D.TR) * DK) * Sh::ES;
+    };
+    auto issue_tile = [&](int t) {
+      if (t >= my_tiles) return;
+      uint32_t bytes;
+      bool live, load;
+      const uint8_t *src = tile_addr(t, bytes, live, load);
+      mbar_arrive_expect_tx(&full[t % NS], load ? bytes : 0u);
+      if (load) bulk_g2s(smem + (int64_t)(t % NS) * D.stage_stride, src, bytes, &full[t % NS]);
+      issued_tiles = t + 1;
+    };
+    issue_conv(0);
+    issue_conv(1);
+    for (int t = 0; t < NS; ++t) issue_tile(t);
+    for (int t = 0; t < my_tiles; ++t) {
+      if (!mbar_wait_bounded(&empty[t % NS], (t / NS) & 1, p.wait_limit_ns)) {
+        report(p.status, LSC_ERR_DEV_TIMEOUT);
+        for (int tt = t; tt < issued_tiles; ++tt)
+          mbar_wait_bounded(&full[tt % NS], (tt / NS) & 1, p.drain_limit_ns);
+        for (int kk = issued_convs - 2 < 0 ? 0 : issued_convs - 2; kk < issued_convs; ++kk)
+          mbar_wait_bounded(&cfull[kk & 1], (kk >> 1) & 1, p.drain_limit_ns);
+        bulk_wait_read_all();
+        return;
+      }
+      uint32_t bytes;
+      bool live, load;
+      uint8_t *dst = tile_addr(t, bytes, live, load);
+      if (live) bulk_s2g(dst, smem + (int64_t)(t % NS) * D.stage_stride, bytes);
+      bulk_commit();
+      // the consumers have finished an item's conv staging before its first tile
+      if (t % D.TPG == 0) issue_conv(t / D.TPG + 2);
+      if (t + NS < my_tiles) {
+        bulk_wait_read_all();  // tile t's store has left the stage
+        issue_tile(t + NS);
+      }
+    }
+    bulk_wait_read_all();
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int lr = tid % Sh::TPR;
+  int t = 0;
+  for (int k = 0; k < my_items; ++k) {
+    const int j = b + k * grid, i = j / Hk, g = j % Hk;
+    const int32_t slot = info_slot[k];
+    const bool valid = slot >= 0;
+    const bool warm = info_warm[k] != 0;
+    uint8_t *page = valid ? p.layer + (int64_t)slot * p.page : nullptr;
+    const uint8_t *cb = smem + D.off_conv + (k & 1) * D.conv_buf;
+    float *ys = reinterpret_cast<float *>(smem + D.off_ys + (k & 1) * D.ys_buf);
+
+    // conv update of the item's channels
+    if (consumer_any(!mbar_wait_bounded(&cfull[k & 1], (k >> 1) & 1, p.wait_limit_ns))) {
+      if (tid == 0) report(p.status, LSC_ERR_DEV_TIMEOUT);
+      return;  // the producer drains the copies in flight
+    }
+    float kq = 0.f;
+    float kreg[Sh::NC], qreg[Sh::NC];
+    if (valid) {
+      for (int cl = tid; cl < D.nch; cl += kConsumers) {
+        const int c = cl < DK ? g * DK + cl
+                              : (cl < 2 * DK ? Hk * DK + g * DK + (cl - DK) : 2 * Hk * DK + g * G * dv + (cl - 2 * DK));
+        float win[kMaxTaps];
+        for (int jj = 0; jj < W - 1; ++jj) {
+          float v = 0.f;
+          if (warm)
+            v = tma_conv ? ld_conv(cb + D.off_st, (int64_t)cl * (W - 1) + jj, cbf)
+                         : ld_conv(page, (int64_t)c * (W - 1) + jj, cbf);
+          win[jj] = v;
+        }
+        win[W - 1] = tma_conv ? ld_conv(cb + D.off_xs, cl, cbf) : ld_conv(p.x, (int64_t)i * C + c, cbf);
+        float z = 0.f;
+        for (int jj = 0; jj < W; ++jj)
+          z = fmaf(tma_conv ? ld_conv(cb + D.off_ws, (int64_t)cl * W + jj, cbf) : ld_conv(p.w, (int64_t)c * W + jj, cbf),
+                   win[jj], z);
+        ys[cl] = z / (1.f + expf(-z));  // SiLU
+        for (int jj = 0; jj < W - 1; ++jj) st_conv(page, (int64_t)c * (W - 1) + jj, win[jj + 1], cbf);
+      }
+      if (tid < G) {
+        ys[D.nch + tid] = p.alpha[(int64_t)i * p.Hv + g * G + tid];
+        ys[D.nch + G + tid] = p.beta[(int64_t)i * p.Hv + g * G + tid];
+      }
+      consumer_sync();
+      float sq = 0.f, sk = 0.f, sqk = 0.f;
+      for (int c = tid; c < DK; c += kConsumers) {
+        const float a = ys[c], bk = ys[DK + c];
+        sq = fmaf(a, a, sq);
+        sk = fmaf(bk, bk, sk);
+        sqk = fmaf(a, bk, sqk);
+      }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, m);
+        sk += __shfl_xor_sync(0xffffffffu, sk, m);
+        sqk += __shfl_xor_sync(0xffffffffu, sqk, m);
+      }
+      if ((tid & 31) == 0) {
+        red[0][tid >> 5] = sq;
+        red[1][tid >> 5] = sk;
+        red[2][tid >> 5] = sqk;
+      }
+      consumer_sync();
+      sq = sk = sqk = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumers / 32; ++w) {
+        sq += red[0][w];
+        sk += red[1][w];
+        sqk += red[2][w];
+      }
+      const float inv_q = 1.f / sqrtf(sq + 1e-6f);
+      const float inv_k = 1.f / sqrtf(sk + 1e-6f);
+      kq = sqk * inv_q * inv_k;
+#pragma unroll
+      for (int jj = 0; jj < Sh::NV; ++jj) {
+        const int c0v = (jj * Sh::TPR + lr) * Sh::EPV;
+#pragma unroll
+        for (int e = 0; e < Sh::EPV; ++e) {
+          qreg[jj * Sh::EPV + e] = ys[c0v + e] * inv_q;
+          kreg[jj * Sh::EPV + e] = ys[DK + c0v + e] * inv_k;
+        }
+      }
+    }
+
+    // the item's state tiles
+    for (int tl = 0; tl < D.TPG; ++tl, ++t) {
+      const int stage = t % NS;
+      if (consumer_any(!mbar_wait_bounded(&full[stage], (t / NS) & 1, p.wait_limit_ns))) {
+        if (tid == 0) report(p.status, LSC_ERR_DEV_TIMEOUT);
+        return;
+      }
+      const int hl = tl / D.TPH, rb = tl % D.TPH;
+      const int rows = min(D.TR, dv - rb * D.TR);
+      TS *S = reinterpret_cast<TS *>(smem + (int64_t)stage * D.stage_stride);
+      float *o = p.out + ((int64_t)i * p.Hv + g * G + hl) * dv + (int64_t)rb * D.TR;
+      if (valid) {
+        const float a = ys[D.nch + hl], bb = ys[D.nch + G + hl];
+        const float *vs = ys + 2 * DK + hl * dv + rb * D.TR;
+        const int npass = (rows + Sh::RPP - 1) / Sh::RPP;
+        for (int r0 = tid / Sh::TPR; r0 < npass * Sh::RPP; r0 += Sh::RPP) {
+          const bool rv = r0 < rows;
+          const int r = rv ? r0 : 0;
+          float s[Sh::NC];
+#pragma unroll
+          for (int jj = 0; jj < Sh::NV; ++jj) {
+            const uint4 v = warm ? *reinterpret_cast<const uint4 *>(S + (int64_t)r * DK + (jj * Sh::TPR + lr) * Sh::EPV)
+                                 : make_uint4(0, 0, 0, 0);
+            StateVec<TS>::unpack(v, s + jj * Sh::EPV);
+          }
+          float u0 = 0.f, u1 = 0.f, w0 = 0.f, w1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < Sh::NC; e += 2) {
+            u0 = fmaf(s[e], kreg[e], u0);
+            u1 = fmaf(s[e + 1], kreg[e + 1], u1);
+            w0 = fmaf(s[e], qreg[e], w0);
+            w1 = fmaf(s[e + 1], qreg[e + 1], w1);
+          }
+          float u = u0 + u1, wq = w0 + w1;
+#pragma unroll
+          for (int m = Sh::TPR / 2; m >= 1; m >>= 1) {
+            u += __shfl_xor_sync(0xffffffffu, u, m);
+            wq += __shfl_xor_sync(0xffffffffu, wq, m);
+          }
+          const float d = bb * ((rv ? vs[r] : 0.f) - a * u);
+          if (rv) {
+#pragma unroll
+            for (int e = 0; e < Sh::NC; ++e) s[e] = fmaf(a, s[e], d * kreg[e]);
+#pragma unroll
+            for (int jj = 0; jj < Sh::NV; ++jj)
+              *reinterpret_cast<uint4 *>(S + (int64_t)r * DK + (jj * Sh::TPR + lr) * Sh::EPV) =
+                  StateVec<TS>::pack(s + jj * Sh::EPV);
+            if (lr == 0) o[r] = fmaf(a, wq, d * kq);
+          }
+        }
+      } else {
+        for (int r = tid; r < rows; r += kConsumers) o[r] = 0.f;
+      }
+      fence_proxy_async_smem();
+      consumer_sync();
+      if (tid == 0) mbar_arrive(&empty[stage]);
+    }
+  }
+}
+
+template <int DK, typename TS>
+int launch_decode_t(const DecodeParams &p0, cudaStream_t stream) {
+  DecodeParams p = p0;
+  const int esc = p.conv_bf16 ? 2 : 4;
+  static int optin = 0;  // per process: the opt-in shared-memory limit of a block
+  if (!optin) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return LSC_ERR_CUDA;
+    }
+  }
+  const DecodeGeom probe(DK, (int)sizeof(TS), p.dv, p.group, p.conv_width, esc, 0);
+  const int64_t fixed = probe.total + 1024;  // conv, y and item buffers, static shared memory
+  int64_t ns = (optin - fixed) / probe.stage_stride;
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns < 2) return LSC_ERR_UNSUPPORTED;
+  p.stages = (int)ns;
+  const DecodeGeom D(DK, (int)sizeof(TS), p.dv, p.group, p.conv_width, esc, p.stages);
+  static int configured = 0;  // per instantiation
+  if (configured < D.total) {
+    if (cudaFuncSetAttribute(decode_kernel<DK, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)D.total) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return LSC_ERR_UNSUPPORTED;
+    }
+    configured = (int)D.total;
+  }
+  // one CTA per SM; rows are split into launches so that no CTA holds more than
+  // kDecodeMaxItems items
+  const int grid_max = p.num_sms;
+  const int rows_per_launch = (int)((int64_t)kDecodeMaxItems * grid_max / p.Hk);
+  for (int r0 = 0; r0 < p0.n; r0 += rows_per_launch) {
+    DecodeParams q = p;
+    q.n = min(rows_per_launch, p0.n - r0);
+    q.idx = p0.idx + r0;
+    q.has_init = p0.has_init ? p0.has_init + r0 : nullptr;
+    q.x = (const uint8_t *)p0.x + (int64_t)r0 * p0.conv_dim * esc;
+    q.alpha = p0.alpha + (int64_t)r0 * p0.Hv;
+    q.beta = p0.beta + (int64_t)r0 * p0.Hv;
+    q.out = p0.out + (int64_t)r0 * p0.Hv * p0.dv;
+    const int64_t items = (int64_t)q.n * q.Hk;
+    const int grid = (int)(items < grid_max ? items : grid_max);
+    decode_kernel<DK, TS><<<grid, kDecodeBlock, (size_t)D.total, stream>>>(q);
+    if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;
+  }
   return LSC_OK;
 }
 
@@ -432,10 +622,10 @@ int launch_decode(const DecodeParams &p, int dk, int ssm_dtype, cudaStream_t s) 
   if (p.dv > kMaxDv || p.conv_width > kMaxTaps || p.group > 8) return LSC_ERR_UNSUPPORTED;
   const bool bf = ssm_dtype == LSC_BF16;
   switch (dk) {
-    case 16: return bf ? dispatch_decode_passes<16, __nv_bfloat16>(p, s) : dispatch_decode_passes<16, float>(p, s);
-    case 32: return bf ? dispatch_decode_passes<32, __nv_bfloat16>(p, s) : dispatch_decode_passes<32, float>(p, s);
-    case 64: return bf ? dispatch_decode_passes<64, __nv_bfloat16>(p, s) : dispatch_decode_passes<64, float>(p, s);
-    case 128: return bf ? dispatch_decode_passes<128, __nv_bfloat16>(p, s) : dispatch_decode_passes<128, float>(p, s);
+    case 16: return bf ? launch_decode_t<16, __nv_bfloat16>(p, s) : launch_decode_t<16, float>(p, s);
+    case 32: return bf ? launch_decode_t<32, __nv_bfloat16>(p, s) : launch_decode_t<32, float>(p, s);
+    case 64: return bf ? launch_decode_t<64, __nv_bfloat16>(p, s) : launch_decode_t<64, float>(p, s);
+    case 128: return bf ? launch_decode_t<128, __nv_bfloat16>(p, s) : launch_decode_t<128, float>(p, s);
     default: return LSC_ERR_UNSUPPORTED;
   }
 }

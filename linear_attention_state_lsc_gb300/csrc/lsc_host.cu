@@ -41,6 +41,9 @@ int esize(int32_t dtype) {
   }
 }
 
+// Bound of every device-side wait (mbarrier), in nanoseconds.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
 // Host-side fault injection for the tests: LSC_FAULT=<name>.
 bool fault(const char *name) {
   const char *f = getenv("LSC_FAULT");
@@ -485,6 +488,17 @@ int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, voi
   d.beta = a->beta;
   d.out = a->out;
   d.status = g.status;
+  // TMA staging of the conv inputs needs every segment (q/k/v channel ranges of
+  // the conv state, x and the weights) 16-byte aligned in start and length.
+  const int64_t esc = g.conv_dtype == LSC_BF16 ? 2 : 4, W = g.conv_width;
+  const int64_t units[] = {g.dk * (W - 1) * esc, (int64_t)g.dv * (W - 1) * esc, g.dk * esc, (int64_t)g.dv * esc,
+                           (int64_t)g.conv_dim * esc, g.dk * W * esc, (int64_t)g.dv * W * esc};
+  bool tma = ((uintptr_t)a->x % 16) == 0 && ((uintptr_t)a->conv_weight % 16) == 0;
+  for (int64_t u : units) tma = tma && (u % 16) == 0;
+  d.conv_tma = tma ? 1 : 0;
+  d.wait_limit_ns = fault("timeout0") ? 0 : kWaitLimitNs;
+  d.drain_limit_ns = kWaitLimitNs;
+  d.num_sms = p->num_sms;
   return lsc::launch_decode(d, g.dk, g.ssm_dtype, (cudaStream_t)stream);
 }
 

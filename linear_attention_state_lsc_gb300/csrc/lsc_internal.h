@@ -78,6 +78,11 @@ struct DecodeParams {
   const float *alpha, *beta;
   float *out;
   int32_t *status;
+  int32_t conv_tma;         // conv segments 16-byte aligned: staged by TMA bulk copies
+  uint64_t wait_limit_ns;   // bound of each mbarrier wait (0: give up at once)
+  uint64_t drain_limit_ns;  // bound of the wait for in-flight copies after a timeout
+  int32_t num_sms;
+  int32_t stages;           // set by the launcher: shared-memory ring depth
 };
 // returns LSC_OK, LSC_ERR_UNSUPPORTED or LSC_ERR_CUDA
 int launch_decode(const DecodeParams &p, int dk, int ssm_dtype, cudaStream_t stream);

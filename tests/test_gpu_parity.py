@@ -314,6 +314,27 @@ def test_decode_out_of_range_row(lsc):
         check_decode(w, P, l, pre, ok, has, x, cw, a, b, out)
 
 
+@pytest.mark.parametrize("name", ["c0p", "s4"])  # conv inputs staged by TMA / read with plain loads
+def test_decode_bounded_wait_expiry_reports_and_writes_nothing(lsc, name, monkeypatch):
+    """LSC_FAULT=timeout0 makes every mbarrier wait of the decode give up at
+    once: the kernel records LSC_ERR_DEV_TIMEOUT, waits (bounded) for its copies
+    in flight, writes no state, and the context stays usable."""
+    w = workload(name)
+    with DevPool(w, seed=15) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, x, cw, a, b = decode_case(w, seed=5)
+        monkeypatch.setenv("LSC_FAULT", "timeout0")
+        rc, _ = run_decode(P, l, w, idx, has, x, cw, a, b)
+        monkeypatch.delenv("LSC_FAULT")
+        assert rc == L.LSC_OK
+        assert P.status() == L.LSC_ERR_DEV_TIMEOUT
+        np.testing.assert_array_equal(P.download(l), pre)
+        rc, out = run_decode(P, l, w, idx, has, x, cw, a, b)
+        assert rc == L.LSC_OK and P.status() == L.LSC_OK
+        check_decode(w, P, l, pre, idx, has, x, cw, a, b, out)
+
+
 def test_decode_rejects(lsc):
     w = workload("c0")
     with DevPool(w) as P:
