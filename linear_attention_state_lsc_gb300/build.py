@@ -15,8 +15,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblsc.so")
-SOURCES = ["lsc_host.cu", "lsc_copy.cu", "lsc_gdn.cu"]
-HEADERS = [os.path.join(CSRC, "lsc_internal.h"), os.path.join(INCLUDE, "lsc.h")]
+SOURCES = ["lsc_host.cu", "lsc_copy.cu", "lsc_gdn.cu", "lsc_decode_f32.cu", "lsc_decode_bf16.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("lsc_internal.h", "lsc_ptx.h", "lsc_gdn_common.cuh", "lsc_decode.cuh")] + \
+    [os.path.join(INCLUDE, "lsc.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
