@@ -254,7 +254,9 @@ typedef struct {
  *   S <- alpha S (I - beta k k^T) + beta v k^T,  out = S q   (per v head)
  * Arithmetic in fp32; states stored back at their dtype (bf16: round to
  * nearest even).  has_init[i] == 0 reads both states as zero.  idx[i] < 0
- * writes zeros to out[i] and touches no state.  Entries of idx that are >= 0
+ * writes zeros to out[i] and touches no state.  If a bounded device wait
+ * expires (LSC_ERR_DEV_TIMEOUT in the status word), the states and outputs of
+ * the call's rows are unspecified; nothing outside their views is written.  Entries of idx that are >= 0
  * must be distinct.  Supported: head_k_dim in {16, 32, 64, 128}, head_v_dim <=
  * 128, Hv/Hk <= 8, conv_width <= 8, ssm dtype f32 or bf16, conv dtype f32 or
  * bf16; else UNSUPPORTED.

@@ -55,7 +55,7 @@ template <> struct VecElem<__nv_bfloat16> {
   }
 };
 
-// Fused decode as a persistent, warp-specialised, TMA-pipelined kernel.
+// Fused decode as a persistent, warp-specialised, pipelined kernel.
 //
 // Work item = (row i, q/k head g): the G = Hv/Hk v heads that share q/k head g.
 // One CTA owns every conv channel of its item (q_g, k_g, and the v channels of
@@ -63,22 +63,23 @@ template <> struct VecElem<__nv_bfloat16> {
 // b, b + grid, ... ; their state tiles (TR rows of one head, <= 32 KiB) stream
 // through a ring of NS shared-memory stages.  Three roles:
 //  * producer warp (one lane): keeps NS tile loads in flight (cp.async.bulk, a
-//    `full` mbarrier per stage) and the raw conv inputs of the next two items
-//    in a double buffer (`cfull`); when the tile warps release a stage
-//    (`empty`) it bulk-stores the tile back through the page stride and refills
-//    the stage once the previous store has left shared memory;
+//    `full` mbarrier per stage); when the tile warps release a stage (`empty`)
+//    it bulk-stores the tile back through the page stride and refills the
+//    stage once the previous store has left shared memory;
 //  * conv warps (kConvThreads): one item ahead of the tile warps, run the conv
-//    update of the item's channels, write the new conv state, L2-normalise q
-//    and k and leave q, k, v, alpha, beta and k.q in a double-buffered y area
+//    update of the item's channels -- each thread owns 8-channel groups whose
+//    inputs it prefetches two items ahead with cp.async and whose new conv
+//    state it writes back with 16-byte stores -- then L2-normalise q and k and
+//    leave q, k, v, alpha, beta and k.q in a double-buffered y area
 //    (`yfull` / `yempty`);
 //  * tile warps (kConsumers): each landed tile in place -- 8 threads per state
-//    row on 16-byte vectors, up to RPT rows per thread at once:
-//    u = S_r.k, w = S_r.q, d = b (v_r - a u), S'_r = a S_r + d k,
-//    o_r = a w + d (k.q).
-// Only the conv and ssm views of a page are addressed.  Every mbarrier wait is
-// bounded: on expiry the role records LSC_ERR_DEV_TIMEOUT and returns; the
-// other roles' waits then expire in turn, and the producer waits (bounded) for
-// every copy it issued before returning.
+//    row on 16-byte vectors: u = S_r.k, w = S_r.q, d = b (v_r - a u),
+//    S'_r = a S_r + d k, o_r = a w + d (k.q).
+// The conv warps keep clear of the TMA unit, whose queue the 32 KiB tile
+// copies fill.  Only the conv and ssm views of a page are addressed.  Every
+// mbarrier wait is bounded: on expiry the role records LSC_ERR_DEV_TIMEOUT and
+// returns; the other roles' waits then expire in turn, and the producer waits
+// (bounded) for every copy it issued before returning.
 constexpr int kMaxStages = 8;
 constexpr int kConvBufs = 3;  // raw conv-input ring of the conv warps
 constexpr int kConsumers = 512;
@@ -106,7 +107,7 @@ __host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + 
 // y area of an item: q (dk), k (dk), v (G dv), alpha (G), beta (G), k.q (1).
 struct DecodeGeom {
   int nch, TR, TPH, TPG, NS, y_ab, y_kq;
-  int64_t stage_stride, conv_buf, off_st, off_xs, off_ws, off_conv, ys_buf, off_ys, off_info, total;
+  int64_t stage_stride, conv_buf, off_conv, ys_buf, off_ys, off_info, total;
   __host__ __device__ DecodeGeom(int dk, int es, int dv, int G, int W, int esc, int ns) {
     nch = 2 * dk + G * dv;
     const int64_t row_bytes = (int64_t)dk * es;
@@ -119,10 +120,7 @@ struct DecodeGeom {
     y_ab = nch;
     y_kq = nch + 2 * G;
     stage_stride = align_up((int64_t)TR * row_bytes, 128);
-    off_st = 0;
-    off_xs = align_up((int64_t)nch * (W - 1) * esc, 16);
-    off_ws = off_xs + align_up((int64_t)nch * esc, 16);
-    conv_buf = align_up(off_ws + (int64_t)nch * W * esc, 128);
+    conv_buf = align_up((int64_t)nch * 2 * W * esc, 128);  // per channel: W-1 state, x, W weights
     off_conv = (int64_t)NS * stage_stride;
     ys_buf = align_up((int64_t)(nch + 2 * G + 1) * 4, 128);
     off_ys = off_conv + kConvBufs * conv_buf;
@@ -154,13 +152,13 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
   using Sh = DecodeShape<DK, TS>;
   using EC = Elem<TC>;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], cfull[kConvBufs], yfull[2], yempty[2];
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], yfull[2], yempty[2];
   __shared__ float red[3][kConvThreads / 32];
 
   const int tid = threadIdx.x;
   const int W = CW ? CW : p.conv_width, C = p.conv_dim, dv = p.dv, G = p.group, Hk = p.Hk;
   constexpr int esc = (int)sizeof(TC);
-  const bool tma_conv = p.conv_tma != 0;
+  const bool vec = CW != 0 && p.conv_vec != 0;
   const DecodeGeom D(DK, Sh::ES, dv, G, W, esc, p.stages);
   const int NS = D.NS;
   const int n_items = p.n * Hk;
@@ -184,7 +182,6 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kConvBufs; ++s) mbar_init(&cfull[s], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&yfull[s], 1);
       mbar_init(&yempty[s], 1);
@@ -247,57 +244,40 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
   if (tid >= kConsumers) {
     // ------------------------------------------------------------ conv warps
     const int ct = tid - kConsumers;
-    // The conv leader (ct == 0) runs the conv warps' own copy pipeline: raw conv
-    // inputs of the next items into a ring of kConvBufs buffers, and bulk stores
-    // of each item's new conv state from its buffer.
-    int issued_convs = 0;
-    auto issue_conv = [&](int k) {
-      if (k >= my_items) return;
-      const int j = b + k * grid, i = j / Hk, g = j % Hk;
-      const int32_t slot = info_slot[k];
-      const bool warm = info_warm[k] != 0;
-      uint8_t *buf = smem + D.off_conv + (k % kConvBufs) * D.conv_buf;
-      const uint32_t bytes = (slot >= 0 && tma_conv) ? (uint32_t)(D.nch * ((warm ? W - 1 : 0) + 1 + W) * esc) : 0u;
-      mbar_arrive_expect_tx(&cfull[k % kConvBufs], bytes);
-      if (bytes) {
-        const uint8_t *page = p.layer + (int64_t)slot * p.page;
-        const int c0[3] = {g * DK, Hk * DK + g * DK, 2 * Hk * DK + g * G * dv};
-        const int cn[3] = {DK, DK, G * dv};
-        const int cl0[3] = {0, DK, 2 * DK};
-        for (int sgm = 0; sgm < 3; ++sgm) {
+    // Vector path (conv width fixed at compile time, 16-byte aligned channel
+    // groups): thread ct owns the 8-channel groups ct, ct + kConvThreads, ...;
+    // it prefetches each group's conv state, x and weights two items ahead with
+    // cp.async into its own slots of a kConvBufs-deep ring, reads them back
+    // itself, and writes the group's new conv state straight to the page.
+    // Other shapes read the conv inputs from global memory channel by channel.
+    constexpr int WW = CW ? CW : 2;
+    constexpr int NSV = 8 * (WW - 1) * esc / 16, NXV = 8 * esc / 16, NWV = 8 * WW * esc / 16;
+    constexpr int NGV = NSV + NXV + NWV;  // 16-byte vectors of one group
+    static_assert(CW == 0 || (8 * (WW - 1) * esc % 16 == 0 && 8 * WW * esc % 16 == 0), "vector conv layout");
+    auto first_channel = [&](int g, int cl0) {
+      return cl0 < DK ? g * DK + cl0 : (cl0 < 2 * DK ? Hk * DK + g * DK + (cl0 - DK) : 2 * Hk * DK + g * G * dv + (cl0 - 2 * DK));
+    };
+    auto prefetch = [&](int k) {
+      if (vec && k < my_items && info_slot[k] >= 0) {
+        const int j = b + k * grid, i = j / Hk, g = j % Hk;
+        const bool warm = info_warm[k] != 0;
+        const uint8_t *page = p.layer + (int64_t)info_slot[k] * p.page;
+        uint8_t *buf = smem + D.off_conv + (k % kConvBufs) * D.conv_buf;
+        for (int grp = ct; grp < D.nch / 8; grp += kConvThreads) {
+          const int c = first_channel(g, grp * 8);
+          uint8_t *dst = buf + (int64_t)grp * NGV * 16;
           if (warm)
-            bulk_g2s(buf + D.off_st + (int64_t)cl0[sgm] * (W - 1) * esc, page + (int64_t)c0[sgm] * (W - 1) * esc,
-                     (uint32_t)(cn[sgm] * (W - 1) * esc), &cfull[k % kConvBufs]);
-          bulk_g2s(buf + D.off_xs + (int64_t)cl0[sgm] * esc, (const uint8_t *)p.x + ((int64_t)i * C + c0[sgm]) * esc,
-                   (uint32_t)(cn[sgm] * esc), &cfull[k % kConvBufs]);
-          bulk_g2s(buf + D.off_ws + (int64_t)cl0[sgm] * W * esc, (const uint8_t *)p.w + (int64_t)c0[sgm] * W * esc,
-                   (uint32_t)(cn[sgm] * W * esc), &cfull[k % kConvBufs]);
+            for (int v = 0; v < NSV; ++v) cp_async16(dst + v * 16, page + (int64_t)c * (WW - 1) * esc + v * 16);
+          for (int v = 0; v < NXV; ++v)
+            cp_async16(dst + (NSV + v) * 16, (const uint8_t *)p.x + ((int64_t)i * C + c) * esc + v * 16);
+          for (int v = 0; v < NWV; ++v)
+            cp_async16(dst + (NSV + NXV + v) * 16, (const uint8_t *)p.w + (int64_t)c * WW * esc + v * 16);
         }
       }
-      issued_convs = k + 1;
+      cp_async_commit();  // one group per item, empty or not
     };
-    auto store_conv_state = [&](int k) {
-      const int32_t slot = info_slot[k];
-      if (slot >= 0 && tma_conv) {  // unaligned shapes store with plain writes
-        const int g = (b + k * grid) % Hk;
-        uint8_t *page = p.layer + (int64_t)slot * p.page;
-        const uint8_t *buf = smem + D.off_conv + (k % kConvBufs) * D.conv_buf;
-        const int c0[3] = {g * DK, Hk * DK + g * DK, 2 * Hk * DK + g * G * dv};
-        const int cn[3] = {DK, DK, G * dv};
-        const int cl0[3] = {0, DK, 2 * DK};
-        for (int sgm = 0; sgm < 3; ++sgm)
-          bulk_s2g(page + (int64_t)c0[sgm] * (W - 1) * esc, buf + D.off_st + (int64_t)cl0[sgm] * (W - 1) * esc,
-                   (uint32_t)(cn[sgm] * (W - 1) * esc));
-      }
-      bulk_commit();
-    };
-    auto conv_drain = [&](int k_from) {
-      for (int kk = k_from; kk < issued_convs; ++kk)
-        mbar_wait_bounded(&cfull[kk % kConvBufs], (kk / kConvBufs) & 1, p.drain_limit_ns);
-      bulk_wait_read_all();
-    };
-    if (ct == 0)
-      for (int kk = 0; kk < kConvBufs; ++kk) issue_conv(kk);
+    prefetch(0);
+    prefetch(1);
     // alpha and beta of the next item, loaded one item ahead (threads < 2G)
     auto load_ab = [&](int k) -> float {
       if (ct >= 2 * G || k >= my_items) return 0.f;
@@ -316,36 +296,28 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
       float *ys = reinterpret_cast<float *>(smem + D.off_ys + (k & 1) * D.ys_buf);
       const float ab = ab_next;
       ab_next = load_ab(k + 1);
-      bool ok = mbar_wait_bounded(&cfull[k % kConvBufs], (k / kConvBufs) & 1, p.wait_limit_ns);
-      if (ok && k >= 2) ok = mbar_wait_bounded(&yempty[k & 1], ((k - 2) >> 1) & 1, p.wait_limit_ns);
+      prefetch(k + 2);
+      cp_async_wait<2>();  // this thread's copies of item k have landed
+      const bool ok = k < 2 || mbar_wait_bounded(&yempty[k & 1], ((k - 2) >> 1) & 1, p.wait_limit_ns);
       if (named_any<2, kConvThreads>(!ok)) {
-        if (ct == 0) {
-          report(p.status, LSC_ERR_DEV_TIMEOUT);
-          conv_drain(k);
-        }
+        if (ct == 0) report(p.status, LSC_ERR_DEV_TIMEOUT);
+        cp_async_wait<0>();
         return;
       }
       float sq = 0.f, sk = 0.f, sqk = 0.f;  // partial sums of this thread's q, k channels
       if (valid) {
-        uint8_t *stg = const_cast<uint8_t *>(cb) + D.off_st;
-        if (CW != 0 && tma_conv && D.nch % 8 == 0) {
-          // 8 consecutive channels per thread with 16-byte shared-memory accesses
-          constexpr int WW = CW ? CW : 2;
-          constexpr int NSV = 8 * (WW - 1) * esc / 16, NXV = 8 * esc / 16, NWV = 8 * WW * esc / 16;
-          static_assert(8 * (WW - 1) * esc % 16 == 0 && 8 * WW * esc % 16 == 0, "vector conv layout");
+        if (vec) {
           using VE = VecElem<TC>;
           for (int grp = ct; grp < D.nch / 8; grp += kConvThreads) {
             const int cl0 = grp * 8;
+            const uint4 *gp = reinterpret_cast<const uint4 *>(cb + (int64_t)grp * NGV * 16);
             uint4 sv[NSV], xv[NXV], wv[NWV];
-            uint4 *sp = reinterpret_cast<uint4 *>(stg + (int64_t)cl0 * (WW - 1) * esc);
-            const uint4 *xp = reinterpret_cast<const uint4 *>(cb + D.off_xs + (int64_t)cl0 * esc);
-            const uint4 *wp = reinterpret_cast<const uint4 *>(cb + D.off_ws + (int64_t)cl0 * WW * esc);
 #pragma unroll
-            for (int v = 0; v < NSV; ++v) sv[v] = warm ? sp[v] : make_uint4(0, 0, 0, 0);
+            for (int v = 0; v < NSV; ++v) sv[v] = warm ? gp[v] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int v = 0; v < NXV; ++v) xv[v] = xp[v];
+            for (int v = 0; v < NXV; ++v) xv[v] = gp[NSV + v];
 #pragma unroll
-            for (int v = 0; v < NWV; ++v) wv[v] = wp[v];
+            for (int v = 0; v < NWV; ++v) wv[v] = gp[NSV + NXV + v];
             uint4 nv[NSV];
             float y[8];
 #pragma unroll
@@ -360,8 +332,9 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
               for (int jj = 0; jj < WW - 1; ++jj)
                 VE::set_bits(nv, c * (WW - 1) + jj, jj < WW - 2 ? VE::bits(sv, c * (WW - 1) + jj + 1) : VE::bits(xv, c));
             }
+            uint4 *gst = reinterpret_cast<uint4 *>(page + (int64_t)first_channel(g, cl0) * (WW - 1) * esc);
 #pragma unroll
-            for (int v = 0; v < NSV; ++v) sp[v] = nv[v];
+            for (int v = 0; v < NSV; ++v) gst[v] = nv[v];
             float4 *yp = reinterpret_cast<float4 *>(ys + cl0);
             yp[0] = make_float4(y[0], y[1], y[2], y[3]);
             yp[1] = make_float4(y[4], y[5], y[6], y[7]);
@@ -374,53 +347,29 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
             }
           }
         } else {
-          // any conv width or alignment: one channel at a time
+          // any conv width or alignment: one channel at a time from global memory
           for (int cl = ct; cl < D.nch; cl += kConvThreads) {
-            const int c = cl < DK ? g * DK + cl
-                                  : (cl < 2 * DK ? Hk * DK + g * DK + (cl - DK) : 2 * Hk * DK + g * G * dv + (cl - 2 * DK));
+            const int c = first_channel(g, cl);
             float win[kMaxTaps];
 #pragma unroll
-            for (int jj = 0; jj < kMaxTaps - 1; ++jj) {
-              float v = 0.f;
-              if (jj < W - 1 && warm)
-                v = tma_conv ? EC::ld(stg, (int64_t)cl * (W - 1) + jj) : EC::ld(page, (int64_t)c * (W - 1) + jj);
-              win[jj] = v;
-            }
-            const float xv = tma_conv ? EC::ld(cb + D.off_xs, cl) : EC::ld(p.x, (int64_t)i * C + c);
+            for (int jj = 0; jj < kMaxTaps - 1; ++jj) win[jj] = (jj < W - 1 && warm) ? EC::ld(page, (int64_t)c * (W - 1) + jj) : 0.f;
+            const float xv = EC::ld(p.x, (int64_t)i * C + c);
             float acc = 0.f;
 #pragma unroll
-            for (int jj = 0; jj < kMaxTaps; ++jj) {
-              if (jj < W) {
-                const float wv = tma_conv ? EC::ld(cb + D.off_ws, (int64_t)cl * W + jj) : EC::ld(p.w, (int64_t)c * W + jj);
-                acc = fmaf(wv, jj == W - 1 ? xv : win[jj], acc);
-              }
-            }
+            for (int jj = 0; jj < kMaxTaps; ++jj)
+              if (jj < W) acc = fmaf(EC::ld(p.w, (int64_t)c * W + jj), jj == W - 1 ? xv : win[jj], acc);
             const float y = __fdividef(acc, 1.f + __expf(-acc));  // SiLU
             ys[cl] = y;
             if (cl < DK) sq = fmaf(y, y, sq);
             else if (cl < 2 * DK) sk = fmaf(y, y, sk);
 #pragma unroll
-            for (int jj = 0; jj < kMaxTaps - 1; ++jj) {
-              if (jj < W - 1) {
-                const float nv = jj < W - 2 ? win[jj + 1] : xv;
-                if (tma_conv) EC::st(stg, (int64_t)cl * (W - 1) + jj, nv);
-                else EC::st(page, (int64_t)c * (W - 1) + jj, nv);
-              }
-            }
+            for (int jj = 0; jj < kMaxTaps - 1; ++jj)
+              if (jj < W - 1) EC::st(page, (int64_t)c * (W - 1) + jj, jj < W - 2 ? win[jj + 1] : xv);
           }
         }
         if (ct < 2 * G) ys[D.y_ab + ct] = ab;
-        fence_proxy_async_smem();  // the producer bulk-stores the new conv state from staging
       }
-      named_sync<2, kConvThreads>();  // raw conv staging consumed, y written
-      if (ct == 0) {
-        store_conv_state(k);
-        // refill the previous item's buffer once its state store has left it
-        if (k >= 1 && k - 1 + kConvBufs < my_items) {
-          bulk_wait_read_one();
-          issue_conv(k - 1 + kConvBufs);
-        }
-      }
+      named_sync<2, kConvThreads>();  // raw y written
       if (valid) {
         // k . q needs the q and k channels of every thread
         for (int c = ct; c < DK; c += kConvThreads) sqk = fmaf(ys[c], ys[DK + c], sqk);
@@ -452,7 +401,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
       }
       if (ct == 0) mbar_arrive(&yfull[k & 1]);
     }
-    if (ct == 0) bulk_wait_read_all();
+    cp_async_wait<0>();
     return;
   }
 

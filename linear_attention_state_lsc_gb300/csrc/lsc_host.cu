@@ -488,14 +488,15 @@ int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, voi
   d.beta = a->beta;
   d.out = a->out;
   d.status = g.status;
-  // TMA staging of the conv inputs needs every segment (q/k/v channel ranges of
-  // the conv state, x and the weights) 16-byte aligned in start and length.
+  // The vector conv path reads and writes 8-channel groups of the conv state,
+  // x and the weights with 16-byte accesses: every segment (q/k/v channel
+  // ranges) must be 16-byte aligned in start and length.
   const int64_t esc = g.conv_dtype == LSC_BF16 ? 2 : 4, W = g.conv_width;
   const int64_t units[] = {g.dk * (W - 1) * esc, (int64_t)g.dv * (W - 1) * esc, g.dk * esc, (int64_t)g.dv * esc,
                            (int64_t)g.conv_dim * esc, g.dk * W * esc, (int64_t)g.dv * W * esc};
   bool tma = ((uintptr_t)a->x % 16) == 0 && ((uintptr_t)a->conv_weight % 16) == 0;
   for (int64_t u : units) tma = tma && (u % 16) == 0;
-  d.conv_tma = tma ? 1 : 0;
+  d.conv_vec = tma ? 1 : 0;
   d.wait_limit_ns = fault("timeout0") ? 0 : kWaitLimitNs;
   d.drain_limit_ns = kWaitLimitNs;
   d.num_sms = p->num_sms;

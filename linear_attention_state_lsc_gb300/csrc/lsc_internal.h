@@ -78,7 +78,7 @@ struct DecodeParams {
   const float *alpha, *beta;
   float *out;
   int32_t *status;
-  int32_t conv_tma;         // conv segments 16-byte aligned: staged by TMA bulk copies
+  int32_t conv_vec;         // conv segments 16-byte aligned: 8-channel vector path
   uint64_t wait_limit_ns;   // bound of each mbarrier wait (0: give up at once)
   uint64_t drain_limit_ns;  // bound of the wait for in-flight copies after a timeout
   int32_t num_sms;

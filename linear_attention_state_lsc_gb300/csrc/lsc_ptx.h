@@ -98,6 +98,20 @@ __device__ __forceinline__ void bulk_wait_read_one() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through the load/store unit
+// (per-thread commit groups; no TMA involvement).
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's most recent cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Cluster-wide barrier without a release fence: orders execution only.
 __device__ __forceinline__ void cluster_barrier_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
