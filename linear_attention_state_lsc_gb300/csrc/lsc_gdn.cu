@@ -20,26 +20,71 @@ int launch_decode_bf16(const DecodeParams &p, int dk, cudaStream_t s);
 namespace {
 
 // ---------------------------------------------------------------------------
-// Token-by-token recurrence.  Grid (Hv, n_seq), one CTA per (sequence, v head);
-// row r of the head's state lives in the registers of TPR threads (CPT columns
-// each) for the whole sequence.  Tokens are staged in shared memory TT at a
-// time; k . q of each token is computed once per tile.
-constexpr int kTileTokens = 16;
+// Token-by-token recurrence.  Grid (Hv, n_seq), one CTA per (sequence, v head),
+// 2 CTAs per SM.  Each thread keeps two rows of the head's state (CPT columns
+// of each, TPR threads per row) in registers for the whole sequence.
+//
+// The state is held scaled, S = gamma * Shat, so that a token costs three
+// FMAs per element: Shat.k and Shat.q for the row's prediction and read-out,
+// then Shat += (d / gamma') k with gamma' = alpha * gamma.  Per row
+//   u = gamma (Shat.k),  d = beta (v - alpha u),  o = gamma' (Shat.q) + d (k.q),
+// which is S' = alpha S + d k^T and o = S' q.  When gamma' falls below 2^-32
+// (or alpha is 0) the scale is folded into Shat and gamma restarts at 1; at the
+// end the state is stored as gamma * Shat.
+// Tokens are staged TT at a time with cp.async, double-buffered, and k.q of
+// each token is formed once per tile.  When there are at most kRankedSeqs
+// sequences, CTAs take them longest first so that long sequences do not finish
+// last.
+constexpr int kTileTokens = 32;
+constexpr int kRecThreads = 256;
+constexpr int kRankedSeqs = 256;
+
+template <int DK>
+struct RecShape {
+  static constexpr int CPT = DK < 32 ? DK : 32;  // columns per thread
+  static constexpr int TPR = DK / CPT;           // threads per row
+  static constexpr int NV4 = CPT / 4;            // float4 vectors per thread per row
+};
+
+__host__ __device__ inline int64_t rec_smem_bytes(int dk, int dv) {
+  // two buffers of: q, k [TT][dk], v [TT][dv], alpha, beta, k.q [TT]
+  return 2 * ((int64_t)kTileTokens * (2 * dk + dv) + 3 * kTileTokens) * 4;
+}
 
 template <int DK, typename TS>
-__global__ void __launch_bounds__(512, 1) recurrent_kernel(const __grid_constant__ RecurrentParams p) {
-  constexpr int CPT = DK < 32 ? DK : 32;
-  constexpr int TPR = DK / CPT;
-  constexpr int NV4 = CPT / 4;
+__global__ void __launch_bounds__(kRecThreads, 2) recurrent_kernel(const __grid_constant__ RecurrentParams p) {
+  using R = RecShape<DK>;
   constexpr int TT = kTileTokens;
-  __shared__ __align__(16) float sq[TT][DK];
-  __shared__ __align__(16) float sk[TT][DK];
-  __shared__ float sv[TT][kMaxDv];
-  __shared__ float sa[TT], sb[TT], skq[TT];
+  extern __shared__ __align__(16) float rsm[];
+  __shared__ int32_t s_len[kRankedSeqs];
+  __shared__ int32_t s_seq;
 
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  const int h = blockIdx.x, i = blockIdx.y;
-  const int g = h / p.group;
+  const int tid = threadIdx.x;
+  const int h = blockIdx.x, g = h / p.group;
+  const int dv = p.dv;
+  const int buf_floats = TT * (2 * DK + dv) + 3 * TT;
+  auto q_s = [&](int b) { return rsm + b * buf_floats; };
+  auto k_s = [&](int b) { return rsm + b * buf_floats + TT * DK; };
+  auto v_s = [&](int b) { return rsm + b * buf_floats + 2 * TT * DK; };
+  auto a_s = [&](int b) { return rsm + b * buf_floats + TT * (2 * DK + dv); };
+  auto b_s = [&](int b) { return a_s(b) + TT; };
+  auto kq_s = [&](int b) { return a_s(b) + 2 * TT; };
+
+  // which sequence: longest first when the sequences are few enough to rank
+  int i = blockIdx.y;
+  if (p.n_seq <= kRankedSeqs) {
+    for (int s = tid; s < p.n_seq; s += kRecThreads) s_len[s] = p.cu[s + 1] - p.cu[s];
+    __syncthreads();
+    for (int s = tid; s < p.n_seq; s += kRecThreads) {
+      const int ls = s_len[s];
+      int rank = 0;
+      for (int jj = 0; jj < p.n_seq; ++jj) rank += (s_len[jj] > ls) || (s_len[jj] == ls && jj < s);
+      if (rank == (int)blockIdx.y) s_seq = s;
+    }
+    __syncthreads();
+    i = s_seq;
+  }
+
   const int32_t slot = p.idx[i];
   const bool bad = slot >= p.num_slots;
   const bool valid = slot >= 0 && !bad;
@@ -50,105 +95,164 @@ __global__ void __launch_bounds__(512, 1) recurrent_kernel(const __grid_constant
     if (tid == 0 && h == 0) report(p.status, LSC_ERR_INVALID_ARG);
     return;
   }
-  const int dv = p.dv;
-  const int r = tid / TPR, lr = tid % TPR;
-  const bool rv = r < dv;
-
   if (!valid) {  // uniform over the CTA
-    for (int64_t e = tid; e < (int64_t)(t1 - t0) * dv; e += nthr) {
+    for (int64_t e = tid; e < (int64_t)(t1 - t0) * dv; e += kRecThreads) {
       const int64_t t = t0 + e / dv;
       p.out[(t * p.Hv + h) * dv + e % dv] = 0.f;
     }
     return;
   }
 
-  TS *Srow = (TS *)(p.layer + (int64_t)slot * p.page + p.ssm_off) + ((int64_t)h * dv + (rv ? r : 0)) * DK;
-  float S[CPT];
-#pragma unroll
-  for (int j = 0; j < NV4; ++j) {
-    const int c0 = (j * TPR + lr) * 4;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float v = 0.f;
-      if (warm && rv) {
-        if constexpr (sizeof(TS) == 4) v = ((const float *)Srow)[c0 + e];
-        else v = bf16_bits_to_float(((const uint16_t *)Srow)[c0 + e]);
-      }
-      S[j * 4 + e] = v;
-    }
-  }
+  const int lr = tid % R::TPR;
+  const int rp = tid / R::TPR;     // row pair
+  const int rh = (dv + 1) / 2;     // rows rp and rp + rh
+  const int rows[2] = {rp, rp + rh};
+  bool rv[2];
+  rv[0] = rp < rh && rows[0] < dv;
+  rv[1] = rp < rh && rows[1] < dv;
 
-  const int nwarps = (nthr + 31) >> 5, warp = tid >> 5, lane = tid & 31;
-  for (int tb = t0; tb < t1; tb += TT) {
-    const int nt = t1 - tb < TT ? t1 - tb : TT;
-    __syncthreads();
-    for (int e = tid; e < nt * (DK / 4); e += nthr) {
-      const int tt = e / (DK / 4), c4 = e % (DK / 4);
-      const int64_t src = ((int64_t)(tb + tt) * p.Hk + g) * DK + c4 * 4;
-      *(float4 *)&sq[tt][c4 * 4] = *(const float4 *)(p.q + src);
-      *(float4 *)&sk[tt][c4 * 4] = *(const float4 *)(p.k + src);
-    }
-    for (int e = tid; e < nt * dv; e += nthr) {
-      const int tt = e / dv, c = e % dv;
-      sv[tt][c] = p.v[((int64_t)(tb + tt) * p.Hv + h) * dv + c];
-    }
-    if (tid < nt) {
-      sa[tid] = p.alpha[(int64_t)(tb + tid) * p.Hv + h];
-      sb[tid] = p.beta[(int64_t)(tb + tid) * p.Hv + h];
-    }
-    __syncthreads();
-    for (int tt = warp; tt < nt; tt += nwarps) {
-      float acc = 0.f;
-      for (int c = lane; c < DK; c += 32) acc = fmaf(sq[tt][c], sk[tt][c], acc);
+  // state rows into registers
+  float S[2][R::CPT];
+  TS *Sg = reinterpret_cast<TS *>(p.layer + (int64_t)slot * p.page + p.ssm_off) + (int64_t)h * dv * DK;
 #pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-      if (lane == 0) skq[tt] = acc;
-    }
-    __syncthreads();
-    for (int tt = 0; tt < nt; ++tt) {
-      // four partial sums per dot product keep the FMA chains short
-      float u4[4] = {0.f, 0.f, 0.f, 0.f}, w4[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int q = 0; q < 2; ++q) {
 #pragma unroll
-      for (int j = 0; j < NV4; ++j) {
-        const int c0 = (j * TPR + lr) * 4;
-        const float4 k4 = *(const float4 *)&sk[tt][c0];
-        const float4 q4 = *(const float4 *)&sq[tt][c0];
-        u4[0] = fmaf(S[j * 4], k4.x, u4[0]); u4[1] = fmaf(S[j * 4 + 1], k4.y, u4[1]);
-        u4[2] = fmaf(S[j * 4 + 2], k4.z, u4[2]); u4[3] = fmaf(S[j * 4 + 3], k4.w, u4[3]);
-        w4[0] = fmaf(S[j * 4], q4.x, w4[0]); w4[1] = fmaf(S[j * 4 + 1], q4.y, w4[1]);
-        w4[2] = fmaf(S[j * 4 + 2], q4.z, w4[2]); w4[3] = fmaf(S[j * 4 + 3], q4.w, w4[3]);
-      }
-      float u = (u4[0] + u4[1]) + (u4[2] + u4[3]);
-      float wq = (w4[0] + w4[1]) + (w4[2] + w4[3]);
-#pragma unroll
-      for (int m = TPR / 2; m >= 1; m >>= 1) {
-        u += __shfl_xor_sync(0xffffffffu, u, m);
-        wq += __shfl_xor_sync(0xffffffffu, wq, m);
-      }
-      const float a = sa[tt], b = sb[tt];
-      const float vr = rv ? sv[tt][r] : 0.f;
-      const float d = b * (vr - a * u);
-#pragma unroll
-      for (int j = 0; j < NV4; ++j) {
-        const int c0 = (j * TPR + lr) * 4;
-        const float4 k4 = *(const float4 *)&sk[tt][c0];
-        S[j * 4] = fmaf(a, S[j * 4], d * k4.x);
-        S[j * 4 + 1] = fmaf(a, S[j * 4 + 1], d * k4.y);
-        S[j * 4 + 2] = fmaf(a, S[j * 4 + 2], d * k4.z);
-        S[j * 4 + 3] = fmaf(a, S[j * 4 + 3], d * k4.w);
-      }
-      if (rv && lr == 0) p.out[((int64_t)(tb + tt) * p.Hv + h) * dv + r] = fmaf(a, wq, d * skq[tt]);
-    }
-  }
-
-  if (rv) {
-#pragma unroll
-    for (int j = 0; j < NV4; ++j) {
-      const int c0 = (j * TPR + lr) * 4;
+    for (int jv = 0; jv < R::NV4; ++jv) {
+      const int c0 = (jv * R::TPR + lr) * 4;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if constexpr (sizeof(TS) == 4) ((float *)Srow)[c0 + e] = S[j * 4 + e];
-        else ((uint16_t *)Srow)[c0 + e] = float_to_bf16_bits(S[j * 4 + e]);
+        float v = 0.f;
+        if (warm && rv[q]) {
+          if constexpr (sizeof(TS) == 4) v = ((const float *)Sg)[(int64_t)rows[q] * DK + c0 + e];
+          else v = bf16_bits_to_float(((const uint16_t *)Sg)[(int64_t)rows[q] * DK + c0 + e]);
+        }
+        S[q][jv * 4 + e] = v;
+      }
+    }
+  }
+  float gam = 1.f;
+
+  const bool v16 = (dv % 4 == 0) && (((uintptr_t)p.v & 15) == 0);
+  auto issue_tile = [&](int tb, int bsel) {
+    const int nt = min(TT, t1 - tb);
+    float *qd = q_s(bsel), *kd = k_s(bsel), *vd = v_s(bsel);
+    for (int e = tid; e < nt * (DK / 4); e += kRecThreads) {
+      const int tt = e / (DK / 4), c4 = e % (DK / 4);
+      const int64_t src = ((int64_t)(tb + tt) * p.Hk + g) * DK + c4 * 4;
+      cp_async16(qd + tt * DK + c4 * 4, p.q + src);
+      cp_async16(kd + tt * DK + c4 * 4, p.k + src);
+    }
+    if (v16) {
+      for (int e = tid; e < nt * (dv / 4); e += kRecThreads) {
+        const int tt = e / (dv / 4), c4 = e % (dv / 4);
+        cp_async16(vd + tt * dv + c4 * 4, p.v + ((int64_t)(tb + tt) * p.Hv + h) * dv + c4 * 4);
+      }
+    } else {
+      for (int e = tid; e < nt * dv; e += kRecThreads) {
+        const int tt = e / dv, c = e % dv;
+        cp_async4(vd + tt * dv + c, p.v + ((int64_t)(tb + tt) * p.Hv + h) * dv + c);
+      }
+    }
+    if (tid < nt) {
+      cp_async4(a_s(bsel) + tid, p.alpha + (int64_t)(tb + tid) * p.Hv + h);
+      cp_async4(b_s(bsel) + tid, p.beta + (int64_t)(tb + tid) * p.Hv + h);
+    }
+  };
+
+  if (t0 < t1) issue_tile(t0, 0);
+  cp_async_commit();
+  const int warp = tid >> 5, lane = tid & 31;
+  int bsel = 0;
+  for (int tb = t0; tb < t1; tb += TT, bsel ^= 1) {
+    const int nt = min(TT, t1 - tb);
+    if (tb + TT < t1) issue_tile(tb + TT, bsel ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // this thread's copies of the current tile have landed
+    __syncthreads();
+    const float *qd = q_s(bsel), *kd = k_s(bsel), *vd = v_s(bsel);
+    for (int tt = warp; tt < nt; tt += kRecThreads / 32) {
+      float acc = 0.f;
+      for (int c = lane; c < DK; c += 32) acc = fmaf(qd[tt * DK + c], kd[tt * DK + c], acc);
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+      if (lane == 0) kq_s(bsel)[tt] = acc;
+    }
+    __syncthreads();
+    const float *al = a_s(bsel), *be = b_s(bsel), *kq = kq_s(bsel);
+    for (int tt = 0; tt < nt; ++tt) {
+      const float *kt = kd + tt * DK, *qt = qd + tt * DK;
+      float kr[R::CPT];
+      float ua[2] = {0.f, 0.f}, ub[2] = {0.f, 0.f}, wa[2] = {0.f, 0.f}, wb[2] = {0.f, 0.f};
+#pragma unroll
+      for (int jv = 0; jv < R::NV4; ++jv) {
+        const int c0 = (jv * R::TPR + lr) * 4;
+        const float4 k4 = *reinterpret_cast<const float4 *>(kt + c0);
+        const float4 q4 = *reinterpret_cast<const float4 *>(qt + c0);
+        kr[jv * 4] = k4.x; kr[jv * 4 + 1] = k4.y; kr[jv * 4 + 2] = k4.z; kr[jv * 4 + 3] = k4.w;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float *s = S[q] + jv * 4;
+          ua[q] = fmaf(s[0], k4.x, ua[q]); ub[q] = fmaf(s[1], k4.y, ub[q]);
+          ua[q] = fmaf(s[2], k4.z, ua[q]); ub[q] = fmaf(s[3], k4.w, ub[q]);
+          wa[q] = fmaf(s[0], q4.x, wa[q]); wb[q] = fmaf(s[1], q4.y, wb[q]);
+          wa[q] = fmaf(s[2], q4.z, wa[q]); wb[q] = fmaf(s[3], q4.w, wb[q]);
+        }
+      }
+      float u[2] = {ua[0] + ub[0], ua[1] + ub[1]}, w[2] = {wa[0] + wb[0], wa[1] + wb[1]};
+#pragma unroll
+      for (int m = R::TPR / 2; m >= 1; m >>= 1) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          u[q] += __shfl_xor_sync(0xffffffffu, u[q], m);
+          w[q] += __shfl_xor_sync(0xffffffffu, w[q], m);
+        }
+      }
+      const float a = al[tt], b = be[tt];
+      float gn = a * gam;  // gamma' = alpha gamma
+      float d[2], o[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float vr = rv[q] ? vd[tt * dv + rows[q]] : 0.f;
+        d[q] = b * (vr - a * (gam * u[q]));
+        o[q] = fmaf(gn, w[q], d[q] * kq[tt]);
+      }
+      if (gn < 0x1p-32f) {  // fold the scale into Shat (uniform over the CTA)
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int c = 0; c < R::CPT; ++c) S[q][c] *= gn;
+        gn = 1.f;
+      }
+      const float inv = 1.f / gn;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float e = d[q] * inv;
+#pragma unroll
+        for (int c = 0; c < R::CPT; ++c) S[q][c] = fmaf(e, kr[c], S[q][c]);
+      }
+      gam = gn;
+      if (lr == 0) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (rv[q]) p.out[((int64_t)(tb + tt) * p.Hv + h) * dv + rows[q]] = o[q];
+      }
+    }
+    __syncthreads();  // the next iteration refills this buffer
+  }
+  cp_async_wait<0>();
+
+  // final state = gamma * Shat
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    if (!rv[q]) continue;
+#pragma unroll
+    for (int jv = 0; jv < R::NV4; ++jv) {
+      const int c0 = (jv * R::TPR + lr) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float v = gam * S[q][jv * 4 + e];
+        if constexpr (sizeof(TS) == 4) ((float *)Sg)[(int64_t)rows[q] * DK + c0 + e] = v;
+        else ((uint16_t *)Sg)[(int64_t)rows[q] * DK + c0 + e] = float_to_bf16_bits(v);
       }
     }
   }
@@ -156,11 +260,19 @@ __global__ void __launch_bounds__(512, 1) recurrent_kernel(const __grid_constant
 
 template <int DK, typename TS>
 int launch_recurrent_t(const RecurrentParams &p, cudaStream_t s) {
-  constexpr int CPT = DK < 32 ? DK : 32;
-  constexpr int TPR = DK / CPT;
-  int threads = (p.dv * TPR + 31) / 32 * 32;
-  if (threads > 512) return LSC_ERR_UNSUPPORTED;
-  recurrent_kernel<DK, TS><<<dim3(p.Hv, p.n_seq, 1), threads, 0, s>>>(p);
+  using R = RecShape<DK>;
+  if ((p.dv + 1) / 2 * R::TPR > kRecThreads) return LSC_ERR_UNSUPPORTED;
+  const int64_t smem = rec_smem_bytes(DK, p.dv);
+  static int configured = 0;
+  if (configured < smem) {
+    if (cudaFuncSetAttribute(recurrent_kernel<DK, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return LSC_ERR_UNSUPPORTED;
+    }
+    configured = (int)smem;
+  }
+  recurrent_kernel<DK, TS><<<dim3(p.Hv, p.n_seq, 1), kRecThreads, (size_t)smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;
   return LSC_OK;
 }

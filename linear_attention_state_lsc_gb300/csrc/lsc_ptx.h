@@ -104,6 +104,11 @@ __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src_gmem)
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared.
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src_gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's most recent cp.async groups are pending.
