@@ -83,6 +83,7 @@ template <> struct VecElem<__nv_bfloat16> {
 constexpr int kMaxStages = 8;
 constexpr int kConvBufs = 3;  // raw conv-input ring of the conv warps
 constexpr int kConsumers = 512;
+constexpr int kTileWarps = kConsumers / 32;  // arrivals that release a stage or a y buffer
 constexpr int kConvThreads = 96;  // 20 warps in all: 96 registers per thread
 constexpr int kDecodeBlock = kConsumers + kConvThreads + 32;
 constexpr int kProducer = kConsumers + kConvThreads;
@@ -180,11 +181,11 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kTileWarps);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&yfull[s], 1);
-      mbar_init(&yempty[s], 1);
+      mbar_init(&yempty[s], kTileWarps);
     }
     fence_mbar_init();
   }
@@ -406,35 +407,39 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
   }
 
   // -------------------------------------------------------------- tile warps
-  const int lr = tid % Sh::TPR;
+  // Each warp runs on its own: it waits for y and for each tile itself and
+  // releases them with one arrival per warp, so no CTA-wide barrier paces the
+  // tile loop and the warps drift apart, hiding one another's latencies.
+  constexpr int NP = Sh::EPV / 2;  // float pairs per 16-byte vector
+  const int lr = tid % Sh::TPR, lane = tid & 31;
   int t = 0;
   for (int k = 0; k < my_items; ++k) {
     const int j = b + k * grid, i = j / Hk, g = j % Hk;
     const bool valid = info_slot[k] >= 0;
     const bool warm = info_warm[k] != 0;
     const float *ys = reinterpret_cast<const float *>(smem + D.off_ys + (k & 1) * D.ys_buf);
-    if (named_any<1, kConsumers>(!mbar_wait_bounded(&yfull[k & 1], (k >> 1) & 1, p.wait_limit_ns))) {
-      if (tid == 0) report(p.status, LSC_ERR_DEV_TIMEOUT);
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&yfull[k & 1], (k >> 1) & 1, p.wait_limit_ns))) {
+      if (lane == 0) report(p.status, LSC_ERR_DEV_TIMEOUT);
       return;
     }
     float kq = 0.f;
-    float kreg[Sh::NC], qreg[Sh::NC];
+    uint64_t k2[Sh::NC / 2], q2[Sh::NC / 2];  // this thread's columns of k and q, in pairs
     if (valid) {
       kq = ys[D.y_kq];
 #pragma unroll
       for (int jj = 0; jj < Sh::NV; ++jj) {
         const int c0v = (jj * Sh::TPR + lr) * Sh::EPV;
 #pragma unroll
-        for (int e = 0; e < Sh::EPV; ++e) {
-          qreg[jj * Sh::EPV + e] = ys[c0v + e];
-          kreg[jj * Sh::EPV + e] = ys[DK + c0v + e];
+        for (int e = 0; e < NP; ++e) {
+          q2[jj * NP + e] = *reinterpret_cast<const uint64_t *>(ys + c0v + 2 * e);
+          k2[jj * NP + e] = *reinterpret_cast<const uint64_t *>(ys + DK + c0v + 2 * e);
         }
       }
     }
     for (int tl = 0; tl < D.TPG; ++tl, ++t) {
       const int stage = t % NS;
-      if (named_any<1, kConsumers>(!mbar_wait_bounded(&full[stage], (t / NS) & 1, p.wait_limit_ns))) {
-        if (tid == 0) report(p.status, LSC_ERR_DEV_TIMEOUT);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[stage], (t / NS) & 1, p.wait_limit_ns))) {
+        if (lane == 0) report(p.status, LSC_ERR_DEV_TIMEOUT);
         return;
       }
       const int hl = tl / D.TPH, rb = tl % D.TPH;
@@ -443,6 +448,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
       float *o = p.out + ((int64_t)i * p.Hv + g * G + hl) * dv + (int64_t)rb * D.TR;
       if (valid) {
         const float a = ys[D.y_ab + hl], bb = ys[D.y_ab + G + hl];
+        const uint64_t a2 = f2_pack(a, a);
         const float *vs = ys + 2 * DK + hl * dv + rb * D.TR;
         const int npass = (rows + Sh::RPP * Sh::RPT - 1) / (Sh::RPP * Sh::RPT);
         for (int ps = 0; ps < npass; ++ps) {
@@ -462,21 +468,22 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
           }
 #pragma unroll
           for (int q = 0; q < Sh::RPT; ++q) {
-            float u0 = 0.f, u1 = 0.f, w0 = 0.f, w1 = 0.f;
+            uint64_t u2 = 0, w2 = 0;  // (even, odd) column partial sums of S_r.k and S_r.q
 #pragma unroll
             for (int jj = 0; jj < Sh::NV; ++jj) {
-              float f[Sh::EPV];
-              StateVec<TS>::unpack(sv[q][jj], f);
+              uint64_t f[NP];
+              StatePairs<TS>::unpack(sv[q][jj], f);
 #pragma unroll
-              for (int e = 0; e < Sh::EPV; e += 2) {
-                u0 = fmaf(f[e], kreg[jj * Sh::EPV + e], u0);
-                u1 = fmaf(f[e + 1], kreg[jj * Sh::EPV + e + 1], u1);
-                w0 = fmaf(f[e], qreg[jj * Sh::EPV + e], w0);
-                w1 = fmaf(f[e + 1], qreg[jj * Sh::EPV + e + 1], w1);
+              for (int e = 0; e < NP; ++e) {
+                u2 = f2_fma(f[e], k2[jj * NP + e], u2);
+                w2 = f2_fma(f[e], q2[jj * NP + e], w2);
               }
             }
-            u[q] = u0 + u1;
-            wq[q] = w0 + w1;
+            float ul, uh, wl, wh;
+            f2_unpack(u2, ul, uh);
+            f2_unpack(w2, wl, wh);
+            u[q] = ul + uh;
+            wq[q] = wl + wh;
           }
 #pragma unroll
           for (int m = Sh::TPR / 2; m >= 1; m >>= 1) {
@@ -490,13 +497,15 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
           for (int q = 0; q < Sh::RPT; ++q) {
             const float d = bb * ((rv[q] ? vs[rr[q]] : 0.f) - a * u[q]);
             if (rv[q]) {
+              const uint64_t d2 = f2_pack(d, d);
 #pragma unroll
               for (int jj = 0; jj < Sh::NV; ++jj) {
-                float f[Sh::EPV];
-                StateVec<TS>::unpack(sv[q][jj], f);
+                uint64_t f[NP];
+                StatePairs<TS>::unpack(sv[q][jj], f);
 #pragma unroll
-                for (int e = 0; e < Sh::EPV; ++e) f[e] = fmaf(a, f[e], d * kreg[jj * Sh::EPV + e]);
-                *reinterpret_cast<uint4 *>(S + (int64_t)rr[q] * DK + (jj * Sh::TPR + lr) * Sh::EPV) = StateVec<TS>::pack(f);
+                for (int e = 0; e < NP; ++e) f[e] = f2_fma(a2, f[e], f2_mul(d2, k2[jj * NP + e]));
+                *reinterpret_cast<uint4 *>(S + (int64_t)rr[q] * DK + (jj * Sh::TPR + lr) * Sh::EPV) =
+                    StatePairs<TS>::pack(f);
               }
               if (lr == 0) o[rr[q]] = fmaf(a, wq[q], d * kq);
             }
@@ -506,10 +515,10 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
         for (int r = tid; r < rows; r += kConsumers) o[r] = 0.f;
       }
       fence_proxy_async_smem();
-      named_sync<1, kConsumers>();
-      if (tid == 0) mbar_arrive(&empty[stage]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
     }
-    if (tid == 0) mbar_arrive(&yempty[k & 1]);  // the last tile's barrier: every tile warp is done with y
+    if (lane == 0) mbar_arrive(&yempty[k & 1]);  // after the last tile's __syncwarp: this warp is done with y
   }
 }
 

@@ -38,31 +38,57 @@ template <> struct Elem<__nv_bfloat16> {
   }
 };
 
-// 16-byte vectors of state elements <-> floats.
-template <typename TS> struct StateVec;
-template <> struct StateVec<float> {
-  __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
-    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
-    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+// Pairs of floats in one 64-bit register (low half = first element) for the
+// packed f32x2 arithmetic of sm_100 and later: one instruction does two
+// independent, individually rounded fp32 operations.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 16-byte vectors of state elements <-> float pairs (EPV / 2 of them).
+template <typename TS> struct StatePairs;
+template <> struct StatePairs<float> {
+  static constexpr int N = 2;
+  __device__ __forceinline__ static void unpack(const uint4 &v, uint64_t *f) {
+    f[0] = f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
+    f[1] = f2_pack(__uint_as_float(v.z), __uint_as_float(v.w));
   }
-  __device__ __forceinline__ static uint4 pack(const float *f) {
-    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  __device__ __forceinline__ static uint4 pack(const uint64_t *f) {
+    float a, b, c, d;
+    f2_unpack(f[0], a, b);
+    f2_unpack(f[1], c, d);
+    return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
   }
 };
-template <> struct StateVec<__nv_bfloat16> {
-  __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
+template <> struct StatePairs<__nv_bfloat16> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4 &v, uint64_t *f) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      f[2 * k] = __uint_as_float(w[k] << 16);
-      f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-    }
+    for (int k = 0; k < 4; ++k) f[k] = f2_pack(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
   }
-  __device__ __forceinline__ static uint4 pack(const float *f) {
+  __device__ __forceinline__ static uint4 pack(const uint64_t *f) {
     uint32_t w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);  // .x = low half
+      float lo, hi;
+      f2_unpack(f[k], lo, hi);
+      __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // .x = low half
       w[k] = *reinterpret_cast<uint32_t *>(&b);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
