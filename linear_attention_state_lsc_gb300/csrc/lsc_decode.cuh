@@ -169,15 +169,6 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
   int32_t *info_slot = reinterpret_cast<int32_t *>(smem + D.off_info);
   int32_t *info_warm = info_slot + kDecodeMaxItems;
 
-  // rows of this CTA's items: slot (or -1) and warm, loaded once
-  for (int k = tid; k < my_items; k += kDecodeBlock) {
-    const int i = (b + k * grid) / Hk;
-    const int32_t slot = p.idx[i];
-    const bool ok = slot >= 0 && slot < p.num_slots;
-    if (slot >= p.num_slots) report(p.status, LSC_ERR_OUT_OF_RANGE);
-    info_slot[k] = ok ? slot : -1;
-    info_warm[k] = ok && (p.has_init == nullptr || p.has_init[i] != 0);
-  }
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
@@ -188,6 +179,19 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
       mbar_init(&yempty[s], kTileWarps);
     }
     fence_mbar_init();
+  }
+  // the previous kernel of the stream may still be running until here
+  griddep_wait();
+  if (tid == 0) griddep_launch_dependents();
+
+  // rows of this CTA's items: slot (or -1) and warm, loaded once
+  for (int k = tid; k < my_items; k += kDecodeBlock) {
+    const int i = (b + k * grid) / Hk;
+    const int32_t slot = p.idx[i];
+    const bool ok = slot >= 0 && slot < p.num_slots;
+    if (slot >= p.num_slots) report(p.status, LSC_ERR_OUT_OF_RANGE);
+    info_slot[k] = ok ? slot : -1;
+    info_warm[k] = ok && (p.has_init == nullptr || p.has_init[i] != 0);
   }
   __syncthreads();
 
@@ -566,8 +570,23 @@ int launch_decode_t(const DecodeParams &p0, cudaStream_t stream) {
     q.out = p0.out + (int64_t)r0 * p0.Hv * p0.dv;
     const int64_t items = (int64_t)q.n * q.Hk;
     const int grid = (int)(items < grid_max ? items : grid_max);
-    decode_kernel<DK, TS, TC, CW><<<grid, kDecodeBlock, (size_t)D.total, stream>>>(q);
-    if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;
+    // programmatic stream serialisation: this grid's CTAs may be placed on SMs
+    // as the previous kernel's CTAs leave them (the kernel waits for that
+    // kernel's completion before its first global access)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecodeBlock);
+    cfg.dynamicSmemBytes = (size_t)D.total;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_kernel<DK, TS, TC, CW>, q) != cudaSuccess) {
+      cudaGetLastError();
+      return LSC_ERR_CUDA;
+    }
   }
   return LSC_OK;
 }

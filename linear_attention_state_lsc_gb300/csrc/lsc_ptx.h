@@ -122,4 +122,15 @@ __device__ __forceinline__ void cluster_barrier_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel of its stream is still
+// running; griddep_wait() blocks until that kernel has completed and its
+// memory operations are visible, so it must precede every global access.
+// griddep_launch_dependents() lets the next such kernel be scheduled early
+// (its CTAs then wait in their own griddep_wait()).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace lsc
