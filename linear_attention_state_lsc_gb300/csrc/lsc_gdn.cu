@@ -111,23 +111,26 @@ __global__ void __launch_bounds__(kRecThreads, 2) recurrent_kernel(const __grid_
   rv[0] = rp < rh && rows[0] < dv;
   rv[1] = rp < rh && rows[1] < dv;
 
-  // state rows into registers
-  float S[2][R::CPT];
+  // state rows into registers, as float pairs for the f32x2 arithmetic
+  constexpr int NP = R::CPT / 2;
+  uint64_t S[2][NP];
   TS *Sg = reinterpret_cast<TS *>(p.layer + (int64_t)slot * p.page + p.ssm_off) + (int64_t)h * dv * DK;
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
 #pragma unroll
     for (int jv = 0; jv < R::NV4; ++jv) {
       const int c0 = (jv * R::TPR + lr) * 4;
+      float v[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float v = 0.f;
+        v[e] = 0.f;
         if (warm && rv[q]) {
-          if constexpr (sizeof(TS) == 4) v = ((const float *)Sg)[(int64_t)rows[q] * DK + c0 + e];
-          else v = bf16_bits_to_float(((const uint16_t *)Sg)[(int64_t)rows[q] * DK + c0 + e]);
+          if constexpr (sizeof(TS) == 4) v[e] = ((const float *)Sg)[(int64_t)rows[q] * DK + c0 + e];
+          else v[e] = bf16_bits_to_float(((const uint16_t *)Sg)[(int64_t)rows[q] * DK + c0 + e]);
         }
-        S[q][jv * 4 + e] = v;
       }
+      S[q][jv * 2] = f2_pack(v[0], v[1]);
+      S[q][jv * 2 + 1] = f2_pack(v[2], v[3]);
     }
   }
   float gam = 1.f;
@@ -181,24 +184,33 @@ __global__ void __launch_bounds__(kRecThreads, 2) recurrent_kernel(const __grid_
     const float *al = a_s(bsel), *be = b_s(bsel), *kq = kq_s(bsel);
     for (int tt = 0; tt < nt; ++tt) {
       const float *kt = kd + tt * DK, *qt = qd + tt * DK;
-      float kr[R::CPT];
-      float ua[2] = {0.f, 0.f}, ub[2] = {0.f, 0.f}, wa[2] = {0.f, 0.f}, wb[2] = {0.f, 0.f};
+      uint64_t kr[NP];
+      uint64_t u2[2] = {0, 0}, w2[2] = {0, 0};  // (even, odd) column partial sums
 #pragma unroll
       for (int jv = 0; jv < R::NV4; ++jv) {
         const int c0 = (jv * R::TPR + lr) * 4;
-        const float4 k4 = *reinterpret_cast<const float4 *>(kt + c0);
-        const float4 q4 = *reinterpret_cast<const float4 *>(qt + c0);
-        kr[jv * 4] = k4.x; kr[jv * 4 + 1] = k4.y; kr[jv * 4 + 2] = k4.z; kr[jv * 4 + 3] = k4.w;
+        const ulonglong2 k4 = *reinterpret_cast<const ulonglong2 *>(kt + c0);
+        const ulonglong2 q4 = *reinterpret_cast<const ulonglong2 *>(qt + c0);
+        kr[jv * 2] = k4.x;
+        kr[jv * 2 + 1] = k4.y;
+        const uint64_t qa = q4.x, qb = q4.y;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const float *s = S[q] + jv * 4;
-          ua[q] = fmaf(s[0], k4.x, ua[q]); ub[q] = fmaf(s[1], k4.y, ub[q]);
-          ua[q] = fmaf(s[2], k4.z, ua[q]); ub[q] = fmaf(s[3], k4.w, ub[q]);
-          wa[q] = fmaf(s[0], q4.x, wa[q]); wb[q] = fmaf(s[1], q4.y, wb[q]);
-          wa[q] = fmaf(s[2], q4.z, wa[q]); wb[q] = fmaf(s[3], q4.w, wb[q]);
+          u2[q] = f2_fma(S[q][jv * 2], kr[jv * 2], u2[q]);
+          u2[q] = f2_fma(S[q][jv * 2 + 1], kr[jv * 2 + 1], u2[q]);
+          w2[q] = f2_fma(S[q][jv * 2], qa, w2[q]);
+          w2[q] = f2_fma(S[q][jv * 2 + 1], qb, w2[q]);
         }
       }
-      float u[2] = {ua[0] + ub[0], ua[1] + ub[1]}, w[2] = {wa[0] + wb[0], wa[1] + wb[1]};
+      float u[2], w[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float lo, hi;
+        f2_unpack(u2[q], lo, hi);
+        u[q] = lo + hi;
+        f2_unpack(w2[q], lo, hi);
+        w[q] = lo + hi;
+      }
 #pragma unroll
       for (int m = R::TPR / 2; m >= 1; m >>= 1) {
 #pragma unroll
@@ -217,18 +229,20 @@ __global__ void __launch_bounds__(kRecThreads, 2) recurrent_kernel(const __grid_
         o[q] = fmaf(gn, w[q], d[q] * kq[tt]);
       }
       if (gn < 0x1p-32f) {  // fold the scale into Shat (uniform over the CTA)
+        const uint64_t g2 = f2_pack(gn, gn);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int c = 0; c < R::CPT; ++c) S[q][c] *= gn;
+          for (int c = 0; c < NP; ++c) S[q][c] = f2_mul(S[q][c], g2);
         gn = 1.f;
       }
       const float inv = 1.f / gn;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const float e = d[q] * inv;
+        const uint64_t e2 = f2_pack(e, e);
 #pragma unroll
-        for (int c = 0; c < R::CPT; ++c) S[q][c] = fmaf(e, kr[c], S[q][c]);
+        for (int c = 0; c < NP; ++c) S[q][c] = f2_fma(e2, kr[c], S[q][c]);
       }
       gam = gn;
       if (lr == 0) {
@@ -248,9 +262,12 @@ __global__ void __launch_bounds__(kRecThreads, 2) recurrent_kernel(const __grid_
 #pragma unroll
     for (int jv = 0; jv < R::NV4; ++jv) {
       const int c0 = (jv * R::TPR + lr) * 4;
+      float f[4];
+      f2_unpack(S[q][jv * 2], f[0], f[1]);
+      f2_unpack(S[q][jv * 2 + 1], f[2], f[3]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float v = gam * S[q][jv * 4 + e];
+        const float v = gam * f[e];
         if constexpr (sizeof(TS) == 4) ((float *)Sg)[(int64_t)rows[q] * DK + c0 + e] = v;
         else ((uint16_t *)Sg)[(int64_t)rows[q] * DK + c0 + e] = float_to_bf16_bits(v);
       }
