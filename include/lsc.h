@@ -50,6 +50,8 @@ extern "C" {
 #define LSC_ERR_NO_MEMORY (-10)     /* allocation failed, or the borrowed buffer is too small */
 #define LSC_ERR_LAYOUT (-11)        /* page stride smaller than the payload, or not a multiple of an element size */
 #define LSC_ERR_WRONG_DEVICE (-12)  /* the current device is not the pool's device */
+#define LSC_ERR_NO_SLOT (-13)       /* prefix cache: no free slot and no unpinned checkpoint to reclaim */
+#define LSC_ERR_ORDER (-14)         /* prefix cache: call out of step order (resolve/commit/release) */
 
 /* ---- enums -------------------------------------------------------------- */
 typedef enum { LSC_LAYER_ATTENTION = 0, LSC_LAYER_GDN = 1 } lsc_layer_kind;

@@ -15,9 +15,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblsc.so")
-SOURCES = ["lsc_host.cu", "lsc_copy.cu", "lsc_gdn.cu", "lsc_decode_f32.cu", "lsc_decode_bf16.cu"]
+SOURCES = ["lsc_host.cu", "lsc_copy.cu", "lsc_gdn.cu", "lsc_decode_f32.cu", "lsc_decode_bf16.cu",
+           "lsc_prefix_cache.cpp"]
 HEADERS = [os.path.join(CSRC, h) for h in ("lsc_internal.h", "lsc_ptx.h", "lsc_gdn_common.cuh", "lsc_decode.cuh")] + \
-    [os.path.join(INCLUDE, "lsc.h")]
+    [os.path.join(INCLUDE, h) for h in ("lsc.h", "lsc_prefix_cache.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,7 +45,7 @@ def build(force: bool = False, ptxas_info: bool = False) -> str:
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         if force or ptxas_info or _stale(o, [s] + HEADERS):
             jobs.append([cc] + flags + ["-c", s, "-o", o])
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
@@ -54,7 +55,7 @@ def build(force: bool = False, ptxas_info: bool = False) -> str:
             sys.stderr.write(r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(BUILD, os.path.splitext(s)[0] + ".o") for s in SOURCES]
     if force or jobs or _stale(LIB, objs):
         subprocess.run([cc] + ARCH + ["-shared", "-o", LIB + ".tmp"] + objs, check=True)
         os.replace(LIB + ".tmp", LIB)

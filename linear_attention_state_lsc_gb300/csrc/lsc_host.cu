@@ -174,6 +174,8 @@ const char *lsc_error_string(int code) {
     case LSC_ERR_NO_MEMORY: return "out of memory or buffer too small";
     case LSC_ERR_LAYOUT: return "page stride smaller than the payload or not a multiple of an element size";
     case LSC_ERR_WRONG_DEVICE: return "current device is not the pool's device";
+    case LSC_ERR_NO_SLOT: return "no free slot and no unpinned checkpoint to reclaim";
+    case LSC_ERR_ORDER: return "prefix cache call out of step order";
     default: return "unknown error";
   }
 }

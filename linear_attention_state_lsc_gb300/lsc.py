@@ -1,4 +1,5 @@
-"""ctypes binding of liblsc (include/lsc.h), same names as the C ABI.
+"""ctypes binding of liblsc (include/lsc.h, include/lsc_prefix_cache.h), same
+names as the C ABI.
 
 Argument marshalling only: every step of the hot path runs in the CUDA kernels
 of liblsc.so.  Pointers are plain integers; torch tensors, numpy arrays and
@@ -28,6 +29,11 @@ LSC_ERR_DEV_TIMEOUT = -9
 LSC_ERR_NO_MEMORY = -10
 LSC_ERR_LAYOUT = -11
 LSC_ERR_WRONG_DEVICE = -12
+LSC_ERR_NO_SLOT = -13
+LSC_ERR_ORDER = -14
+
+# prefix-cache slot states (include/lsc_prefix_cache.h)
+LSC_SLOT_FREE, LSC_SLOT_LIVE, LSC_SLOT_CHECKPOINT, LSC_SLOT_RESERVED = 0, 1, 2, 3
 
 LSC_LAYER_ATTENTION, LSC_LAYER_GDN = 0, 1
 LSC_F32, LSC_BF16, LSC_F16 = 0, 1, 2
@@ -88,6 +94,16 @@ class lsc_gdn_recurrent_args(C.Structure):
                 ("alpha", C.c_void_p), ("beta", C.c_void_p), ("out", C.c_void_p)]
 
 
+class lsc_pc_row(C.Structure):
+    _fields_ = [("seq_id", C.c_int64), ("restore_prefix_hash", C.c_uint64),
+                ("save_prefix_hash", C.c_uint64), ("tokens_after_step", C.c_int64)]
+
+
+class lsc_pc_report(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("restore_hit", "restore_miss", "save", "skip_duplicate",
+                                          "skip_cached", "skip_unaligned", "skip_no_slot", "reserved")]
+
+
 _lib = None
 
 
@@ -113,6 +129,17 @@ def load():
         "lsc_scatter": ([P, I32, P, I32, P, P, P], C.c_int),
         "lsc_gdn_decode": ([P, I32, C.POINTER(lsc_gdn_decode_args), P], C.c_int),
         "lsc_gdn_recurrent": ([P, I32, C.POINTER(lsc_gdn_recurrent_args), P], C.c_int),
+        "lsc_pc_create": ([I32, I32, C.POINTER(P)], C.c_int),
+        "lsc_pc_destroy": ([P], C.c_int),
+        "lsc_pc_allocate_live_slot": ([P, I64, C.POINTER(I32)], C.c_int),
+        "lsc_pc_release_sequence": ([P, I64], C.c_int),
+        "lsc_pc_match": ([P, C.c_uint64, C.POINTER(I32)], C.c_int),
+        "lsc_pc_unpin": ([P, I32], C.c_int),
+        "lsc_pc_resolve": ([P, P, I32, P, P, C.POINTER(lsc_pc_report)], C.c_int),
+        "lsc_pc_commit": ([P], C.c_int),
+        "lsc_pc_slot": ([P, I32, C.POINTER(I32), C.POINTER(I32), C.POINTER(C.c_uint64)], C.c_int),
+        "lsc_pc_sequence": ([P, I64, C.POINTER(I32), C.POINTER(I32)], C.c_int),
+        "lsc_pc_counts": ([P, C.POINTER(I32), C.POINTER(I32), C.POINTER(I32), C.POINTER(I32)], C.c_int),
         "lsc_error_string": ([C.c_int], C.c_char_p),
         "lsc_build_info": ([], C.c_char_p),
     }
@@ -274,3 +301,89 @@ def recurrent_args(n_seq, num_k_heads, total_tokens, idx, has_init, cu_seqlens, 
 
 def lsc_gdn_recurrent(pool, layer, args, stream=None):
     return load().lsc_gdn_recurrent(pool, layer, C.byref(args), _stream(stream))
+
+
+# ---- scheduler-side prefix cache (include/lsc_prefix_cache.h) ---------------
+
+PC_ROW_DTYPE = np.dtype([("seq_id", "<i8"), ("restore_prefix_hash", "<u8"),
+                         ("save_prefix_hash", "<u8"), ("tokens_after_step", "<i8")])
+
+
+def lsc_pc_create(num_slots, block_size):
+    """Returns (rc, cache handle)."""
+    h = C.c_void_p()
+    rc = load().lsc_pc_create(num_slots, block_size, C.byref(h))
+    return rc, h.value
+
+
+def lsc_pc_destroy(pc):
+    return load().lsc_pc_destroy(pc)
+
+
+def lsc_pc_allocate_live_slot(pc, seq_id):
+    """Returns (rc, slot)."""
+    s = C.c_int32(-1)
+    rc = load().lsc_pc_allocate_live_slot(pc, seq_id, C.byref(s))
+    return rc, s.value
+
+
+def lsc_pc_release_sequence(pc, seq_id):
+    return load().lsc_pc_release_sequence(pc, seq_id)
+
+
+def lsc_pc_match(pc, prefix_hash):
+    """Returns (rc, slot or -1)."""
+    s = C.c_int32(-1)
+    rc = load().lsc_pc_match(pc, prefix_hash, C.byref(s))
+    return rc, s.value
+
+
+def lsc_pc_unpin(pc, slot):
+    return load().lsc_pc_unpin(pc, slot)
+
+
+def pc_rows(seq_ids, restore_hashes, save_hashes, tokens_after_step):
+    rows = np.zeros(len(seq_ids), PC_ROW_DTYPE)
+    rows["seq_id"] = seq_ids
+    rows["restore_prefix_hash"] = restore_hashes
+    rows["save_prefix_hash"] = save_hashes
+    rows["tokens_after_step"] = tokens_after_step
+    return rows
+
+
+def lsc_pc_resolve(pc, rows):
+    """rows: a PC_ROW_DTYPE array.  Returns (rc, ops OP_DTYPE [n],
+    linear_state_initialized uint8 [n], lsc_pc_report)."""
+    assert rows.dtype == PC_ROW_DTYPE
+    rows = np.ascontiguousarray(rows)
+    ops = np.zeros(len(rows), OP_DTYPE)
+    init = np.zeros(len(rows), np.uint8)
+    rep = lsc_pc_report()
+    rc = load().lsc_pc_resolve(pc, rows.ctypes.data, len(rows), ops.ctypes.data, init.ctypes.data,
+                               C.byref(rep))
+    return rc, ops, init, rep
+
+
+def lsc_pc_commit(pc):
+    return load().lsc_pc_commit(pc)
+
+
+def lsc_pc_slot(pc, slot):
+    """Returns (rc, state, pins, hash)."""
+    st, pins, h = C.c_int32(), C.c_int32(), C.c_uint64()
+    rc = load().lsc_pc_slot(pc, slot, C.byref(st), C.byref(pins), C.byref(h))
+    return rc, st.value, pins.value, h.value
+
+
+def lsc_pc_sequence(pc, seq_id):
+    """Returns (rc, live slot, linear_state_initialized)."""
+    s, i = C.c_int32(-1), C.c_int32(0)
+    rc = load().lsc_pc_sequence(pc, seq_id, C.byref(s), C.byref(i))
+    return rc, s.value, i.value
+
+
+def lsc_pc_counts(pc):
+    """Returns (rc, (free, live, checkpoint, reserved))."""
+    c = [C.c_int32() for _ in range(4)]
+    rc = load().lsc_pc_counts(pc, *[C.byref(x) for x in c])
+    return rc, tuple(x.value for x in c)

@@ -36,14 +36,20 @@ Readings where the page is silent (also listed in the design notes):
   * Pins taken by resolve's matches are released by the step's commit: the
     restore copy that reads the checkpoint runs during the forward.
   * Each sequence appears at most once per batch; resolve may not run again
-    before commit.
+    before commit, and a sequence of the resolved step may not be released
+    before the commit (its forward is writing the live slot).
 """
 
 FREE, LIVE, CHECKPOINT, RESERVED = 0, 1, 2, 3
 
 
 class PrefixCacheError(Exception):
-    pass
+    """kind: "arg" (bad argument), "no_slot" (nothing free or reclaimable) or
+    "order" (a call out of step order)."""
+
+    def __init__(self, what, kind="arg"):
+        super().__init__(what)
+        self.kind = kind
 
 
 class PrefixCache:
@@ -95,7 +101,7 @@ class PrefixCache:
         if s is None:
             s = self._lru_unpinned_checkpoint()
             if s is None:
-                raise PrefixCacheError("no slot")
+                raise PrefixCacheError("no slot", "no_slot")
             self._drop_checkpoint(s)
         self.state[s] = LIVE
         self.seq_slot[seq] = s
@@ -105,8 +111,8 @@ class PrefixCache:
     def release_sequence(self, seq):
         if seq not in self.seq_slot:
             raise PrefixCacheError("unknown sequence")
-        if self.pending is not None and any(pr[1] == seq for pr in self.pending["promotions"]):
-            raise PrefixCacheError("promotion pending")
+        if self.pending is not None and seq in self.pending["seqs"]:
+            raise PrefixCacheError("the sequence is in the resolved step", "order")
         s = self.seq_slot.pop(seq)
         del self.seq_initialized[seq]
         self.state[s] = FREE
@@ -140,7 +146,7 @@ class PrefixCache:
         Returns (ops, initialized, report); ops are dicts with the six
         LinearStateCacheOp fields."""
         if self.pending is not None:
-            raise PrefixCacheError("previous step not committed")
+            raise PrefixCacheError("previous step not committed", "order")
         seen = set()
         for seq, _, _, _ in rows:
             if seq not in self.seq_slot or seq in seen:
@@ -186,7 +192,7 @@ class PrefixCache:
 
     def commit(self):
         if self.pending is None:
-            raise PrefixCacheError("nothing to commit")
+            raise PrefixCacheError("nothing to commit", "order")
         # the forward wrote every row's live slot
         for seq in self.pending["seqs"]:
             self.seq_initialized[seq] = True

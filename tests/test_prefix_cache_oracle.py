@@ -173,6 +173,14 @@ def test_errors_leave_state_unchanged():
     with pytest.raises(PrefixCacheError):
         pc.allocate_live_slot(1)                      # already holds a slot
     assert pc.counts() == (3, 1, 0, 0) and pc.pending is None
+    pc.resolve([(1, 0, 0, 16)])
+    with pytest.raises(PrefixCacheError):
+        pc.release_sequence(1)                        # its forward is writing the slot
+    with pytest.raises(PrefixCacheError):
+        pc.resolve([(1, 0, 0, 16)])                   # previous step not committed
+    pc.commit()
+    pc.release_sequence(1)
+    assert pc.counts() == (4, 0, 0, 0)
 
 
 def check_invariants(pc):
