@@ -488,7 +488,89 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     L.lsc_pool_destroy(pool)
     del buf, out, dev
     torch.cuda.empty_cache()
+    parts["prefix_cache_host"] = measure_prefix_cache(L)
     return parts
+
+
+def prefix_cache_schedule(steps, num_slots=1024, block=64, batch=256, churn=4, seed=0):
+    """A deterministic scheduler workload: `batch` running sequences advance 16
+    tokens per step; a sequence saves its prefix at every block boundary and a
+    new one asks to restore its family's 4-block prefix; `churn` sequences
+    finish and are replaced every step.  Returns per-step (rows, released,
+    joined) -- rows as lsc_pc_row tuples."""
+    rng = np.random.default_rng(seed)
+    fam = {}
+    tokens = {}
+    nxt = 0
+    for _ in range(batch):
+        fam[nxt], tokens[nxt] = int(rng.integers(1, 65)), 0
+        nxt += 1
+    sched = []
+    for _ in range(steps):
+        rows = []
+        for s in sorted(tokens):
+            new = tokens[s] == 0
+            after = 4 * block if new else tokens[s] + 16
+            rh = (fam[s] << 32) | 4 if new else 0
+            sh = (fam[s] << 32) | (after // block) if after % block == 0 else 0
+            rows.append((s, rh, sh, after))
+            tokens[s] = after
+        gone = [int(x) for x in rng.choice(sorted(tokens), churn, replace=False)]
+        joined = []
+        for g in gone:
+            del tokens[g], fam[g]
+            fam[nxt], tokens[nxt] = int(rng.integers(1, 65)), 0
+            joined.append(nxt)
+            nxt += 1
+        sched.append((rows, gone, joined))
+    return sched, num_slots, block, batch
+
+
+def measure_prefix_cache(L, steps=3000, oracle_steps=60):
+    """Host-side cost of the scheduler's prefix cache per step (resolve + commit
+    + sequence churn), through the C ABI; the plain oracle on a prefix of the
+    same schedule beside it."""
+    sched, num_slots, block, batch = prefix_cache_schedule(steps)
+    arrays = [L.pc_rows(*zip(*rows)) for rows, _, _ in sched]
+    rc, pc = L.lsc_pc_create(num_slots, block)
+    assert rc == L.LSC_OK
+    for s in range(batch):
+        assert L.lsc_pc_allocate_live_slot(pc, s)[0] == L.LSC_OK
+    saves = hits = 0
+    t = time.perf_counter()
+    for arr, (_, gone, joined) in zip(arrays, sched):
+        rc, ops, init, rep = L.lsc_pc_resolve(pc, arr)
+        assert rc == L.LSC_OK
+        saves += rep.save
+        hits += rep.restore_hit
+        assert L.lsc_pc_commit(pc) == L.LSC_OK
+        for g in gone:
+            assert L.lsc_pc_release_sequence(pc, g) == L.LSC_OK
+        for j in joined:
+            assert L.lsc_pc_allocate_live_slot(pc, j)[0] == L.LSC_OK
+    el = time.perf_counter() - t
+    counts = L.lsc_pc_counts(pc)[1]
+    L.lsc_pc_destroy(pc)
+    from oracle.prefix_cache import PrefixCache  # the plain model, timed as it stands
+    orc = PrefixCache(num_slots, block)
+    for s in range(batch):
+        orc.allocate_live_slot(s)
+    t = time.perf_counter()
+    for rows, gone, joined in sched[:oracle_steps]:
+        orc.resolve(rows)
+        orc.commit()
+        for g in gone:
+            orc.release_sequence(g)
+        for j in joined:
+            orc.allocate_live_slot(j)
+    el_o = time.perf_counter() - t
+    return {"workload": f"{num_slots} slots, {batch}-row batches, 4 sequences replaced per step, "
+                        f"saves at {block}-token boundaries, restores of 4-block family prefixes",
+            "us_per_step": round(el / steps * 1e6, 2), "rows_per_s": round(batch * steps / el, 1),
+            "steps": steps, "promotions": saves, "restore_hits": hits,
+            "final_free_live_checkpoint_reserved": list(counts),
+            "oracle_us_per_step": round(el_o / oracle_steps * 1e6, 1), "oracle_steps": oracle_steps,
+            "clock": "host wall clock, one thread, includes the ctypes calls"}
 
 
 # ---------------------------------------------------------------- CPU oracle
