@@ -286,6 +286,19 @@ def seq_lengths(n_seq: int, lo: int, hi: int, seed: int = 0):
     return rng.integers(lo, hi + 1, size=n_seq).astype(np.int32)
 
 
+def prefill_inputs(w: Workload, lengths, seed: int = 0, layer: int = 0):
+    """Inputs of the prefill conv: cu_seqlens int32, x ~ N(0,1) [T, conv_dim] and
+    conv weights ~ N(0, 0.1) [conv_dim, conv_width], float32 (the caller encodes
+    them at the conv dtype)."""
+    rng = np.random.default_rng(seed * 1000 + layer + 43)
+    lengths = np.asarray(lengths, np.int64)
+    cu = np.zeros(len(lengths) + 1, np.int32)
+    cu[1:] = np.cumsum(lengths)
+    x = _normal_f32(rng, (int(lengths.sum()), w.conv_dim))
+    cw = (0.1 * _normal_f32(rng, (w.conv_dim, w.conv_width))).astype(np.float32)
+    return cu, x, cw
+
+
 def recurrent_inputs(w: Workload, lengths, seed: int = 0, layer: int = 0):
     """q, k ~ N(0,1) scaled to unit L2 norm per head; v ~ N(0,1);
     alpha = sigmoid(N(2,1)), beta = sigmoid(N(0,1)); cu_seqlens int32."""

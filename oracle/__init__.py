@@ -55,6 +55,8 @@ def lib():
         _lib.orc_gdn_decode.argtypes = [C.POINTER(_Pool), P, C.c_int, P, P, P, P, C.c_int, P, P, P]
         _lib.orc_gdn_recurrent.argtypes = [C.POINTER(_Pool), P, C.c_int, P, P, P, C.c_int,
                                            P, P, P, P, P, P]
+        _lib.orc_gdn_prefill_conv.argtypes = [C.POINTER(_Pool), P, C.c_int, P, P, P, C.c_int,
+                                               P, P, P, P, P]
         _lib.orc_bf16_bits.argtypes = [C.c_float]
         _lib.orc_bf16_bits.restype = C.c_ushort
         _lib.orc_num_threads.restype = C.c_int
@@ -173,6 +175,24 @@ def gdn_recurrent(pool, region, idx, has_init, cu_seqlens, num_k_heads, q, k, v,
                                  _ptr(cu), num_k_heads, _ptr(q), _ptr(k), _ptr(v), _ptr(a),
                                  _ptr(b), _ptr(out))
     return rc, out
+
+
+def gdn_prefill_conv(pool, region, idx, has_init, cu_seqlens, num_k_heads, x_raw, conv_w_raw):
+    """x_raw [T, conv_dim] / conv_w_raw [conv_dim, W]: arrays holding the conv
+    dtype's bytes.  Returns (rc, q, k [T, Hk, dk], v [T, Hv, dv] float32); the
+    slots' conv states are updated in place."""
+    idx = _c(idx, np.int32)
+    hs = _c(has_init, np.uint8)
+    cu = _c(cu_seqlens, np.int32)
+    x = np.ascontiguousarray(x_raw)
+    w = np.ascontiguousarray(conv_w_raw)
+    T = int(cu[-1]) if len(cu) else 0
+    q = np.full((T, num_k_heads, pool.head_k_dim), np.nan, np.float32)
+    k = np.full((T, num_k_heads, pool.head_k_dim), np.nan, np.float32)
+    v = np.full((T, pool.num_v_heads, pool.head_v_dim), np.nan, np.float32)
+    rc = lib().orc_gdn_prefill_conv(C.byref(pool.s), _ptr(region), len(idx), _ptr(idx), _ptr(hs),
+                                    _ptr(cu), num_k_heads, _ptr(x), _ptr(w), _ptr(q), _ptr(k), _ptr(v))
+    return rc, q, k, v
 
 
 def bf16_bits(f):

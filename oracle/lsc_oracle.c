@@ -549,6 +549,99 @@ int orc_gdn_recurrent(const orc_pool *p, unsigned char *region, int n_seq, const
   return ORC_OK;
 }
 
+/*
+ * Prefill conv of a resumed prefill, for one GDN layer: causal_conv1d over each
+ * sequence's tokens from the slot's conv state, then the split into q | k | v
+ * and the L2 norm of q and k per head.
+ *
+ * [VA] §6 names causal_conv1d_fn (the multi-token conv) beside
+ * causal_conv1d_update.  [KP] "相同前缀不一定能全部复用": the prefill continues
+ * from the restored checkpoint, so the conv starts from the slot's conv state.
+ * READING 10 (as in orc_gdn_decode): the conv state of channel c holds the last
+ * W-1 inputs, oldest first; token t of a sequence sees the window of its last W
+ * inputs [.., x_(t-1), x_t], the inputs before the sequence's first token being
+ * the conv state (zero when has_init[i] == 0); y = SiLU(sum_j w[c][j] window[j]),
+ * no bias.  After the sequence, the slot's conv state holds the last W-1 entries
+ * of [state, x_(t0) .. x_(t1-1)].  READING 6/7: channels [q | k | v] head-major;
+ * q and k L2-normalised per head.  idx[i] < 0: zero outputs, no state touched.
+ * The ssm state is not touched.
+ *
+ * x [T, conv_dim] and conv_w [conv_dim, conv_width] at the conv dtype; q, k
+ * [T, Hk, dk], v [T, Hv, dv] binary32.
+ */
+int orc_gdn_prefill_conv(const orc_pool *p, unsigned char *region, int n_seq, const int *idx,
+                         const unsigned char *has_init, const int *cu_seqlens, int num_k_heads,
+                         const unsigned char *x, const unsigned char *conv_w, float *q, float *k,
+                         float *v) {
+  orc_layout_t L;
+  int rc = orc_layout(p, &L);
+  if (rc != ORC_OK) return rc;
+  const int C = p->conv_dim, W = p->conv_width, Hv = p->num_v_heads;
+  const int dv = p->head_v_dim, dk = p->head_k_dim, Hk = num_k_heads;
+  if (p->conv_dtype == ORC_F16) return ORC_REJECT_ARG;
+  if (Hk <= 0 || Hv % Hk != 0 || C != 2 * Hk * dk + Hv * dv) return ORC_REJECT_ARG;
+  if (n_seq < 0 || (n_seq > 0 && (!region || !idx || !cu_seqlens))) return ORC_REJECT_ARG;
+  if (n_seq > 0 && cu_seqlens[0] != 0) return ORC_REJECT_ARG;
+  for (int i = 0; i < n_seq; ++i) {
+    if (cu_seqlens[i + 1] < cu_seqlens[i]) return ORC_REJECT_ARG;
+    if (idx[i] >= p->num_slots) return ORC_REJECT_RANGE;
+    for (int j = 0; j < i; ++j)
+      if (idx[i] >= 0 && idx[j] == idx[i]) return ORC_REJECT_DUP_DST;
+  }
+  if (n_seq > 0 && cu_seqlens[n_seq] > 0 && (!x || !conv_w || !q || !k || !v)) return ORC_REJECT_ARG;
+  const int es = elem_size(p->conv_dtype);
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < n_seq; ++i) {
+    const int t0 = cu_seqlens[i], t1 = cu_seqlens[i + 1];
+    if (idx[i] < 0) {
+      for (int t = t0; t < t1; ++t) {
+        for (int e = 0; e < Hk * dk; ++e) {
+          q[(long long)t * Hk * dk + e] = 0.0f;
+          k[(long long)t * Hk * dk + e] = 0.0f;
+        }
+        for (int e = 0; e < Hv * dv; ++e) v[(long long)t * Hv * dv + e] = 0.0f;
+      }
+      continue;
+    }
+    int warm = !has_init || has_init[i] != 0;
+    unsigned char *conv_state = region + (long long)idx[i] * L.page;
+    /* hist[c][j]: the last W-1 inputs of channel c, oldest first */
+    double *hist = (double *)malloc(sizeof(double) * C * (W - 1));
+    double *y = (double *)malloc(sizeof(double) * C);
+    for (int c = 0; c < C; ++c)
+      for (int j = 0; j < W - 1; ++j)
+        hist[c * (W - 1) + j] = warm ? load_elem(conv_state, p->conv_dtype, (long long)c * (W - 1) + j) : 0.0;
+    for (int t = t0; t < t1; ++t) {
+      const unsigned char *x_row = x + (long long)t * C * es;
+      for (int c = 0; c < C; ++c) {
+        const double xt = load_elem(x_row, p->conv_dtype, c);
+        double z = 0.0;
+        for (int j = 0; j < W - 1; ++j) z += load_elem(conv_w, p->conv_dtype, (long long)c * W + j) * hist[c * (W - 1) + j];
+        z += load_elem(conv_w, p->conv_dtype, (long long)c * W + W - 1) * xt;
+        y[c] = silu(z);
+        for (int j = 0; j + 1 < W - 1; ++j) hist[c * (W - 1) + j] = hist[c * (W - 1) + j + 1];
+        hist[c * (W - 1) + W - 2] = xt;
+      }
+      for (int g = 0; g < Hk; ++g) {
+        l2_normalise(y + g * dk, dk);
+        l2_normalise(y + Hk * dk + g * dk, dk);
+      }
+      for (int e = 0; e < Hk * dk; ++e) {
+        q[(long long)t * Hk * dk + e] = (float)y[e];
+        k[(long long)t * Hk * dk + e] = (float)y[Hk * dk + e];
+      }
+      for (int e = 0; e < Hv * dv; ++e) v[(long long)t * Hv * dv + e] = (float)y[2 * Hk * dk + e];
+    }
+    for (int c = 0; c < C; ++c)
+      for (int j = 0; j < W - 1; ++j)
+        store_elem(conv_state, p->conv_dtype, (long long)c * (W - 1) + j, hist[c * (W - 1) + j]);
+    free(y);
+    free(hist);
+  }
+  return ORC_OK;
+}
+
 /* Number of host threads OpenMP will use (reported beside CPU timings). */
 int orc_num_threads(void) {
 #ifdef _OPENMP
