@@ -42,7 +42,9 @@ extern "C" {
 #define LSC_ERR_OUT_OF_RANGE (-2)   /* slot id outside [0, num_slots), or layer id outside the pool */
 #define LSC_ERR_DUP_DST (-3)        /* two restoring rows write one live slot */
 #define LSC_ERR_SRC_IS_DST (-4)     /* a source slot is a destination of the same call */
-#define LSC_ERR_MISALIGNED (-5)     /* page stride not a multiple of 16 B, or base not 256 B aligned */
+#define LSC_ERR_MISALIGNED (-5)     /* page stride not a multiple of 16 B, base not 256 B aligned, or a
+                                       device array not aligned to its element size (q, k of the
+                                       recurrence: 16 B) */
 #define LSC_ERR_STATELESS_LAYER (-6)/* the layer is an attention layer: it has no state */
 #define LSC_ERR_UNSUPPORTED (-7)    /* shape/dtype combination without a kernel */
 #define LSC_ERR_CUDA (-8)           /* a CUDA runtime call failed */
@@ -261,7 +263,8 @@ typedef struct {
  * the call's rows are unspecified; nothing outside their views is written.  Entries of idx that are >= 0
  * must be distinct.  Supported: head_k_dim in {16, 32, 64, 128}, head_v_dim <=
  * 128, Hv/Hk <= 8, conv_width <= 8, ssm dtype f32 or bf16, conv dtype f32 or
- * bf16; else UNSUPPORTED.
+ * bf16; else UNSUPPORTED.  Every device array must be aligned to its element
+ * size (MISALIGNED).
  */
 int lsc_gdn_decode(lsc_pool *pool, int32_t layer, const lsc_gdn_decode_args *args, void *stream);
 
@@ -295,6 +298,44 @@ typedef struct {
  */
 int lsc_gdn_recurrent(lsc_pool *pool, int32_t layer, const lsc_gdn_recurrent_args *args,
                       void *stream);
+
+/* Arguments of lsc_gdn_prefill_conv.  T = total_tokens; sequence i owns tokens
+ * cu_seqlens[i] .. cu_seqlens[i+1]-1 of x, q, k and v. */
+typedef struct {
+  int32_t n_seq;
+  int32_t num_k_heads;       /* Hk; num_v_heads % Hk == 0, conv_dim == 2 Hk dk + Hv dv */
+  int32_t total_tokens;
+  int32_t reserved;          /* must be 0 */
+  const int32_t *idx;        /* device [n_seq]: slot per sequence, -1 = padding */
+  const uint8_t *has_init;   /* device [n_seq]: 1 warm, 0 cold; NULL = all warm */
+  const int32_t *cu_seqlens; /* device [n_seq + 1] */
+  const void *x;             /* device [T, conv_dim] at the conv dtype */
+  const void *conv_weight;   /* device [conv_dim, conv_width] at the conv dtype */
+  float *q;                  /* device [T, Hk, dk]: L2-normalised per head */
+  float *k;                  /* device [T, Hk, dk]: L2-normalised per head */
+  float *v;                  /* device [T, Hv, dv] */
+} lsc_gdn_prefill_conv_args;
+
+/*
+ * Prefill conv of a resumed prefill for GDN layer `layer` ([VA] §6 names
+ * causal_conv1d_fn; [KP] "相同前缀不一定能全部复用": the prefill continues from
+ * the restored checkpoint): for each sequence, a depthwise causal conv over its
+ * tokens whose first W-1 window inputs come from slot idx[i]'s conv state (zero
+ * when has_init[i] == 0); y = SiLU(sum_j w[c][j] window[j]), no bias; y splits
+ * into q | k | v (head-major) and q, k are L2-normalised per head (eps 1e-6
+ * inside the square root).  The slot's conv state then holds the last W-1
+ * entries of [old state, the sequence's x], so a later decode or prefill
+ * continues from it; the ssm state is untouched.  idx[i] < 0: zero outputs, no
+ * state touched.  Sequences must name distinct slots.  Inconsistent cu_seqlens
+ * (outside [0, total_tokens] or decreasing) are skipped and LSC_ERR_INVALID_ARG
+ * is recorded in the status word.  Two kernels on `stream`: the conv (outputs)
+ * and the conv-state update.  Conv dtype f32 or bf16, conv_width <= 8; the fast
+ * path (q/k norm fused) needs conv_dim, head_k_dim and head_v_dim multiples of
+ * 8, head_k_dim / 8 a power of two <= 32 and 16-byte aligned x and weights;
+ * other shapes run a two-pass path.
+ */
+int lsc_gdn_prefill_conv(lsc_pool *pool, int32_t layer, const lsc_gdn_prefill_conv_args *args,
+                         void *stream);
 
 /* ---- misc ------------------------------------------------------------------- */
 

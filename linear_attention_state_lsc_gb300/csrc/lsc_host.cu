@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <initializer_list>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -39,6 +40,14 @@ int esize(int32_t dtype) {
     case LSC_F16: return 2;
     default: return 0;
   }
+}
+
+// Every pointer aligned to `a` bytes (NULL counts as aligned).  Device arrays
+// must be aligned to their element size: a misaligned element access faults.
+bool all_aligned(std::initializer_list<const void *> ptrs, uintptr_t a) {
+  for (const void *q : ptrs)
+    if ((uintptr_t)q % a) return false;
+  return true;
 }
 
 // Bound of every device-side wait (mbarrier), in nanoseconds.
@@ -466,6 +475,9 @@ int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, voi
     return LSC_ERR_INVALID_ARG;
   if (g.conv_dtype == LSC_F16 || g.ssm_dtype == LSC_F16) return LSC_ERR_UNSUPPORTED;
   if (g.conv_width > 8 || g.Hv / Hk > 8 || a->n > 65535) return LSC_ERR_UNSUPPORTED;
+  if (!all_aligned({a->x, a->conv_weight}, (uintptr_t)esize(g.conv_dtype)) ||
+      !all_aligned({a->idx, a->alpha, a->beta, a->out}, 4))
+    return LSC_ERR_MISALIGNED;
   rc = check_device(p);
   if (rc != LSC_OK) return rc;
   if (a->n == 0) return LSC_OK;
@@ -505,6 +517,60 @@ int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, voi
   return lsc::launch_decode(d, g.dk, g.ssm_dtype, (cudaStream_t)stream);
 }
 
+int lsc_gdn_prefill_conv(lsc_pool *p, int32_t layer, const lsc_gdn_prefill_conv_args *a, void *stream) {
+  if (!p || !a) return LSC_ERR_INVALID_ARG;
+  uint8_t *region;
+  int rc = layer_base(p, layer, &region);
+  if (rc != LSC_OK) return rc;
+  const lsc::Geom &g = p->g;
+  const int32_t Hk = a->num_k_heads;
+  if (a->n_seq < 0 || a->total_tokens < 0 || a->reserved != 0 || Hk <= 0 || g.Hv % Hk != 0 ||
+      g.conv_dim != 2 * Hk * g.dk + g.Hv * g.dv)
+    return LSC_ERR_INVALID_ARG;
+  if (a->n_seq == 0 && a->total_tokens > 0) return LSC_ERR_INVALID_ARG;
+  if (a->n_seq > 0 && (!a->idx || !a->cu_seqlens)) return LSC_ERR_INVALID_ARG;
+  if (a->total_tokens > 0 && (!a->x || !a->conv_weight || !a->q || !a->k || !a->v)) return LSC_ERR_INVALID_ARG;
+  if (g.conv_dtype == LSC_F16) return LSC_ERR_UNSUPPORTED;
+  if (g.conv_width > 8 || a->n_seq > 65535) return LSC_ERR_UNSUPPORTED;
+  if (!all_aligned({a->x, a->conv_weight}, (uintptr_t)esize(g.conv_dtype)) ||
+      !all_aligned({a->idx, a->cu_seqlens, a->q, a->k, a->v}, 4))
+    return LSC_ERR_MISALIGNED;
+  rc = check_device(p);
+  if (rc != LSC_OK) return rc;
+  if (a->n_seq == 0) return LSC_OK;
+  lsc::PrefillConvParams d{};
+  d.layer = region;
+  d.page = g.page;
+  d.num_slots = g.num_slots;
+  d.conv_dim = g.conv_dim;
+  d.conv_width = g.conv_width;
+  d.conv_bf16 = g.conv_dtype == LSC_BF16;
+  d.Hk = Hk;
+  d.Hv = g.Hv;
+  d.dk = g.dk;
+  d.dv = g.dv;
+  d.n_seq = a->n_seq;
+  d.total_tokens = a->total_tokens;
+  d.idx = a->idx;
+  d.has_init = a->has_init;
+  d.cu = a->cu_seqlens;
+  d.x = a->x;
+  d.w = a->conv_weight;
+  d.q = a->q;
+  d.k = a->k;
+  d.v = a->v;
+  d.status = g.status;
+  // The fast path reads 8-channel groups of x, the weights and the conv state
+  // with 16-byte loads, writes 8 outputs as two 16-byte stores, and reduces a
+  // q/k head's sum of squares over dk / 8 consecutive lanes.
+  const int tph = g.dk / 8;
+  const bool pow2 = tph > 0 && tph <= 32 && (tph & (tph - 1)) == 0;
+  const uintptr_t al = (uintptr_t)a->x | (uintptr_t)a->conv_weight | (uintptr_t)a->q | (uintptr_t)a->k |
+                       (uintptr_t)a->v;
+  d.vec = g.conv_dim % 8 == 0 && g.dk % 8 == 0 && g.dv % 8 == 0 && pow2 && (al % 16) == 0 ? 1 : 0;
+  return lsc::launch_prefill_conv(d, (cudaStream_t)stream);
+}
+
 int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *a, void *stream) {
   if (!p || !a) return LSC_ERR_INVALID_ARG;
   uint8_t *region;
@@ -517,6 +583,7 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
   if (a->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->alpha || !a->beta || !a->out))
     return LSC_ERR_INVALID_ARG;
   if (((uintptr_t)a->q | (uintptr_t)a->k) & 15) return LSC_ERR_MISALIGNED;
+  if (!all_aligned({a->idx, a->cu_seqlens, a->v, a->alpha, a->beta, a->out}, 4)) return LSC_ERR_MISALIGNED;
   if (g.ssm_dtype == LSC_F16) return LSC_ERR_UNSUPPORTED;
   if (a->n_seq > 65535) return LSC_ERR_UNSUPPORTED;
   rc = check_device(p);

@@ -100,4 +100,22 @@ struct RecurrentParams {
 };
 int launch_recurrent(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
 
+struct PrefillConvParams {
+  uint8_t *layer;
+  int64_t page;
+  int32_t num_slots, conv_dim, conv_width, conv_bf16;
+  int32_t Hk, Hv, dk, dv;
+  int32_t n_seq, total_tokens;
+  const int32_t *idx;
+  const uint8_t *has_init;
+  const int32_t *cu;
+  const void *x;
+  const void *w;
+  float *q, *k, *v;
+  int32_t *status;
+  int32_t vec;  // fast path: 8-channel groups, q/k norm fused (see lsc_prefill.cu)
+};
+// returns LSC_OK, LSC_ERR_UNSUPPORTED or LSC_ERR_CUDA
+int launch_prefill_conv(const PrefillConvParams &p, cudaStream_t stream);
+
 }  // namespace lsc

@@ -1,0 +1,362 @@
+// lsc_prefill.cu -- the prefill conv of a resumed prefill: a depthwise causal
+// conv over each sequence's tokens that starts from the slot's conv state,
+// the q | k | v split with the per-head L2 norm of q and k, and the write-back
+// of the new conv state.
+//
+// Sources, cited by page title and section:
+//   [VA] "非连续 KV Cache" §6 (causal_conv1d_fn beside causal_conv1d_update)
+//   [KP] "Kapitsa 源码拆解 05：前缀缓存与模型状态恢复", "相同前缀不一定能全部复用"
+//        (the prefill continues from the restored checkpoint)
+//
+// The conv state of channel c holds its last W-1 inputs, oldest first.  Token
+// t of a sequence sees the window [x_(t-W+1) .. x_t]; window inputs before the
+// sequence's first token are the slot's conv state (zero when cold).
+// y = SiLU(sum_j w[c][j] window[j]), no bias.  Afterwards the slot holds the last
+// W-1 entries of [old state, the sequence's x].
+//
+// Kernels (one stream, in order):
+//   prefill_conv_vec_kernel  (fast path) thread = 8 consecutive channels over a
+//       tile of kPrefillTile tokens of the flattened token axis, rolling the
+//       window in registers, x read with 16-byte loads one token ahead; the
+//       sum of squares of a q/k head is reduced over the head's dk/8 lanes with
+//       shuffles, so q and k leave normalised.  HBM-bound: per token and channel
+//       one conv-dtype read and one fp32 write.
+//   prefill_conv_scalar_kernel + qk_norm_kernel  (any other shape) one channel
+//       per thread, then q and k normalised in a second pass.
+//   prefill_state_kernel  the new conv state of each sequence (after the
+//       outputs, so no tile reads a state another tile has already replaced).
+#include "lsc_gdn_common.cuh"
+
+namespace lsc {
+namespace {
+
+constexpr int kPrefillThreads = 256;
+constexpr int kPrefillTile = 64;  // tokens per CTA
+
+// The sequence holding token t: the largest s with cu[s] <= t.  Well defined for
+// consistent cu_seqlens; for others the caller checks the result.
+__device__ __forceinline__ int seq_of(const int32_t *cu, int n_seq, int t) {
+  int lo = 0, hi = n_seq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Eight floats, passed by value.
+struct F8 {
+  float v[8];
+};
+
+// Eight consecutive conv-dtype values at a 16-byte-aligned address, as floats.
+template <typename TC> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+  __device__ __forceinline__ static F8 load(const void *p) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    F8 f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f.v[2 * i] = __uint_as_float(w[i] << 16);
+      f.v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+    return f;
+  }
+};
+template <> struct Vec8<float> {
+  __device__ __forceinline__ static F8 load(const void *p) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    F8 f;
+    f.v[0] = a.x; f.v[1] = a.y; f.v[2] = a.z; f.v[3] = a.w;
+    f.v[4] = b.x; f.v[5] = b.y; f.v[6] = b.z; f.v[7] = b.w;
+    return f;
+  }
+};
+
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+
+// Where channel c's output goes: q [T, Hk dk], k [T, Hk dk] or v [T, Hv dv].
+__device__ __forceinline__ float *out_ptr(const PrefillConvParams &p, int64_t t, int c) {
+  const int qk = p.Hk * p.dk;
+  if (c < qk) return p.q + t * qk + c;
+  if (c < 2 * qk) return p.k + t * qk + (c - qk);
+  return p.v + t * (int64_t)(p.Hv * p.dv) + (c - 2 * qk);
+}
+
+// Is token t inside sequence s, with consistent bounds?  Reports otherwise.
+__device__ __forceinline__ bool seq_ok(const PrefillConvParams &p, int s, int t, int &ts, int &te) {
+  ts = p.cu[s];
+  te = p.cu[s + 1];
+  const bool ok = ts >= 0 && te >= ts && te <= p.total_tokens && ts <= t && t < te;
+  if (!ok) report(p.status, LSC_ERR_INVALID_ARG);
+  return ok;
+}
+
+// ------------------------------------------------------------------ fast path
+template <typename TC, int CW>
+__global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const __grid_constant__ PrefillConvParams p) {
+  constexpr int WW = CW ? CW : kMaxTaps;  // register window, W <= WW
+  constexpr int esc = (int)sizeof(TC);
+  const int W = CW ? CW : p.conv_width;
+  const int C = p.conv_dim;
+  const int grp = blockIdx.x * kPrefillThreads + threadIdx.x;
+  const bool live = grp < C / 8;
+  const int c0 = live ? grp * 8 : 0;
+  const int lanes_per_head = p.dk / 8;  // a power of two <= 32
+  const bool is_qk = c0 < 2 * p.Hk * p.dk;
+  const int t_begin = blockIdx.y * kPrefillTile;
+  const int t_end = min(t_begin + kPrefillTile, p.total_tokens);
+  if (t_begin >= t_end) return;  // uniform over the CTA
+
+  __shared__ int s_first;
+  if (threadIdx.x == 0) s_first = seq_of(p.cu, p.n_seq, t_begin);
+  __syncthreads();
+
+  // weights of the group's 8 channels
+  float wt[8][WW];
+  {
+    F8 buf[WW];  // the 8 W weights of the group, row-major [8][W]
+    const uint8_t *wp = reinterpret_cast<const uint8_t *>(p.w) + (int64_t)c0 * W * esc;
+#pragma unroll
+    for (int v = 0; v < WW; ++v) buf[v] = v < W ? Vec8<TC>::load(wp + v * 8 * esc) : F8{};
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+      for (int j = 0; j < WW; ++j) {
+        float wv = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8 * WW; ++e)
+          if (e == cc * W + j && j < W) wv = buf[e / 8].v[e % 8];
+        wt[cc][j] = wv;
+      }
+  }
+  const uint8_t *xg = reinterpret_cast<const uint8_t *>(p.x) + (int64_t)c0 * esc;
+  const int64_t xrow = (int64_t)C * esc;
+
+  F8 hist[WW - 1];  // window inputs before the current token, oldest first
+  int s = s_first;
+  // The tile is walked in segments, one per sequence piece: the window is
+  // rebuilt at a segment's first token, then slides token by token.
+  for (int t = t_begin; t < t_end;) {
+    while (s + 1 < p.n_seq && p.cu[s + 1] <= t) ++s;
+    int ts, te;
+    const bool ok = seq_ok(p, s, t, ts, te);
+    const int seg_end = ok ? min(te, t_end) : t + 1;  // a bad sequence is re-checked token by token
+    int32_t slot = ok ? p.idx[s] : -1;
+    if (slot >= p.num_slots) {
+      report(p.status, LSC_ERR_OUT_OF_RANGE);
+      slot = -1;
+    }
+    const bool warm = slot >= 0 && (p.has_init == nullptr || p.has_init[s] != 0);
+    {
+      F8 st[WW - 1];  // the group's conv state, row-major [8][W - 1]
+#pragma unroll
+      for (int v = 0; v < WW - 1; ++v) st[v] = F8{};
+      if (warm && live && t - ts < W - 1) {
+        const uint8_t *sp = p.layer + (int64_t)slot * p.page + (int64_t)c0 * (W - 1) * esc;
+#pragma unroll
+        for (int v = 0; v < WW - 1; ++v)
+          if (v < W - 1) st[v] = Vec8<TC>::load(sp + v * 8 * esc);
+      }
+      // hist[j] is token t - (W - 1 - j); before the sequence it is state
+      // entry (t - ts) + j (entries are picked with compile-time indices)
+#pragma unroll
+      for (int j = 0; j < WW - 1; ++j) {
+        if (j >= W - 1) continue;
+        const int back = W - 1 - j;
+        if (t - back >= ts) {
+          hist[j] = Vec8<TC>::load(xg + (int64_t)(t - back) * xrow);
+        } else {
+          const int e = (t - ts) + j;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            float val = 0.f;
+#pragma unroll
+            for (int ee = 0; ee < 8 * (WW - 1); ++ee)
+              if (ee == cc * (W - 1) + e) val = st[ee / 8].v[ee % 8];
+            hist[j].v[cc] = val;
+          }
+        }
+      }
+    }
+    F8 xn = Vec8<TC>::load(xg + (int64_t)t * xrow);
+    for (; t < seg_end; ++t) {
+      const F8 xc = xn;
+      if (t + 1 < seg_end) xn = Vec8<TC>::load(xg + (int64_t)(t + 1) * xrow);  // one token ahead
+      float y[8];
+      float ss = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < WW; ++j) {
+          if (j < W - 1) z = fmaf(wt[cc][j], hist[j].v[cc], z);
+          else if (j == W - 1) z = fmaf(wt[cc][j], xc.v[cc], z);
+        }
+        y[cc] = silu(z);
+        ss = fmaf(y[cc], y[cc], ss);
+      }
+      // slide the window: drop the oldest input, append this token's x
+#pragma unroll
+      for (int j = 0; j < WW - 1; ++j) {
+        if (j < W - 2) hist[j] = hist[j + 1 < WW - 1 ? j + 1 : j];
+        else if (j == W - 2) hist[j] = xc;
+      }
+      // sum of squares of the head: its dk/8 lanes are consecutive and aligned
+      for (int m = 1; m < lanes_per_head; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      if (live) {
+        const float scale = is_qk ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
+        float4 *o = reinterpret_cast<float4 *>(out_ptr(p, t, c0));
+        if (slot >= 0) {
+          o[0] = make_float4(y[0] * scale, y[1] * scale, y[2] * scale, y[3] * scale);
+          o[1] = make_float4(y[4] * scale, y[5] * scale, y[6] * scale, y[7] * scale);
+        } else {
+          o[0] = o[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- any shape
+template <typename TC>
+__global__ void __launch_bounds__(kPrefillThreads) prefill_conv_scalar_kernel(const __grid_constant__ PrefillConvParams p) {
+  using E = Elem<TC>;
+  const int W = p.conv_width, C = p.conv_dim;
+  const int c = blockIdx.x * kPrefillThreads + threadIdx.x;
+  const bool live = c < C;
+  const int t_begin = blockIdx.y * kPrefillTile;
+  const int t_end = min(t_begin + kPrefillTile, p.total_tokens);
+  if (t_begin >= t_end) return;
+  __shared__ int s_first;
+  if (threadIdx.x == 0) s_first = seq_of(p.cu, p.n_seq, t_begin);
+  __syncthreads();
+  if (!live) return;
+  float wt[kMaxTaps], hist[kMaxTaps - 1];
+#pragma unroll
+  for (int j = 0; j < kMaxTaps; ++j) wt[j] = j < W ? E::ld(p.w, (int64_t)c * W + j) : 0.f;
+  int s = s_first, ts = 0, te = 0;
+  int32_t slot = -1;
+  for (int t = t_begin; t < t_end; ++t) {
+    if (t == t_begin || t >= te) {
+      while (s + 1 < p.n_seq && p.cu[s + 1] <= t) ++s;
+      const bool ok = seq_ok(p, s, t, ts, te);
+      slot = ok ? p.idx[s] : -1;
+      if (slot >= p.num_slots) {
+        report(p.status, LSC_ERR_OUT_OF_RANGE);
+        slot = -1;
+      }
+      if (!ok) te = t + 1;
+      const bool warm = slot >= 0 && (p.has_init == nullptr || p.has_init[s] != 0);
+      const uint8_t *sp = slot >= 0 ? p.layer + (int64_t)slot * p.page : nullptr;
+#pragma unroll
+      for (int j = 0; j < kMaxTaps - 1; ++j) {
+        if (j >= W - 1) continue;
+        const int back = W - 1 - j;  // hist[j] is token t - back
+        hist[j] = t - back >= ts ? E::ld(p.x, (int64_t)(t - back) * C + c)
+                                 : (warm ? E::ld(sp, (int64_t)c * (W - 1) + (t - ts) + j) : 0.f);
+      }
+    }
+    const float xc = E::ld(p.x, (int64_t)t * C + c);
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTaps; ++j) {
+      if (j < W - 1) z = fmaf(wt[j], hist[j], z);
+      else if (j == W - 1) z = fmaf(wt[j], xc, z);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTaps - 1; ++j) {
+      if (j < W - 2) hist[j] = hist[j + 1 < kMaxTaps - 1 ? j + 1 : j];
+      else if (j == W - 2) hist[j] = xc;
+    }
+    *out_ptr(p, t, c) = slot >= 0 ? silu(z) : 0.f;
+  }
+}
+
+// q and k of every (token, head) divided by sqrt(sum of squares + 1e-6): one
+// warp per (token, head).
+__global__ void __launch_bounds__(kPrefillThreads) qk_norm_kernel(const __grid_constant__ PrefillConvParams p) {
+  const int64_t wid = (int64_t)blockIdx.x * (kPrefillThreads / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = (int64_t)p.total_tokens * p.Hk * 2;
+  if (wid >= n) return;
+  const int64_t th = wid / 2;  // (token, head)
+  float *base = ((wid & 1) ? p.k : p.q) + th * p.dk;
+  float ss = 0.f;
+  for (int c = lane; c < p.dk; c += 32) ss = fmaf(base[c], base[c], ss);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+  const float inv = 1.f / sqrtf(ss + 1e-6f);
+  for (int c = lane; c < p.dk; c += 32) base[c] *= inv;
+}
+
+// The new conv state of each sequence: the last W-1 entries of [old state, x],
+// copied bit for bit.  One thread per (sequence, channel).
+template <typename TB>  // raw element bits: uint16_t (bf16) or uint32_t (f32)
+__global__ void __launch_bounds__(kPrefillThreads) prefill_state_kernel(const __grid_constant__ PrefillConvParams p) {
+  const int W = p.conv_width, C = p.conv_dim;
+  const int c = blockIdx.x * kPrefillThreads + threadIdx.x;
+  const int s = blockIdx.y;
+  if (c >= C) return;
+  const int ts = p.cu[s], te = p.cu[s + 1];
+  if (ts < 0 || te < ts || te > p.total_tokens) {  // inconsistent cu_seqlens: touch nothing
+    if (c == 0) report(p.status, LSC_ERR_INVALID_ARG);
+    return;
+  }
+  const int32_t slot = p.idx[s];
+  if (slot < 0 || slot >= p.num_slots) return;
+  const bool warm = p.has_init == nullptr || p.has_init[s] != 0;
+  TB *st = reinterpret_cast<TB *>(p.layer + (int64_t)slot * p.page) + (int64_t)c * (W - 1);
+  const TB *x = reinterpret_cast<const TB *>(p.x);
+  const int L = te - ts;
+  TB old[kMaxTaps - 1], nv[kMaxTaps - 1];
+#pragma unroll
+  for (int j = 0; j < kMaxTaps - 1; ++j) old[j] = (j < W - 1 && warm) ? st[j] : TB(0);
+#pragma unroll
+  for (int j = 0; j < kMaxTaps - 1; ++j) {
+    if (j >= W - 1) continue;
+    const int pos = L - (W - 1) + j;  // position in the sequence of the entry
+    nv[j] = pos >= 0 ? x[(int64_t)(ts + pos) * C + c] : old[(W - 1) + pos];
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxTaps - 1; ++j)
+    if (j < W - 1) st[j] = nv[j];
+}
+
+template <typename TC>
+int launch_prefill_t(const PrefillConvParams &p, cudaStream_t s) {
+  const int tiles = (p.total_tokens + kPrefillTile - 1) / kPrefillTile;
+  if (tiles > 0) {
+    if (p.vec) {
+      const dim3 grid((p.conv_dim / 8 + kPrefillThreads - 1) / kPrefillThreads, tiles);
+      if (p.conv_width == 4) prefill_conv_vec_kernel<TC, 4><<<grid, kPrefillThreads, 0, s>>>(p);
+      else prefill_conv_vec_kernel<TC, 0><<<grid, kPrefillThreads, 0, s>>>(p);
+    } else {
+      const dim3 grid((p.conv_dim + kPrefillThreads - 1) / kPrefillThreads, tiles);
+      prefill_conv_scalar_kernel<TC><<<grid, kPrefillThreads, 0, s>>>(p);
+      const int64_t warps = (int64_t)p.total_tokens * p.Hk * 2;
+      const int64_t blocks = (warps + kPrefillThreads / 32 - 1) / (kPrefillThreads / 32);
+      if (blocks > 0) qk_norm_kernel<<<(unsigned)blocks, kPrefillThreads, 0, s>>>(p);
+    }
+    if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;
+  }
+  if (p.n_seq > 0) {
+    const dim3 grid((p.conv_dim + kPrefillThreads - 1) / kPrefillThreads, p.n_seq);
+    if (sizeof(TC) == 2) prefill_state_kernel<uint16_t><<<grid, kPrefillThreads, 0, s>>>(p);
+    else prefill_state_kernel<uint32_t><<<grid, kPrefillThreads, 0, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;
+  }
+  return LSC_OK;
+}
+
+}  // namespace
+
+int launch_prefill_conv(const PrefillConvParams &p, cudaStream_t stream) {
+  if (p.conv_width < 2 || p.conv_width > kMaxTaps) return LSC_ERR_UNSUPPORTED;
+  return p.conv_bf16 ? launch_prefill_t<__nv_bfloat16>(p, stream) : launch_prefill_t<float>(p, stream);
+}
+
+}  // namespace lsc

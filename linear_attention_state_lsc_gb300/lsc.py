@@ -104,6 +104,13 @@ class lsc_pc_report(C.Structure):
                                           "skip_cached", "skip_unaligned", "skip_no_slot", "reserved")]
 
 
+class lsc_gdn_prefill_conv_args(C.Structure):
+    _fields_ = [("n_seq", C.c_int32), ("num_k_heads", C.c_int32), ("total_tokens", C.c_int32),
+                ("reserved", C.c_int32), ("idx", C.c_void_p), ("has_init", C.c_void_p),
+                ("cu_seqlens", C.c_void_p), ("x", C.c_void_p), ("conv_weight", C.c_void_p),
+                ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p)]
+
+
 _lib = None
 
 
@@ -129,6 +136,7 @@ def load():
         "lsc_scatter": ([P, I32, P, I32, P, P, P], C.c_int),
         "lsc_gdn_decode": ([P, I32, C.POINTER(lsc_gdn_decode_args), P], C.c_int),
         "lsc_gdn_recurrent": ([P, I32, C.POINTER(lsc_gdn_recurrent_args), P], C.c_int),
+        "lsc_gdn_prefill_conv": ([P, I32, C.POINTER(lsc_gdn_prefill_conv_args), P], C.c_int),
         "lsc_pc_create": ([I32, I32, C.POINTER(P)], C.c_int),
         "lsc_pc_destroy": ([P], C.c_int),
         "lsc_pc_allocate_live_slot": ([P, I64, C.POINTER(I32)], C.c_int),
@@ -301,6 +309,15 @@ def recurrent_args(n_seq, num_k_heads, total_tokens, idx, has_init, cu_seqlens, 
 
 def lsc_gdn_recurrent(pool, layer, args, stream=None):
     return load().lsc_gdn_recurrent(pool, layer, C.byref(args), _stream(stream))
+
+
+def prefill_conv_args(n_seq, num_k_heads, total_tokens, idx, has_init, cu_seqlens, x, conv_weight, q, k, v):
+    return lsc_gdn_prefill_conv_args(n_seq, num_k_heads, total_tokens, 0, ptr(idx), ptr(has_init),
+                                     ptr(cu_seqlens), ptr(x), ptr(conv_weight), ptr(q), ptr(k), ptr(v))
+
+
+def lsc_gdn_prefill_conv(pool, layer, args, stream=None):
+    return load().lsc_gdn_prefill_conv(pool, layer, C.byref(args), _stream(stream))
 
 
 # ---- scheduler-side prefix cache (include/lsc_prefix_cache.h) ---------------
