@@ -488,6 +488,40 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     L.lsc_pool_destroy(pool)
     del buf, out, dev
     torch.cuda.empty_cache()
+
+    # prefill conv of the same token mix (x bf16 [T, 8192] -> q, k, v fp32, conv
+    # states updated), on two GDN layers of c4's shapes, alternating
+    w = W.get("c4")
+    w.layers = [W.GDN, W.ATTN, W.GDN]
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    cu, x, cw = W.prefill_inputs(w, lengths, seed=0, layer=0)
+    T = int(cu[-1])
+    idx = torch.from_numpy(rng.permutation(w.num_slots)[:64].astype(np.int32)).cuda()
+    xd = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    cwd = torch.from_numpy(cw).to(torch.bfloat16).cuda()
+    q = torch.empty((T, w.num_k_heads, w.head_k_dim), device="cuda")
+    k = torch.empty_like(q)
+    v = torch.empty((T, w.num_v_heads, w.head_v_dim), device="cuda")
+    pa = L.prefill_conv_args(64, w.num_k_heads, T, idx, has, torch.from_numpy(cu).cuda(), xd, cwd, q, k, v)
+    i_l = [0]
+
+    def conv_one():
+        i_l[0] += 1
+        assert L.lsc_gdn_prefill_conv(pool, w.gdn_layers[i_l[0] % 2], pa, fwd) == L.LSC_OK
+
+    t = timed(conv_one, 10)
+    C, Wd = w.conv_dim, w.conv_width
+    pbytes = T * C * (2 + 4) + C * Wd * 2 + 64 * C * (Wd - 1) * 2 * 2
+    parts["prefill_conv_c4"] = {"workload": f"c4: 64 sequences, {T} tokens, conv [8192, 3] bf16 from the slots, "
+                                            "q/k/v fp32 out, one layer per launch",
+                                "kernel": "prefill_conv_vec_kernel<bf16,4> + prefill_state_kernel",
+                                "launch_ms": round(t * 1e3, 4), "bytes_per_launch": pbytes,
+                                "GB/s": round(pbytes / t / 1e9, 1), "frac": round(pbytes / t / 1e9 / hbm_peak, 4),
+                                "bytes_basis": "x read (bf16) + q, k, v written (fp32) + weights + conv state read and "
+                                               "written per sequence"}
+    L.lsc_pool_destroy(pool)
+    del buf, xd, q, k, v
+    torch.cuda.empty_cache()
     parts["prefix_cache_host"] = measure_prefix_cache(L)
     return parts
 
@@ -680,6 +714,7 @@ NCU_CASES = {
     "decode_bf16": ("c2", 256, "decode"),    # bf16 state, 256 rows, 571 MB per launch
     "restore": ("c1", 64, "restore"),        # 64 hits x 2 layers, 549 MB per launch
     "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer
+    "prefill": ("c4", 32, "prefill"),        # prefill conv: 32 sequences of 64..2048 tokens, one layer
 }
 
 
@@ -716,6 +751,21 @@ def run_ncu_case(args):
 
         def launch(i):
             assert L.lsc_gdn_decode(pool, w.gdn_layers[i % 2], da, fwd) == L.LSC_OK
+    elif kind == "prefill":
+        lengths = W.seq_lengths(n, 64, 2048, seed=0)
+        cu, x, cw = W.prefill_inputs(w, lengths, seed=0, layer=0)
+        T = int(cu[-1])
+        idx = torch.from_numpy(rng.permutation(w.num_slots)[:n].astype(np.int32)).cuda()
+        has = torch.ones(n, dtype=torch.uint8, device="cuda")
+        q = torch.empty((T, w.num_k_heads, w.head_k_dim), device="cuda")
+        k = torch.empty_like(q)
+        v = torch.empty((T, w.num_v_heads, w.head_v_dim), device="cuda")
+        pa = L.prefill_conv_args(n, w.num_k_heads, T, idx, has, torch.from_numpy(cu).cuda(),
+                                 torch.from_numpy(x).to(torch.bfloat16).cuda(),
+                                 torch.from_numpy(cw).to(torch.bfloat16).cuda(), q, k, v)
+
+        def launch(i):
+            assert L.lsc_gdn_prefill_conv(pool, w.gdn_layers[i % 2], pa, fwd) == L.LSC_OK
     else:
         lengths = W.seq_lengths(n, 64, 512, seed=0)
         cu, q, k, vv, a, b = W.recurrent_inputs(w, lengths, seed=0, layer=0)

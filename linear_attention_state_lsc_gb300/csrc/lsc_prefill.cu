@@ -17,7 +17,9 @@
 // Kernels (one stream, in order):
 //   prefill_conv_vec_kernel  (fast path) thread = 8 consecutive channels over a
 //       tile of kPrefillTile tokens of the flattened token axis, rolling the
-//       window in registers, x read with 16-byte loads one token ahead; the
+//       window in registers; each thread streams its x rows through a
+//       128-byte cp.async ring in shared memory (7 bf16 or 3 f32 rows in
+//       flight per thread without holding registers); the
 //       sum of squares of a q/k head is reduced over the head's dk/8 lanes with
 //       shuffles, so q and k leave normalised.  HBM-bound: per token and channel
 //       one conv-dtype read and one fp32 write.
@@ -32,6 +34,7 @@ namespace {
 
 constexpr int kPrefillThreads = 256;
 constexpr int kPrefillTile = 64;  // tokens per CTA
+constexpr int kPrefillRingBytes = 128;  // per thread: the cp.async ring of x rows in shared memory
 
 // The sequence holding token t: the largest s with cu[s] <= t.  Well defined for
 // consistent cu_seqlens; for others the caller checks the result.
@@ -44,6 +47,27 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int n_seq, int t) {
   }
   return lo;
 }
+
+// Eight conv-dtype values from shared memory (16-byte aligned), as floats.
+template <typename TC> struct Smem8;
+template <> struct Smem8<__nv_bfloat16> {
+  __device__ __forceinline__ static void unpack(const uint4 *q, float *f) {
+    const uint4 u = q[0];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+template <> struct Smem8<float> {
+  __device__ __forceinline__ static void unpack(const uint4 *q, float *f) {
+    const uint4 a = q[0], b = q[1];
+    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+    f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+  }
+};
 
 // Eight floats, passed by value.
 struct F8 {
@@ -136,6 +160,9 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const
   const uint8_t *xg = reinterpret_cast<const uint8_t *>(p.x) + (int64_t)c0 * esc;
   const int64_t xrow = (int64_t)C * esc;
 
+  constexpr int NH = 8 * esc / 16;  // 16-byte pieces of one x row of the group
+  constexpr int A = kPrefillRingBytes / (8 * esc);  // ring slots: 8 rows (bf16) or 4 (f32)
+  __shared__ __align__(16) uint4 ring[A][NH][kPrefillThreads];
   F8 hist[WW - 1];  // window inputs before the current token, oldest first
   int s = s_first;
   // The tile is walked in segments, one per sequence piece: the window is
@@ -182,10 +209,31 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const
         }
       }
     }
-    F8 xn = Vec8<TC>::load(xg + (int64_t)t * xrow);
+    // the ring: slot (u % A) holds token seg_t0 + u.  One cp.async group per
+    // token (empty past the segment).  Token u + A - 1 is issued into the slot
+    // read one token earlier, then wait_group<A - 1> leaves token u landed.
+    const int seg_t0 = t;
+#pragma unroll
+    for (int u = 0; u < A - 1; ++u) {
+      if (seg_t0 + u < seg_end)
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          cp_async16(&ring[u][h][threadIdx.x], xg + (int64_t)(seg_t0 + u) * xrow + h * 16);
+      cp_async_commit();
+    }
     for (; t < seg_end; ++t) {
-      const F8 xc = xn;
-      if (t + 1 < seg_end) xn = Vec8<TC>::load(xg + (int64_t)(t + 1) * xrow);  // one token ahead
+      const int u = t - seg_t0;
+      if (t + A - 1 < seg_end)
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          cp_async16(&ring[(u + A - 1) % A][h][threadIdx.x], xg + (int64_t)(t + A - 1) * xrow + h * 16);
+      cp_async_commit();
+      cp_async_wait<A - 1>();
+      F8 xc;
+      uint4 raw[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) raw[h] = ring[u % A][h][threadIdx.x];
+      Smem8<TC>::unpack(raw, xc.v);
       float y[8];
       float ss = 0.f;
 #pragma unroll
@@ -219,6 +267,7 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const
       }
     }
   }
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------- any shape
