@@ -57,10 +57,53 @@ def lib():
                                            P, P, P, P, P, P]
         _lib.orc_gdn_prefill_conv.argtypes = [C.POINTER(_Pool), P, C.c_int, P, P, P, C.c_int,
                                                P, P, P, P, P]
+        _lib.orc_kv_layout.argtypes = [C.POINTER(_KvPool), C.POINTER(_KvLayout)]
+        _lib.orc_copy_prefix.argtypes = [C.POINTER(_KvPool), P, P, P, P, C.c_int]
         _lib.orc_bf16_bits.argtypes = [C.c_float]
         _lib.orc_bf16_bits.restype = C.c_ushort
         _lib.orc_num_threads.restype = C.c_int
     return _lib
+
+
+class _KvPool(C.Structure):
+    _fields_ = [("num_layers", C.c_int), ("num_blocks", C.c_int), ("block_tokens", C.c_int),
+                ("num_kv_heads", C.c_int), ("head_dim", C.c_int), ("dtype", C.c_int), ("page_bytes", C.c_longlong)]
+
+
+class _KvLayout(C.Structure):
+    _fields_ = [(n, C.c_longlong) for n in ("row_bytes", "payload", "page", "block_stride_elems",
+                                             "lane_stride_elems", "region_bytes")]
+
+
+class KvPool:
+    """Oracle-side description of an attention K/V pool."""
+
+    def __init__(self, num_layers, num_blocks, block_tokens, num_kv_heads, head_dim, dtype, page_bytes):
+        self.s = _KvPool(num_layers, num_blocks, block_tokens, num_kv_heads, head_dim, dtype, page_bytes)
+
+    def __getattr__(self, name):
+        s = self.__dict__.get("s")
+        if s is not None and name in dict(_KvPool._fields_):
+            return getattr(s, name)
+        raise AttributeError(name)
+
+
+def kv_layout(pool):
+    """Returns (rc, dict of _KvLayout fields)."""
+    L = _KvLayout()
+    rc = lib().orc_kv_layout(C.byref(pool.s), C.byref(L))
+    return rc, {n: getattr(L, n) for n, _ in _KvLayout._fields_}
+
+
+def copy_prefix(pool, regions, src, dst, n_tokens):
+    """regions: list of uint8 arrays, one per attention layer (2 lanes each)."""
+    src, dst, nt = _c(src, np.int32), _c(dst, np.int32), _c(n_tokens, np.int32)
+    ptrs = (C.c_void_p * max(pool.num_layers, 1))()
+    for l in range(pool.num_layers):
+        r = regions[l]
+        assert r.dtype == np.uint8 and r.flags.c_contiguous
+        ptrs[l] = r.ctypes.data
+    return lib().orc_copy_prefix(C.byref(pool.s), ptrs, _ptr(src), _ptr(dst), _ptr(nt), len(src))
 
 
 class Pool:

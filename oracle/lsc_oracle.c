@@ -642,6 +642,98 @@ int orc_gdn_prefill_conv(const orc_pool *p, unsigned char *region, int n_seq, co
   return ORC_OK;
 }
 
+/* ---- attention K/V blocks and copy_prefix -------------------------------- */
+
+/*
+ * An attention K/V pool: per attention layer, one allocation of two lanes
+ * [K lane][V lane], each lane num_blocks physical pages; a block's logical
+ * payload is block_tokens x kv_heads x head_dim elements followed by padding.
+ *
+ * [VA] §3: the block stride of the view is the physical page size over the
+ * element size, not the logical block size; §3.4: the merged two-lane view
+ * (2, blocks, block_tokens, kv_heads, head_dim) takes its lane stride and block
+ * stride from the physical allocation.
+ * READING 12: inside a block, token-major (the §3.4 order); §3 lists
+ * [block, kv_head, token, head_dim] for the unmerged view -- the page uses both
+ * orders, and the copy of a token prefix below is defined on token rows either
+ * way.
+ */
+typedef struct {
+  int num_layers, num_blocks, block_tokens, num_kv_heads, head_dim, dtype;
+  long long page_bytes;
+} orc_kv_pool;
+
+typedef struct {
+  long long row_bytes;          /* one token row: kv_heads x head_dim elements */
+  long long payload;            /* block_tokens rows */
+  long long page;
+  long long block_stride_elems; /* page / element size */
+  long long lane_stride_elems;  /* num_blocks pages, in elements */
+  long long region_bytes;       /* one layer: 2 lanes */
+} orc_kv_layout_t;
+
+int orc_kv_layout(const orc_kv_pool *p, orc_kv_layout_t *out) {
+  if (!p || !out || p->num_layers < 0 || p->num_blocks <= 0 || p->block_tokens <= 0 || p->num_kv_heads <= 0 ||
+      p->head_dim <= 0)
+    return ORC_REJECT_ARG;
+  const int es = elem_size(p->dtype);
+  if (!es) return ORC_REJECT_ARG;
+  orc_kv_layout_t L;
+  L.row_bytes = (long long)p->num_kv_heads * p->head_dim * es;
+  L.payload = L.row_bytes * p->block_tokens;
+  L.page = p->page_bytes;
+  if (L.page < L.payload || L.page % es) return ORC_REJECT_LAYOUT;
+  L.block_stride_elems = L.page / es;
+  L.lane_stride_elems = (long long)p->num_blocks * L.page / es;
+  L.region_bytes = 2LL * p->num_blocks * L.page;
+  *out = L;
+  return ORC_OK;
+}
+
+/*
+ * copy_prefix: for op r, token rows [0, n_tokens[r]) of block src[r] are copied
+ * to block dst[r] in both lanes of every attention layer.
+ *
+ * [KP] "混合架构需要同时保存 KV 缓存和递归状态" (figure 2): reusing a prefix in
+ * another slot copies its KV with copy_prefix, beside the restore of the
+ * recurrent state.  READING 13: a prefix of T tokens is given block by block
+ * (full blocks, then the partial last one); rows past n_tokens, the block's
+ * padding, the source blocks and every other block stay as they were.  Ops with
+ * n_tokens == 0 copy nothing and are not checked; copying ops must name blocks
+ * in range, distinct destinations, and no source that is a destination.
+ */
+int orc_copy_prefix(const orc_kv_pool *p, unsigned char *const *regions, const int *src, const int *dst,
+                    const int *n_tokens, int n_ops) {
+  orc_kv_layout_t L;
+  int rc = orc_kv_layout(p, &L);
+  if (rc != ORC_OK) return rc;
+  if (n_ops < 0 || (n_ops > 0 && (!src || !dst || !n_tokens))) return ORC_REJECT_ARG;
+  for (int r = 0; r < n_ops; ++r) {
+    if (n_tokens[r] < 0 || n_tokens[r] > p->block_tokens) return ORC_REJECT_ARG;
+    if (n_tokens[r] == 0) continue;
+    if (src[r] < 0 || src[r] >= p->num_blocks || dst[r] < 0 || dst[r] >= p->num_blocks) return ORC_REJECT_RANGE;
+  }
+  for (int r = 0; r < n_ops; ++r) {
+    if (n_tokens[r] == 0) continue;
+    for (int q = 0; q < n_ops; ++q) {
+      if (n_tokens[q] == 0) continue;
+      if (q < r && dst[q] == dst[r]) return ORC_REJECT_DUP_DST;
+      if (src[r] == dst[q]) return ORC_REJECT_SRC_IS_DST;
+    }
+  }
+  for (int l = 0; l < p->num_layers; ++l)
+    if (!regions[l]) return ORC_REJECT_ARG;
+  for (int r = 0; r < n_ops; ++r)
+    for (int l = 0; l < p->num_layers; ++l)
+      for (int lane = 0; lane < 2; ++lane) {
+        unsigned char *base = regions[l] + (long long)lane * p->num_blocks * L.page;
+        for (int t = 0; t < n_tokens[r]; ++t)
+          memcpy(base + (long long)dst[r] * L.page + t * L.row_bytes,
+                 base + (long long)src[r] * L.page + t * L.row_bytes, (size_t)L.row_bytes);
+      }
+  return ORC_OK;
+}
+
 /* Number of host threads OpenMP will use (reported beside CPU timings). */
 int orc_num_threads(void) {
 #ifdef _OPENMP
