@@ -97,6 +97,28 @@ __global__ void __launch_bounds__(kThreads) restore_kernel(const __grid_constant
   }
 }
 
+// copy_prefix: unit = (op, attention layer, lane, chunk of the op's rows);
+// the rows [0, n) of a block are one contiguous span of n * row_bytes bytes.
+__global__ void __launch_bounds__(kThreads) kv_copy_kernel(const __grid_constant__ KvPlan p) {
+  const int64_t per_op = (int64_t)p.num_layers * 2 * p.chunks_per_op;
+  const int64_t total = (int64_t)p.n_ops * per_op;
+  for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
+    const int o = (int)(u / per_op);
+    int64_t rem = u - (int64_t)o * per_op;
+    const int l = (int)(rem / (2 * p.chunks_per_op));
+    rem -= (int64_t)l * 2 * p.chunks_per_op;
+    const int lane = (int)(rem / p.chunks_per_op);
+    const int c = (int)(rem - (int64_t)lane * p.chunks_per_op);
+    const int3 op = p.op[o];
+    const int64_t span = (int64_t)op.z * p.row_bytes;
+    const int64_t off = (int64_t)c * p.chunk_bytes;
+    if (off >= span) continue;  // a partial block has fewer chunks
+    const int64_t len = span - off < p.chunk_bytes ? span - off : p.chunk_bytes;
+    uint8_t *lane_base = p.base + (int64_t)l * p.region_bytes + (int64_t)lane * p.lane_bytes;
+    copy_span(lane_base + (int64_t)op.y * p.page + off, lane_base + (int64_t)op.x * p.page + off, len);
+  }
+}
+
 // Gather: unit = (row, chunk of the conv view or of the ssm view).
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ AccessParams p) {
   const int cps = p.conv_chunks + p.ssm_chunks;
@@ -168,8 +190,11 @@ int blocks_per_sm(const void *kernel) {
 }
 
 int grid_for(const void *kernel, int num_sms, int64_t units) {
-  static int cached[3] = {0, 0, 0};
-  const int slot = kernel == (const void *)restore_kernel ? 0 : kernel == (const void *)gather_kernel ? 1 : 2;
+  static int cached[4] = {0, 0, 0, 0};
+  const int slot = kernel == (const void *)restore_kernel  ? 0
+                   : kernel == (const void *)gather_kernel ? 1
+                   : kernel == (const void *)kv_copy_kernel ? 3
+                                                            : 2;
   if (!cached[slot]) cached[slot] = blocks_per_sm(kernel);
   int64_t g = (int64_t)num_sms * cached[slot];
   if (units < g) g = units;
@@ -188,6 +213,13 @@ cudaError_t launch_restore(const RestorePlan &plan, int grid, cudaStream_t strea
 cudaError_t launch_gather(const AccessParams &p, int num_sms, cudaStream_t stream) {
   const int64_t units = (int64_t)p.n * (p.conv_chunks + p.ssm_chunks);
   gather_kernel<<<grid_for((const void *)gather_kernel, num_sms, units), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_copy(const KvPlan &p, int num_sms, cudaStream_t stream) {
+  const int64_t units = (int64_t)p.n_ops * p.num_layers * 2 * p.chunks_per_op;
+  if (units == 0) return cudaSuccess;
+  kv_copy_kernel<<<grid_for((const void *)kv_copy_kernel, num_sms, units), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -118,4 +118,16 @@ struct PrefillConvParams {
 // returns LSC_OK, LSC_ERR_UNSUPPORTED or LSC_ERR_CUDA
 int launch_prefill_conv(const PrefillConvParams &p, cudaStream_t stream);
 
+// copy_prefix plan, passed by value (<= 32 KB of kernel parameters)
+constexpr int kKvPlanMaxOps = 2560;
+struct KvPlan {
+  uint8_t *base;
+  int64_t region_bytes;  // one attention layer: both lanes
+  int64_t lane_bytes;    // num_blocks pages
+  int64_t page, row_bytes, chunk_bytes;
+  int32_t num_layers, n_ops, chunks_per_op, pad;
+  int3 op[kKvPlanMaxOps];  // (src block, dst block, n_tokens > 0)
+};
+cudaError_t launch_kv_copy(const KvPlan &p, int num_sms, cudaStream_t stream);
+
 }  // namespace lsc

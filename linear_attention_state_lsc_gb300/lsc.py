@@ -1,5 +1,5 @@
-"""ctypes binding of liblsc (include/lsc.h, include/lsc_prefix_cache.h), same
-names as the C ABI.
+"""ctypes binding of liblsc (include/lsc.h, include/lsc_prefix_cache.h,
+include/lsc_kv.h), same names as the C ABI.
 
 Argument marshalling only: every step of the hot path runs in the CUDA kernels
 of liblsc.so.  Pointers are plain integers; torch tensors, numpy arrays and
@@ -111,6 +111,23 @@ class lsc_gdn_prefill_conv_args(C.Structure):
                 ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p)]
 
 
+class lsc_kv_pool_desc(C.Structure):
+    _fields_ = [("num_layers", C.c_int32), ("num_blocks", C.c_int32), ("block_tokens", C.c_int32),
+                ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("dtype", C.c_int32),
+                ("page_bytes", C.c_int64)]
+
+
+class lsc_kv_layer_view(C.Structure):
+    _fields_ = [("region", C.c_void_p), ("region_bytes", C.c_int64), ("k", C.c_void_p), ("v", C.c_void_p),
+                ("shape", C.c_int64 * 4), ("strides", C.c_int64 * 4), ("lane_stride", C.c_int64),
+                ("page_bytes", C.c_int64), ("payload_bytes", C.c_int64), ("row_bytes", C.c_int64),
+                ("dtype", C.c_int32), ("reserved", C.c_int32)]
+
+
+# numpy view of an array of lsc_kv_copy_op
+KV_OP_DTYPE = np.dtype([("src_block", "<i4"), ("dst_block", "<i4"), ("n_tokens", "<i4"), ("reserved", "<i4")])
+
+
 _lib = None
 
 
@@ -137,6 +154,11 @@ def load():
         "lsc_gdn_decode": ([P, I32, C.POINTER(lsc_gdn_decode_args), P], C.c_int),
         "lsc_gdn_recurrent": ([P, I32, C.POINTER(lsc_gdn_recurrent_args), P], C.c_int),
         "lsc_gdn_prefill_conv": ([P, I32, C.POINTER(lsc_gdn_prefill_conv_args), P], C.c_int),
+        "lsc_kv_pool_required_bytes": ([C.POINTER(lsc_kv_pool_desc), C.POINTER(C.c_size_t)], C.c_int),
+        "lsc_kv_pool_create": ([C.POINTER(lsc_kv_pool_desc), P, C.c_size_t, C.POINTER(P)], C.c_int),
+        "lsc_kv_pool_destroy": ([P], C.c_int),
+        "lsc_kv_pool_layer_view": ([P, I32, C.POINTER(lsc_kv_layer_view)], C.c_int),
+        "lsc_copy_prefix": ([P, P, I32, P, P, C.POINTER(I64)], C.c_int),
         "lsc_pc_create": ([I32, I32, C.POINTER(P)], C.c_int),
         "lsc_pc_destroy": ([P], C.c_int),
         "lsc_pc_allocate_live_slot": ([P, I64, C.POINTER(I32)], C.c_int),
@@ -404,3 +426,47 @@ def lsc_pc_counts(pc):
     c = [C.c_int32() for _ in range(4)]
     rc = load().lsc_pc_counts(pc, *[C.byref(x) for x in c])
     return rc, tuple(x.value for x in c)
+
+
+# ---- attention K/V block pool (include/lsc_kv.h) ------------------------------
+
+def lsc_kv_pool_required_bytes(desc):
+    n = C.c_size_t(0)
+    rc = load().lsc_kv_pool_required_bytes(C.byref(desc), C.byref(n))
+    if rc != LSC_OK:
+        raise LscError(rc, "lsc_kv_pool_required_bytes")
+    return n.value
+
+
+def lsc_kv_pool_create(desc, device_base=None, base_bytes=0):
+    """Returns (rc, pool handle)."""
+    h = C.c_void_p()
+    rc = load().lsc_kv_pool_create(C.byref(desc), ptr(device_base), base_bytes, C.byref(h))
+    return rc, h.value
+
+
+def lsc_kv_pool_destroy(pool):
+    return load().lsc_kv_pool_destroy(pool)
+
+
+def lsc_kv_pool_layer_view(pool, layer):
+    v = lsc_kv_layer_view()
+    rc = load().lsc_kv_pool_layer_view(pool, layer, C.byref(v))
+    return rc, v
+
+
+def kv_ops(src_blocks, dst_blocks, n_tokens):
+    ops = np.zeros(len(src_blocks), KV_OP_DTYPE)
+    ops["src_block"] = src_blocks
+    ops["dst_block"] = dst_blocks
+    ops["n_tokens"] = n_tokens
+    return ops
+
+
+def lsc_copy_prefix(pool, ops, stream=None, done_event=None):
+    """ops: a KV_OP_DTYPE array on the host.  Returns (rc, bytes_copied)."""
+    assert ops.dtype == KV_OP_DTYPE
+    ops = np.ascontiguousarray(ops)
+    b = C.c_int64(0)
+    rc = load().lsc_copy_prefix(pool, ops.ctypes.data, len(ops), _stream(stream), _event(done_event), C.byref(b))
+    return rc, b.value
