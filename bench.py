@@ -522,6 +522,39 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     L.lsc_pool_destroy(pool)
     del buf, xd, q, k, v
     torch.cuda.empty_cache()
+    # copy_prefix: 12 attention layers, 2048 blocks of 64 tokens x 2 kv heads x 256
+    # dims bf16 (64 KiB) in 64.5 KiB pages; 16 prefixes of 2016 tokens (31 full
+    # blocks + a half block) copied into other blocks
+    d = L.lsc_kv_pool_desc(12, 2048, 64, 2, 256, L.LSC_BF16, 65536 + 512)
+    kvn = L.lsc_kv_pool_required_bytes(d)
+    kbuf = torch.empty(kvn, dtype=torch.uint8, device="cuda")
+    kbuf.view(torch.int32).random_(generator=torch.Generator(device="cuda").manual_seed(0))
+    rc, kpool = L.lsc_kv_pool_create(d, kbuf, kvn)
+    assert rc == L.LSC_OK
+    perm = np.random.default_rng(7).permutation(2048)
+    ksrc, kdst, knt = [], [], []
+    for i in range(16):
+        ksrc += list(perm[64 * i:64 * i + 32])
+        kdst += list(perm[1024 + 64 * i:1024 + 64 * i + 32])
+        knt += [64] * 31 + [32]
+    kops = L.kv_ops(ksrc, kdst, knt)
+    nb = [0]
+
+    def copy_one():
+        rc, nb[0] = L.lsc_copy_prefix(kpool, kops, fwd)
+        assert rc == L.LSC_OK
+
+    t = timed(copy_one, 20)
+    kbytes = 2 * nb[0]  # read + write
+    parts["copy_prefix_kv"] = {"workload": "12 attention layers, 2048 blocks x 64 tokens x 2 kv heads x 256 dims bf16 "
+                                           "in 64.5 KiB pages; 16 prefixes of 2016 tokens (512 block ops)",
+                               "kernel": "kv_copy_kernel", "launch_ms": round(t * 1e3, 4),
+                               "bytes_per_launch": kbytes, "GB/s": round(kbytes / t / 1e9, 1),
+                               "frac": round(kbytes / t / 1e9 / hbm_peak, 4),
+                               "bytes_basis": "token rows copied: read + write"}
+    L.lsc_kv_pool_destroy(kpool)
+    del kbuf
+    torch.cuda.empty_cache()
     parts["prefix_cache_host"] = measure_prefix_cache(L)
     return parts
 
