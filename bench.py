@@ -748,6 +748,7 @@ NCU_CASES = {
     "restore": ("c1", 64, "restore"),        # 64 hits x 2 layers, 549 MB per launch
     "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer
     "prefill": ("c4", 32, "prefill"),        # prefill conv: 32 sequences of 64..2048 tokens, one layer
+    "copy_prefix": ("c1", 4, "copy_prefix"), # K/V copy: 12 layers x 512 blocks of 64 KiB, 4 prefixes of 32 blocks
 }
 
 
@@ -765,7 +766,18 @@ def run_ncu_case(args):
     buf, pool, views = make_pool(L, W, w, seed=0)
     fwd = torch.cuda.current_stream()
     rng = np.random.default_rng(0)
-    if kind == "restore":
+    if kind == "copy_prefix":
+        d = L.lsc_kv_pool_desc(12, 512, 64, 2, 256, L.LSC_BF16, 65536 + 512)
+        kvn = L.lsc_kv_pool_required_bytes(d)
+        kbuf = torch.zeros(kvn, dtype=torch.uint8, device="cuda")
+        rc, kpool = L.lsc_kv_pool_create(d, kbuf, kvn)
+        assert rc == L.LSC_OK
+        perm = rng.permutation(512)
+        kops = L.kv_ops(perm[:32 * n], perm[256:256 + 32 * n], [64] * (32 * n))
+
+        def launch(i):
+            assert L.lsc_copy_prefix(kpool, kops, fwd)[0] == L.LSC_OK
+    elif kind == "restore":
         rows = W.restore_rows("c1")
         ops = L.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
         hs = torch.from_numpy(rows.hs_prefill.copy()).cuda()
