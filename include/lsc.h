@@ -54,6 +54,10 @@ extern "C" {
 #define LSC_ERR_WRONG_DEVICE (-12)  /* the current device is not the pool's device */
 #define LSC_ERR_NO_SLOT (-13)       /* prefix cache: no free slot and no unpinned checkpoint to reclaim */
 #define LSC_ERR_ORDER (-14)         /* prefix cache: call out of step order (resolve/commit/release) */
+#define LSC_ERR_NO_SPACE (-15)      /* snapshot store: no room within the quota after make_room */
+#define LSC_ERR_CORRUPT (-16)       /* snapshot store: a damaged file (it and its entries were dropped) */
+#define LSC_ERR_NOT_FOUND (-17)     /* snapshot store: no such blob or entry */
+#define LSC_ERR_IO (-18)            /* snapshot store: a file operation failed */
 
 /* ---- enums -------------------------------------------------------------- */
 typedef enum { LSC_LAYER_ATTENTION = 0, LSC_LAYER_GDN = 1 } lsc_layer_kind;

@@ -185,6 +185,10 @@ const char *lsc_error_string(int code) {
     case LSC_ERR_WRONG_DEVICE: return "current device is not the pool's device";
     case LSC_ERR_NO_SLOT: return "no free slot and no unpinned checkpoint to reclaim";
     case LSC_ERR_ORDER: return "prefix cache call out of step order";
+    case LSC_ERR_NO_SPACE: return "snapshot store: no room within the quota";
+    case LSC_ERR_CORRUPT: return "snapshot store: damaged file dropped";
+    case LSC_ERR_NOT_FOUND: return "snapshot store: no such blob or entry";
+    case LSC_ERR_IO: return "snapshot store: file operation failed";
     default: return "unknown error";
   }
 }

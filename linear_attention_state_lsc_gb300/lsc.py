@@ -1,5 +1,5 @@
 """ctypes binding of liblsc (include/lsc.h, include/lsc_prefix_cache.h,
-include/lsc_kv.h), same names as the C ABI.
+include/lsc_kv.h, include/lsc_store.h), same names as the C ABI.
 
 Argument marshalling only: every step of the hot path runs in the CUDA kernels
 of liblsc.so.  Pointers are plain integers; torch tensors, numpy arrays and
@@ -31,6 +31,10 @@ LSC_ERR_LAYOUT = -11
 LSC_ERR_WRONG_DEVICE = -12
 LSC_ERR_NO_SLOT = -13
 LSC_ERR_ORDER = -14
+LSC_ERR_NO_SPACE = -15
+LSC_ERR_CORRUPT = -16
+LSC_ERR_NOT_FOUND = -17
+LSC_ERR_IO = -18
 
 # prefix-cache slot states (include/lsc_prefix_cache.h)
 LSC_SLOT_FREE, LSC_SLOT_LIVE, LSC_SLOT_CHECKPOINT, LSC_SLOT_RESERVED = 0, 1, 2, 3
@@ -470,3 +474,104 @@ def lsc_copy_prefix(pool, ops, stream=None, done_event=None):
     b = C.c_int64(0)
     rc = load().lsc_copy_prefix(pool, ops.ctypes.data, len(ops), _stream(stream), _event(done_event), C.byref(b))
     return rc, b.value
+
+
+# ---- snapshot store (include/lsc_store.h) -------------------------------------
+
+class lsc_store_stats(C.Structure):
+    _fields_ = [("used_bytes", C.c_int64), ("quota_bytes", C.c_int64), ("n_blobs", C.c_int32),
+                ("n_entries", C.c_int32), ("n_unreferenced", C.c_int32), ("n_pinned", C.c_int32)]
+
+
+_STORE_SIG = {
+    "lsc_store_open": ([C.c_char_p, C.c_uint64, C.c_int64, C.POINTER(C.c_void_p)], C.c_int),
+    "lsc_store_close": ([C.c_void_p], C.c_int),
+    "lsc_store_put_blob": ([C.c_void_p, C.c_uint64, C.c_int32, C.c_void_p, C.c_int64], C.c_int),
+    "lsc_store_get_blob": ([C.c_void_p, C.c_uint64, C.c_void_p, C.c_int64, C.POINTER(C.c_int64),
+                            C.POINTER(C.c_int32)], C.c_int),
+    "lsc_store_blob_size": ([C.c_void_p, C.c_uint64, C.POINTER(C.c_int64)], C.c_int),
+    "lsc_store_put_entry": ([C.c_void_p, C.c_uint64, C.c_void_p, C.c_int32], C.c_int),
+    "lsc_store_get_entry": ([C.c_void_p, C.c_uint64, C.c_void_p, C.c_int32, C.POINTER(C.c_int32)], C.c_int),
+    "lsc_store_drop_entry": ([C.c_void_p, C.c_uint64], C.c_int),
+    "lsc_store_pin": ([C.c_void_p, C.c_uint64], C.c_int),
+    "lsc_store_unpin": ([C.c_void_p, C.c_uint64], C.c_int),
+    "lsc_store_stats_get": ([C.c_void_p, C.POINTER(lsc_store_stats)], C.c_int),
+    "lsc_store_save_state": ([C.c_void_p, C.c_uint64, C.c_void_p, C.c_int32, C.c_void_p], C.c_int),
+    "lsc_store_load_state": ([C.c_void_p, C.c_uint64, C.c_void_p, C.c_int32, C.c_void_p], C.c_int),
+}
+
+
+def _store_fn(name):
+    lib = load()
+    f = getattr(lib, name)
+    if name in _STORE_SIG and f.argtypes is None:
+        f.argtypes, f.restype = _STORE_SIG[name]
+    return f
+
+
+def lsc_store_open(directory, namespace_digest, quota_bytes):
+    """Returns (rc, store handle)."""
+    h = C.c_void_p()
+    rc = _store_fn("lsc_store_open")(os.fsencode(directory), namespace_digest, quota_bytes, C.byref(h))
+    return rc, h.value
+
+
+def lsc_store_close(store):
+    return _store_fn("lsc_store_close")(store)
+
+
+def lsc_store_put_blob(store, key, kind, data):
+    """data: a bytes-like object or numpy array (host)."""
+    a = np.frombuffer(bytes(data), np.uint8) if not isinstance(data, np.ndarray) else np.ascontiguousarray(data)
+    return _store_fn("lsc_store_put_blob")(store, key, kind, a.ctypes.data if a.size else None, a.nbytes)
+
+
+def lsc_store_get_blob(store, key):
+    """Returns (rc, kind, payload bytes or None)."""
+    n = C.c_int64(0)
+    rc = _store_fn("lsc_store_blob_size")(store, key, C.byref(n))
+    if rc != LSC_OK:
+        return rc, None, None
+    buf = np.zeros(max(n.value, 1), np.uint8)
+    kind = C.c_int32(-1)
+    rc = _store_fn("lsc_store_get_blob")(store, key, buf.ctypes.data, buf.nbytes, C.byref(n), C.byref(kind))
+    return rc, kind.value, (bytes(buf[:n.value]) if rc == LSC_OK else None)
+
+
+def lsc_store_put_entry(store, key, blob_keys):
+    a = np.ascontiguousarray(blob_keys, dtype=np.uint64)
+    return _store_fn("lsc_store_put_entry")(store, key, a.ctypes.data if a.size else None, len(a))
+
+
+def lsc_store_get_entry(store, key):
+    """Returns (rc, list of blob keys)."""
+    n = C.c_int32(0)
+    buf = np.zeros(4096, np.uint64)
+    rc = _store_fn("lsc_store_get_entry")(store, key, buf.ctypes.data, len(buf), C.byref(n))
+    return rc, [int(x) for x in buf[:n.value]] if rc == LSC_OK else []
+
+
+def lsc_store_drop_entry(store, key):
+    return _store_fn("lsc_store_drop_entry")(store, key)
+
+
+def lsc_store_pin(store, key):
+    return _store_fn("lsc_store_pin")(store, key)
+
+
+def lsc_store_unpin(store, key):
+    return _store_fn("lsc_store_unpin")(store, key)
+
+
+def lsc_store_stats_get(store):
+    st = lsc_store_stats()
+    rc = _store_fn("lsc_store_stats_get")(store, C.byref(st))
+    return rc, st
+
+
+def lsc_store_save_state(store, key, pool, slot, stream=None):
+    return _store_fn("lsc_store_save_state")(store, key, pool, slot, _stream(stream))
+
+
+def lsc_store_load_state(store, key, pool, slot, stream=None):
+    return _store_fn("lsc_store_load_state")(store, key, pool, slot, _stream(stream))

@@ -26,7 +26,9 @@ key, payload bytes (40 bytes), 20 reserved zero bytes, then the CRC-32C of
 those 60 bytes; then the payload, then the payload CRC, all little-endian); "blocks" are the stored blobs
 (K/V blocks and state snapshots alike) and an entry references blobs; a blob
 written with no entry referencing it is unreferenced until an entry takes it;
-"recently used" advances on put_entry, pin and unpin; make_room runs before a
+"recently used" advances on put_entry, pin and unpin; a blob key is written
+once (a second put of the same key is refused); reopening a store clears pins
+and orders entries by key; make_room runs before a
 blob is written and counts file sizes (header + payload + CRC).
 """
 import struct
@@ -131,19 +133,14 @@ class Store:
         return True
 
     def put_blob(self, key, kind, payload):
-        if key == 0:
-            raise StoreError("key 0", "arg")
-        old = self.blobs.get(key, 0)
+        if key == 0 or kind == 255 or key in self.blobs:
+            raise StoreError("bad blob", "arg")
         size = HEADER + len(payload) + 4
-        if key in self.blobs:   # rewriting a blob replaces it in place
-            self.blobs[key] = 0
         if not self.make_room(size):
-            if key in self.blobs:
-                self.blobs[key] = old
             raise StoreError("no room", "no_space")
         self.files[key] = file_bytes(kind, self.namespace, key, payload)
         self.blobs[key] = size
-        self.refs.setdefault(key, 0)
+        self.refs[key] = 0
 
     def get_blob(self, key):
         if key not in self.blobs:
@@ -180,7 +177,17 @@ class Store:
         self._touch(key)
 
     def unpin(self, key):
-        if key not in self.entries or self.pins[key] == 0:
+        if key not in self.entries:
+            raise StoreError("missing", "missing")
+        if self.pins[key] == 0:
             raise StoreError("not pinned", "arg")
         self.pins[key] -= 1
         self._touch(key)
+
+    def reopen(self):
+        """The index as a reopened store rebuilds it from the files: pins
+        cleared, entries' recency in ascending key order."""
+        self.pins = {e: 0 for e in self.entries}
+        self.clock = 0
+        for e in sorted(self.entries):
+            self._touch(e)

@@ -50,7 +50,7 @@ def test_struct_layouts(lsc):
 
 
 def test_error_strings(lsc):
-    for code in range(-14, 2):
+    for code in range(-18, 2):
         s = L.lsc_error_string(code)
         assert s and s != "unknown error", code
     assert L.lsc_error_string(-99) == "unknown error"
