@@ -556,7 +556,46 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     del kbuf
     torch.cuda.empty_cache()
     parts["prefix_cache_host"] = measure_prefix_cache(L)
+    parts["snapshot_store_c1"] = measure_store(L, W, torch)
     return parts
+
+
+def measure_store(L, W, torch, n_slots=8):
+    """Save and load a c1 slot's linear state (36 GDN layers: conv + ssm views,
+    77.3 MB) through the snapshot store in a scratch directory of the host:
+    device -> pinned host -> CRC-32C -> temporary file -> rename, and back."""
+    import shutil
+    import tempfile
+    w = W.get("c1")
+    w.num_slots = n_slots
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    d = tempfile.mkdtemp(prefix="lsc_store_")
+    try:
+        rc, st = L.lsc_store_open(d, 0xC1, 1 << 40)
+        assert rc == L.LSC_OK
+        v0 = views[w.gdn_layers[0]]
+        per = len(w.gdn_layers) * (v0.conv_bytes + v0.ssm_bytes)
+        fwd = torch.cuda.current_stream()
+        t0 = time.perf_counter()
+        for i in range(n_slots):
+            assert L.lsc_store_save_state(st, 100 + i, pool, i, fwd) == L.LSC_OK
+        t_save = (time.perf_counter() - t0) / n_slots
+        t0 = time.perf_counter()
+        for i in range(n_slots):
+            assert L.lsc_store_load_state(st, 100 + i, pool, n_slots - 1 - i, fwd) == L.LSC_OK
+        t_load = (time.perf_counter() - t0) / n_slots
+        L.lsc_store_close(st)
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+        L.lsc_pool_destroy(pool)
+        del buf
+        torch.cuda.empty_cache()
+    return {"workload": f"c1 slot snapshot: 36 GDN layers, {per} bytes of conv + ssm views per slot, "
+                        f"{n_slots} slots saved then loaded, host scratch directory",
+            "bytes_per_slot": per, "save_ms": round(t_save * 1e3, 2), "load_ms": round(t_load * 1e3, 2),
+            "save_GB/s": round(per / t_save / 1e9, 2), "load_GB/s": round(per / t_load / 1e9, 2),
+            "clock": "host wall clock; includes D2H / H2D, CRC-32C, file write + fsync + rename / read",
+            "bound": "host I/O and CRC (no HBM roofline)"}
 
 
 def prefix_cache_schedule(steps, num_slots=1024, block=64, batch=256, churn=4, seed=0):
