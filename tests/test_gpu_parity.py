@@ -281,6 +281,25 @@ def test_decode_matches_oracle(lsc, name, kw):
         assert P.status() == L.LSC_OK
 
 
+@pytest.mark.big
+def test_decode_more_items_than_one_launch_holds(lsc):
+    """A CTA holds at most 512 work items per launch, so more than 512 x SMs /
+    Hk rows are split over several launches; the result is the same."""
+    w0 = W.small("s1")   # Hk = 2: the split happens below the 65535-row limit
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = 512 * sms // w0.num_k_heads + 123
+    assert n <= 65535
+    w = workload("s1", num_slots=n + 7, layers=[W.GDN])
+    with DevPool(w, seed=17) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, x, cw, a, b = decode_case(w, seed=19, n=n)
+        rc, out = run_decode(P, l, w, idx, has, x, cw, a, b)
+        assert rc == L.LSC_OK
+        check_decode(w, P, l, pre, idx, has, x, cw, a, b, out)
+        assert P.status() == L.LSC_OK
+
+
 def test_decode_two_steps_all_warm(lsc):
     """Two consecutive tokens on the same slots (the second reads what the first
     wrote), has_init NULL."""
