@@ -371,8 +371,11 @@ def test_decode_rejects(lsc):
         assert L.lsc_gdn_decode(P.pool, 0, args) == L.LSC_OK
     w = workload("c0", head_k_dim=24, conv_dim=2 * 24 + 2 * 16, ssm_dtype=W.F32)
     with DevPool(w) as P:
-        args = L.decode_args(2, 1, 1, 1, 1, 1, 1, 1, 1)
+        # aligned stand-in addresses (never dereferenced: the shape is refused first)
+        args = L.decode_args(2, 1, 256, 256, 256, 256, 256, 256, 256)
         assert L.lsc_gdn_decode(P.pool, 0, args) == L.LSC_ERR_UNSUPPORTED
+        args = L.decode_args(2, 1, 1, 1, 1, 1, 1, 1, 1)
+        assert L.lsc_gdn_decode(P.pool, 0, args) == L.LSC_ERR_MISALIGNED
 
 
 # ---------------------------------------------------------------- recurrence
