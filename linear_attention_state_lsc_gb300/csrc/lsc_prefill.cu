@@ -27,6 +27,8 @@
 //       per thread, then q and k normalised in a second pass.
 //   prefill_state_kernel  the new conv state of each sequence (after the
 //       outputs, so no tile reads a state another tile has already replaced).
+#include <type_traits>
+
 #include "lsc_gdn_common.cuh"
 
 namespace lsc {
@@ -120,9 +122,59 @@ __device__ __forceinline__ bool seq_ok(const PrefillConvParams &p, int s, int t,
 }
 
 // ------------------------------------------------------------------ fast path
+// 2^x and 1/x on the special-function unit (PTX ex2.approx / rcp.approx with
+// flush to zero; a few ulp of relative error each).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// SiLU of a float pair: z * sigmoid(z) with sigmoid(z) = 1 / (1 + 2^(-z log2 e)).
+// Large negative z gives 2^(+inf) = inf, 1/inf = 0 and SiLU -0.
+__device__ __forceinline__ uint64_t silu2(uint64_t z) {
+  const uint64_t neg_log2e = f2_pack(-1.44269504088896341f, -1.44269504088896341f);
+  const uint64_t one = f2_pack(1.f, 1.f);
+  float a, b;
+  f2_unpack(f2_mul(z, neg_log2e), a, b);
+  f2_unpack(f2_add(f2_pack(ex2_approx(a), ex2_approx(b)), one), a, b);
+  return f2_mul(z, f2_pack(rcp_approx(a), rcp_approx(b)));
+}
+
+// Eight consecutive conv-dtype values at a 16-byte-aligned global address, as
+// four float pairs (channel 2i low, 2i + 1 high).
+template <typename TC>
+__device__ __forceinline__ void load_pairs8(const void *p, uint64_t *f) {
+  const uint4 *q = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+  for (int h = 0; h < 8 * (int)sizeof(TC) / 16; ++h) StatePairs<TC>::unpack(__ldg(q + h), f + h * StatePairs<TC>::N);
+}
+
+template <int R>
+using Rot = std::integral_constant<int, R>;
+
+// Calls tok(Rot<R>{}) for R = R0 .. H-1, one token each, advancing t; false
+// once t reaches end.
+template <int R, int H, typename F>
+__device__ __forceinline__ bool tokens_rotated(F &tok, int &t, int end) {
+  if constexpr (R == H) {
+    return true;
+  } else {
+    tok(Rot<R>{});
+    if (++t >= end) return false;
+    return tokens_rotated<R + 1, H>(tok, t, end);
+  }
+}
+
 template <typename TC, int CW>
-__global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const __grid_constant__ PrefillConvParams p) {
+__global__ void __launch_bounds__(kPrefillThreads, CW ? 3 : 1) prefill_conv_vec_kernel(const __grid_constant__ PrefillConvParams p) {
   constexpr int WW = CW ? CW : kMaxTaps;  // register window, W <= WW
+  constexpr int H = WW - 1;               // window inputs before the current token
   constexpr int esc = (int)sizeof(TC);
   const int W = CW ? CW : p.conv_width;
   const int C = p.conv_dim;
@@ -130,31 +182,51 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const
   const bool live = grp < C / 8;
   const int c0 = live ? grp * 8 : 0;
   const int lanes_per_head = p.dk / 8;  // a power of two <= 32
-  const bool is_qk = c0 < 2 * p.Hk * p.dk;
+  const int qk = p.Hk * p.dk;
+  const bool is_qk = live && c0 < 2 * qk;
   const int t_begin = blockIdx.y * kPrefillTile;
   const int t_end = min(t_begin + kPrefillTile, p.total_tokens);
   if (t_begin >= t_end) return;  // uniform over the CTA
+  // does any lane of the warp carry q or k channels (the norm's shuffles then
+  // run on the whole warp)
+  const bool warp_qk = __any_sync(0xffffffffu, is_qk);
 
   __shared__ int s_first;
   if (threadIdx.x == 0) s_first = seq_of(p.cu, p.n_seq, t_begin);
   __syncthreads();
 
-  // weights of the group's 8 channels
-  float wt[8][WW];
+  // where the group's outputs go: q [T, Hk dk], k [T, Hk dk] or v [T, Hv dv]
+  float *obase;
+  int64_t orow;
+  if (c0 < qk) {
+    obase = p.q + c0;
+    orow = qk;
+  } else if (c0 < 2 * qk) {
+    obase = p.k + (c0 - qk);
+    orow = qk;
+  } else {
+    obase = p.v + (c0 - 2 * qk);
+    orow = (int64_t)p.Hv * p.dv;
+  }
+
+  // weights of the group's 8 channels as pairs: w2[i][j] = tap j of channels 2i, 2i + 1
+  uint64_t w2[4][WW];
   {
     F8 buf[WW];  // the 8 W weights of the group, row-major [8][W]
     const uint8_t *wp = reinterpret_cast<const uint8_t *>(p.w) + (int64_t)c0 * W * esc;
 #pragma unroll
     for (int v = 0; v < WW; ++v) buf[v] = v < W ? Vec8<TC>::load(wp + v * 8 * esc) : F8{};
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < WW; ++j) {
-        float wv = 0.f;
+        float wv[2] = {0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 8 * WW; ++e)
-          if (e == cc * W + j && j < W) wv = buf[e / 8].v[e % 8];
-        wt[cc][j] = wv;
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 8 * WW; ++e)
+            if (e == (2 * i + h) * W + j && j < W) wv[h] = buf[e / 8].v[e % 8];
+        w2[i][j] = f2_pack(wv[0], wv[1]);
       }
   }
   const uint8_t *xg = reinterpret_cast<const uint8_t *>(p.x) + (int64_t)c0 * esc;
@@ -163,7 +235,10 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const
   constexpr int NH = 8 * esc / 16;  // 16-byte pieces of one x row of the group
   constexpr int A = kPrefillRingBytes / (8 * esc);  // ring slots: 8 rows (bf16) or 4 (f32)
   __shared__ __align__(16) uint4 ring[A][NH][kPrefillThreads];
-  F8 hist[WW - 1];  // window inputs before the current token, oldest first
+  // hist[(j + R) % H] is window input j (0 = oldest) of a token processed at
+  // rotation R: a new token's x overwrites the oldest input in place.  With a
+  // run-time width (CW = 0) the rotation stays 0 and the inputs shift instead.
+  uint64_t hist[H][4];
   int s = s_first;
   // The tile is walked in segments, one per sequence piece: the window is
   // rebuilt at a segment's first token, then slides token by token.
@@ -179,33 +254,35 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const
     }
     const bool warm = slot >= 0 && (p.has_init == nullptr || p.has_init[s] != 0);
     {
-      F8 st[WW - 1];  // the group's conv state, row-major [8][W - 1]
+      F8 st[H];  // the group's conv state, row-major [8][W - 1]
 #pragma unroll
-      for (int v = 0; v < WW - 1; ++v) st[v] = F8{};
+      for (int v = 0; v < H; ++v) st[v] = F8{};
       if (warm && live && t - ts < W - 1) {
         const uint8_t *sp = p.layer + (int64_t)slot * p.page + (int64_t)c0 * (W - 1) * esc;
 #pragma unroll
-        for (int v = 0; v < WW - 1; ++v)
+        for (int v = 0; v < H; ++v)
           if (v < W - 1) st[v] = Vec8<TC>::load(sp + v * 8 * esc);
       }
-      // hist[j] is token t - (W - 1 - j); before the sequence it is state
-      // entry (t - ts) + j (entries are picked with compile-time indices)
+      // window input j is token t - (W - 1 - j); before the sequence it is
+      // state entry (t - ts) + j (entries are picked with compile-time indices)
 #pragma unroll
-      for (int j = 0; j < WW - 1; ++j) {
+      for (int j = 0; j < H; ++j) {
         if (j >= W - 1) continue;
         const int back = W - 1 - j;
         if (t - back >= ts) {
-          hist[j] = Vec8<TC>::load(xg + (int64_t)(t - back) * xrow);
+          load_pairs8<TC>(xg + (int64_t)(t - back) * xrow, hist[j]);
         } else {
           const int e = (t - ts) + j;
+          float val[8];
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
-            float val = 0.f;
+            val[cc] = 0.f;
 #pragma unroll
-            for (int ee = 0; ee < 8 * (WW - 1); ++ee)
-              if (ee == cc * (W - 1) + e) val = st[ee / 8].v[ee % 8];
-            hist[j].v[cc] = val;
+            for (int ee = 0; ee < 8 * H; ++ee)
+              if (ee == cc * (W - 1) + e) val[cc] = st[ee / 8].v[ee % 8];
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) hist[j][i] = f2_pack(val[2 * i], val[2 * i + 1]);
         }
       }
     }
@@ -221,7 +298,8 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const
           cp_async16(&ring[u][h][threadIdx.x], xg + (int64_t)(seg_t0 + u) * xrow + h * 16);
       cp_async_commit();
     }
-    for (; t < seg_end; ++t) {
+    auto token = [&](auto rot) {
+      constexpr int R = decltype(rot)::value;
       const int u = t - seg_t0;
       if (t + A - 1 < seg_end)
 #pragma unroll
@@ -229,42 +307,70 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_vec_kernel(const
           cp_async16(&ring[(u + A - 1) % A][h][threadIdx.x], xg + (int64_t)(t + A - 1) * xrow + h * 16);
       cp_async_commit();
       cp_async_wait<A - 1>();
-      F8 xc;
-      uint4 raw[NH];
+      uint64_t xc[4];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) raw[h] = ring[u % A][h][threadIdx.x];
-      Smem8<TC>::unpack(raw, xc.v);
-      float y[8];
-      float ss = 0.f;
+      for (int h = 0; h < NH; ++h) StatePairs<TC>::unpack(ring[u % A][h][threadIdx.x], xc + h * StatePairs<TC>::N);
+      uint64_t y[4];
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        float z = 0.f;
+      for (int i = 0; i < 4; ++i) {
+        uint64_t z = f2_mul(w2[i][0], hist[R % H][i]);  // W >= 2: tap 0 is a window input
 #pragma unroll
-        for (int j = 0; j < WW; ++j) {
-          if (j < W - 1) z = fmaf(wt[cc][j], hist[j].v[cc], z);
-          else if (j == W - 1) z = fmaf(wt[cc][j], xc.v[cc], z);
+        for (int j = 1; j < WW; ++j) {
+          if (j < W - 1) z = f2_fma(w2[i][j], hist[(j + R) % H][i], z);
+          else if (j == W - 1) z = f2_fma(w2[i][j], xc[i], z);
         }
-        y[cc] = silu(z);
-        ss = fmaf(y[cc], y[cc], ss);
+        y[i] = silu2(z);
       }
-      // slide the window: drop the oldest input, append this token's x
+      // slide the window: this token's x replaces the oldest input
+      if constexpr (CW != 0) {
 #pragma unroll
-      for (int j = 0; j < WW - 1; ++j) {
-        if (j < W - 2) hist[j] = hist[j + 1 < WW - 1 ? j + 1 : j];
-        else if (j == W - 2) hist[j] = xc;
+        for (int i = 0; i < 4; ++i) hist[R % H][i] = xc[i];
+      } else {
+#pragma unroll
+        for (int j = 0; j < H - 1; ++j)
+          if (j < W - 2)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hist[j][i] = hist[j + 1][i];
+#pragma unroll
+        for (int j = 0; j < H; ++j)
+          if (j == W - 2)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hist[j][i] = xc[i];
       }
-      // sum of squares of the head: its dk/8 lanes are consecutive and aligned
-      for (int m = 1; m < lanes_per_head; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      // q and k: divide by the head's sqrt(sum of squares + 1e-6); the head's
+      // dk/8 lanes are consecutive and aligned, reduced with shuffles
+      float scale = 1.f;
+      if (warp_qk) {
+        uint64_t s2 = f2_mul(y[0], y[0]);
+#pragma unroll
+        for (int i = 1; i < 4; ++i) s2 = f2_fma(y[i], y[i], s2);
+        float a, b;
+        f2_unpack(s2, a, b);
+        float ss = a + b;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1)
+          if (m < lanes_per_head) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        if (is_qk) scale = rsqrtf(ss + 1e-6f);
+      }
       if (live) {
-        const float scale = is_qk ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
-        float4 *o = reinterpret_cast<float4 *>(out_ptr(p, t, c0));
+        float4 *o = reinterpret_cast<float4 *>(obase + (int64_t)t * orow);
         if (slot >= 0) {
-          o[0] = make_float4(y[0] * scale, y[1] * scale, y[2] * scale, y[3] * scale);
-          o[1] = make_float4(y[4] * scale, y[5] * scale, y[6] * scale, y[7] * scale);
+          const uint64_t sc = f2_pack(scale, scale);
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) f2_unpack(warp_qk ? f2_mul(y[i], sc) : y[i], f[2 * i], f[2 * i + 1]);
+          o[0] = make_float4(f[0], f[1], f[2], f[3]);
+          o[1] = make_float4(f[4], f[5], f[6], f[7]);
         } else {
           o[0] = o[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
+    };
+    if constexpr (CW != 0) {
+      while (t < seg_end && tokens_rotated<0, H>(token, t, seg_end)) {
+      }
+    } else {
+      for (; t < seg_end; ++t) token(Rot<0>{});
     }
   }
   cp_async_wait<0>();
