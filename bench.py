@@ -466,25 +466,31 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     has = torch.from_numpy((rng.random(64) < 0.5).astype(np.uint8)).cuda()
     dev = [torch.from_numpy(z).cuda() for z in (cu, q, k, vv, a, b)]
     out = torch.empty((T, w.num_v_heads, w.head_v_dim), device="cuda")
-    ra = L.recurrent_args(64, w.num_k_heads, T, idx, has, *dev, out)
-
-    def rec_all():
+    def rec_all(ra):
         for l in w.gdn_layers:
             assert L.lsc_gdn_recurrent(pool, l, ra, fwd) == L.LSC_OK
 
-    t = timed(rec_all, 2)
     nl = len(w.gdn_layers)
     flops = 6.0 * T * w.num_v_heads * w.head_v_dim * w.head_k_dim * nl
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     fp32_peak = sms * 128 * 2 * 2070e6
+    rec = {}
+    for algo in (L.LSC_RECURRENT_TOKEN, L.LSC_RECURRENT_CHUNKED):
+        ra = L.recurrent_args(64, w.num_k_heads, T, idx, has, *dev, out, algorithm=algo)
+        rec[algo] = timed(lambda: rec_all(ra), 2)
+    t, t_ch = rec[L.LSC_RECURRENT_TOKEN], rec[L.LSC_RECURRENT_CHUNKED]
     parts["recurrent_c4"] = {"workload": f"c4: 64 sequences, {T} tokens, 36 layers, state [32,128,128] f32",
-                             "kernel": "recurrent_kernel<128,f32>", "ms_per_36_layers": round(t * 1e3, 3),
+                             "kernel": "recurrent128_kernel<f32> (token by token, the default)",
+                             "ms_per_36_layers": round(t * 1e3, 3),
                              "token_layers_per_s": round(T * nl / t, 1),
                              "TFLOP/s": round(flops / t / 1e12, 2),
                              "roofline": {"bound": "alu", "peak_TFLOP/s": round(fp32_peak / 1e12, 1),
                                           "frac": round(flops / t / fp32_peak, 4),
                                           "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 flop x 2070 MHz"},
-                             "flops_basis": "6 dk dv per (token, head): S k, the rank-1 update, S q"}
+                             "flops_basis": "6 dk dv per (token, head): S k, the rank-1 update, S q",
+                             "chunked": {"kernel": "recurrent_chunked_kernel<f32> (16-token chunks)",
+                                         "ms_per_36_layers": round(t_ch * 1e3, 3),
+                                         "frac": round(flops / t_ch / fp32_peak, 4)}}
     L.lsc_pool_destroy(pool)
     del buf, out, dev
     torch.cuda.empty_cache()
@@ -785,7 +791,8 @@ NCU_CASES = {
     "decode_f32": ("c1", 64, "decode"),      # serving-step decode: fp32 state, 64 rows, 277 MB per launch
     "decode_bf16": ("c2", 256, "decode"),    # bf16 state, 256 rows, 571 MB per launch
     "restore": ("c1", 64, "restore"),        # 64 hits x 2 layers, 549 MB per launch
-    "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer
+    "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer (token by token)
+    "recurrent_chunked": ("c4", 16, "recurrent_chunked"),  # the same, 16-token chunks
     "prefill": ("c4", 32, "prefill"),        # prefill conv: 32 sequences of 64..2048 tokens, one layer
     "copy_prefix": ("c1", 4, "copy_prefix"), # K/V copy: 12 layers x 512 blocks of 64 KiB, 4 prefixes of 32 blocks
 }
@@ -858,7 +865,8 @@ def run_ncu_case(args):
         has = torch.ones(n, dtype=torch.uint8, device="cuda")
         dev = [torch.from_numpy(z).cuda() for z in (cu, q, k, vv, a, b)]
         out = torch.empty((T, w.num_v_heads, w.head_v_dim), device="cuda")
-        ra = L.recurrent_args(n, w.num_k_heads, T, idx, has, *dev, out)
+        algo = L.LSC_RECURRENT_CHUNKED if kind == "recurrent_chunked" else L.LSC_RECURRENT_TOKEN
+        ra = L.recurrent_args(n, w.num_k_heads, T, idx, has, *dev, out, algorithm=algo)
 
         def launch(i):
             assert L.lsc_gdn_recurrent(pool, w.gdn_layers[i % 2], ra, fwd) == L.LSC_OK

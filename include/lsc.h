@@ -276,7 +276,7 @@ typedef struct {
   int32_t n_seq;
   int32_t num_k_heads;
   int32_t total_tokens;      /* == cu_seqlens[n_seq] (host copy, sizes the launch) */
-  int32_t reserved;
+  int32_t algorithm;         /* LSC_RECURRENT_AUTO (0), _TOKEN or _CHUNKED */
   const int32_t *idx;        /* device [n_seq]: live slot, < 0 = padding sequence */
   const uint8_t *has_init;   /* device [n_seq] or NULL (all warm) */
   const int32_t *cu_seqlens; /* device [n_seq + 1], cu_seqlens[0] == 0, non-decreasing */
@@ -288,17 +288,25 @@ typedef struct {
   float *out;                /* device [T, Hv, dv] */
 } lsc_gdn_recurrent_args;
 
+/* Evaluation order of lsc_gdn_recurrent (both give the token recurrence's
+ * result up to fp32 rounding). */
+#define LSC_RECURRENT_AUTO 0    /* the library's choice (currently TOKEN, the faster one) */
+#define LSC_RECURRENT_TOKEN 1   /* one token at a time */
+#define LSC_RECURRENT_CHUNKED 2 /* 16 tokens at a time: the token recurrence rearranged into
+                                   per-chunk products (head_k_dim 128 only) */
+
 /*
- * Token-by-token gated delta rule of a resumed prefill ([KP] "相同前缀不一定能
- * 全部复用": continue from the restored checkpoint), for GDN layer `layer`:
- * sequence i runs its tokens in order from slot idx[i]'s ssm state (zero when
+ * Gated delta rule of a resumed prefill ([KP] "相同前缀不一定能全部复用":
+ * continue from the restored checkpoint), for GDN layer `layer`: sequence i
+ * runs its tokens in order from slot idx[i]'s ssm state (zero when
  * has_init[i] == 0), writes out[t] = S_t q_t for each token, and writes its
  * final state back to the slot.  No conv stage; the conv state is untouched.
  * idx[i] < 0: zero outputs, no state touched.  A sequence whose cu_seqlens
  * entries fall outside [0, total_tokens] or decrease is skipped and
  * LSC_ERR_INVALID_ARG is recorded in the status word.  q and k must be 16-byte
- * aligned (MISALIGNED).  Supported: head_k_dim in {16, 32, 64, 128},
- * head_v_dim <= 128, ssm dtype f32 or bf16.
+ * aligned (MISALIGNED).  algorithm selects the evaluation order (any other
+ * value: INVALID_ARG).  Supported: head_k_dim in {16, 32, 64, 128} (CHUNKED:
+ * 128 only), head_v_dim <= 128, ssm dtype f32 or bf16; else UNSUPPORTED.
  */
 int lsc_gdn_recurrent(lsc_pool *pool, int32_t layer, const lsc_gdn_recurrent_args *args,
                       void *stream);

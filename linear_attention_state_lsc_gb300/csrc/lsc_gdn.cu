@@ -20,9 +20,11 @@ int launch_decode_bf16(const DecodeParams &p, int dk, cudaStream_t s);
 namespace {
 
 // ---------------------------------------------------------------------------
-// Token-by-token recurrence.  Grid (Hv, n_seq), one CTA per (sequence, v head),
-// 2 CTAs per SM.  Each thread keeps two rows of the head's state (CPT columns
-// of each, TPR threads per row) in registers for the whole sequence.
+// Token-by-token recurrence for head_k_dim 16, 32 and 64 (128 has its own
+// kernel with eight rows per thread, lsc_rec128.cu).  Grid (Hv, n_seq), one
+// CTA per (sequence, v head), 2 CTAs per SM.  Each thread keeps two rows of
+// the head's state (CPT columns of each, TPR threads per row) in registers for
+// the whole sequence.
 //
 // The state is held scaled, S = gamma * Shat, so that a token costs three
 // FMAs per element: Shat.k and Shat.q for the row's prediction and read-out,
@@ -37,7 +39,6 @@ namespace {
 // last.
 constexpr int kTileTokens = 32;
 constexpr int kRecThreads = 256;
-constexpr int kRankedSeqs = 256;
 
 template <int DK>
 struct RecShape {
@@ -70,20 +71,7 @@ __global__ void __launch_bounds__(kRecThreads, 2) recurrent_kernel(const __grid_
   auto b_s = [&](int b) { return a_s(b) + TT; };
   auto kq_s = [&](int b) { return a_s(b) + 2 * TT; };
 
-  // which sequence: longest first when the sequences are few enough to rank
-  int i = blockIdx.y;
-  if (p.n_seq <= kRankedSeqs) {
-    for (int s = tid; s < p.n_seq; s += kRecThreads) s_len[s] = p.cu[s + 1] - p.cu[s];
-    __syncthreads();
-    for (int s = tid; s < p.n_seq; s += kRecThreads) {
-      const int ls = s_len[s];
-      int rank = 0;
-      for (int jj = 0; jj < p.n_seq; ++jj) rank += (s_len[jj] > ls) || (s_len[jj] == ls && jj < s);
-      if (rank == (int)blockIdx.y) s_seq = s;
-    }
-    __syncthreads();
-    i = s_seq;
-  }
+  const int i = ranked_sequence(p.cu, p.n_seq, s_len, &s_seq);
 
   const int32_t slot = p.idx[i];
   const bool bad = slot >= p.num_slots;
@@ -308,7 +296,7 @@ int launch_recurrent(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream
     case 16: return bf ? launch_recurrent_t<16, __nv_bfloat16>(p, s) : launch_recurrent_t<16, float>(p, s);
     case 32: return bf ? launch_recurrent_t<32, __nv_bfloat16>(p, s) : launch_recurrent_t<32, float>(p, s);
     case 64: return bf ? launch_recurrent_t<64, __nv_bfloat16>(p, s) : launch_recurrent_t<64, float>(p, s);
-    case 128: return bf ? launch_recurrent_t<128, __nv_bfloat16>(p, s) : launch_recurrent_t<128, float>(p, s);
+    case 128: return launch_recurrent128(p, ssm_dtype, s);  // eight rows per thread (lsc_rec128.cu)
     default: return LSC_ERR_UNSUPPORTED;
   }
 }

@@ -65,6 +65,25 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+// The sequence a CTA of a per-sequence grid takes.  With at most kRankedSeqs
+// sequences, the CTA with blockIdx.y = b takes the sequence of rank b by
+// length (longest first, ties by index), so that long sequences do not start
+// last; otherwise sequence b.  Every thread of the CTA calls it.
+constexpr int kRankedSeqs = 256;
+__device__ __forceinline__ int ranked_sequence(const int32_t *cu, int n_seq, int32_t *s_len, int32_t *s_seq) {
+  if (n_seq > kRankedSeqs) return blockIdx.y;
+  for (int s = threadIdx.x; s < n_seq; s += blockDim.x) s_len[s] = cu[s + 1] - cu[s];
+  __syncthreads();
+  for (int s = threadIdx.x; s < n_seq; s += blockDim.x) {
+    const int ls = s_len[s];
+    int rank = 0;
+    for (int j = 0; j < n_seq; ++j) rank += (s_len[j] > ls) || (s_len[j] == ls && j < s);
+    if (rank == (int)blockIdx.y) *s_seq = s;
+  }
+  __syncthreads();
+  return *s_seq;
+}
+
 // 16-byte vectors of state elements <-> float pairs (EPV / 2 of them).
 template <typename TS> struct StatePairs;
 template <> struct StatePairs<float> {

@@ -583,6 +583,7 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
   const lsc::Geom &g = p->g;
   const int32_t Hk = a->num_k_heads;
   if (a->n_seq < 0 || a->total_tokens < 0 || Hk <= 0 || g.Hv % Hk != 0) return LSC_ERR_INVALID_ARG;
+  if (a->algorithm < LSC_RECURRENT_AUTO || a->algorithm > LSC_RECURRENT_CHUNKED) return LSC_ERR_INVALID_ARG;
   if (a->n_seq > 0 && (!a->idx || !a->cu_seqlens)) return LSC_ERR_INVALID_ARG;
   if (a->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->alpha || !a->beta || !a->out))
     return LSC_ERR_INVALID_ARG;
@@ -590,6 +591,9 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
   if (!all_aligned({a->idx, a->cu_seqlens, a->v, a->alpha, a->beta, a->out}, 4)) return LSC_ERR_MISALIGNED;
   if (g.ssm_dtype == LSC_F16) return LSC_ERR_UNSUPPORTED;
   if (a->n_seq > 65535) return LSC_ERR_UNSUPPORTED;
+  // AUTO takes the token kernel: on the CUDA cores it is the faster of the two
+  const bool chunked = a->algorithm == LSC_RECURRENT_CHUNKED;
+  if (chunked && g.dk != 128) return LSC_ERR_UNSUPPORTED;
   rc = check_device(p);
   if (rc != LSC_OK) return rc;
   if (a->n_seq == 0) return LSC_OK;
@@ -614,7 +618,8 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
   r.beta = a->beta;
   r.out = a->out;
   r.status = g.status;
-  return lsc::launch_recurrent(r, g.dk, g.ssm_dtype, (cudaStream_t)stream);
+  return chunked ? lsc::launch_recurrent_chunked(r, g.dk, g.ssm_dtype, (cudaStream_t)stream)
+                 : lsc::launch_recurrent(r, g.dk, g.ssm_dtype, (cudaStream_t)stream);
 }
 
 }  // extern "C"

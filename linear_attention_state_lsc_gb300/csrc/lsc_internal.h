@@ -99,6 +99,10 @@ struct RecurrentParams {
   int32_t *status;
 };
 int launch_recurrent(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
+// the token recurrence for head_k_dim 128 (lsc_rec128.cu)
+int launch_recurrent128(const RecurrentParams &p, int ssm_dtype, cudaStream_t stream);
+// the chunked evaluation (lsc_chunked.cu): head_k_dim 128, head_v_dim <= 128
+int launch_recurrent_chunked(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
 
 struct PrefillConvParams {
   uint8_t *layer;

@@ -40,6 +40,7 @@ LSC_ERR_IO = -18
 LSC_SLOT_FREE, LSC_SLOT_LIVE, LSC_SLOT_CHECKPOINT, LSC_SLOT_RESERVED = 0, 1, 2, 3
 
 LSC_LAYER_ATTENTION, LSC_LAYER_GDN = 0, 1
+LSC_RECURRENT_AUTO, LSC_RECURRENT_TOKEN, LSC_RECURRENT_CHUNKED = 0, 1, 2
 LSC_F32, LSC_BF16, LSC_F16 = 0, 1, 2
 
 
@@ -93,7 +94,7 @@ class lsc_gdn_decode_args(C.Structure):
 
 class lsc_gdn_recurrent_args(C.Structure):
     _fields_ = [("n_seq", C.c_int32), ("num_k_heads", C.c_int32), ("total_tokens", C.c_int32),
-                ("reserved", C.c_int32), ("idx", C.c_void_p), ("has_init", C.c_void_p),
+                ("algorithm", C.c_int32), ("idx", C.c_void_p), ("has_init", C.c_void_p),
                 ("cu_seqlens", C.c_void_p), ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p),
                 ("alpha", C.c_void_p), ("beta", C.c_void_p), ("out", C.c_void_p)]
 
@@ -327,8 +328,8 @@ def lsc_gdn_decode(pool, layer, args, stream=None):
 
 
 def recurrent_args(n_seq, num_k_heads, total_tokens, idx, has_init, cu_seqlens, q, k, v, alpha,
-                   beta, out):
-    return lsc_gdn_recurrent_args(n_seq, num_k_heads, total_tokens, 0, ptr(idx), ptr(has_init),
+                   beta, out, algorithm=0):
+    return lsc_gdn_recurrent_args(n_seq, num_k_heads, total_tokens, algorithm, ptr(idx), ptr(has_init),
                                   ptr(cu_seqlens), ptr(q), ptr(k), ptr(v), ptr(alpha), ptr(beta),
                                   ptr(out))
 

@@ -68,7 +68,8 @@ def test_c2_decode_full_layer(lsc):
         assert P.status() == L.LSC_OK
 
 
-def test_c4_resume_prefill_sampled_sequences(lsc):
+@pytest.mark.parametrize("algorithm", [L.LSC_RECURRENT_TOKEN, L.LSC_RECURRENT_CHUNKED], ids=["token", "chunked"])
+def test_c4_resume_prefill_sampled_sequences(lsc, algorithm):
     w = W.get("c4")
     lengths = W.seq_lengths(64, 64, 2048, seed=0)
     rng = np.random.default_rng(4)
@@ -81,7 +82,7 @@ def test_c4_resume_prefill_sampled_sequences(lsc):
         T = int(cu[-1])
         out = torch.empty((T, w.num_v_heads, w.head_v_dim), device="cuda")
         t = [dev(z) for z in (idx, has, cu, q, k, v, a, b)]
-        args = L.recurrent_args(64, w.num_k_heads, T, *t, out)
+        args = L.recurrent_args(64, w.num_k_heads, T, *t, out, algorithm=algorithm)
         assert L.lsc_gdn_recurrent(P.pool, l, args, torch.cuda.current_stream()) == L.LSC_OK
         torch.cuda.synchronize()
         got = P.download(l).reshape(w.num_slots, -1)

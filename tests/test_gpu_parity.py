@@ -394,11 +394,11 @@ def rec_case(w, lengths, seed, pad_seq=True):
     return idx, has, cu, q, k, v, a, b
 
 
-def run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b):
+def run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b, algorithm=L.LSC_RECURRENT_AUTO):
     T = int(cu[-1])
     out = torch.full((max(T, 1), w.num_v_heads, w.head_v_dim), float("nan"), device="cuda")
     t = [dev(z) for z in (idx, has, cu, q, k, v, a, b)]
-    args = L.recurrent_args(len(idx), w.num_k_heads, T, *t, out)
+    args = L.recurrent_args(len(idx), w.num_k_heads, T, *t, out, algorithm=algorithm)
     rc = L.lsc_gdn_recurrent(P.pool, l, args, torch.cuda.current_stream())
     torch.cuda.synchronize()
     return rc, out.cpu().numpy()[:T]
@@ -421,33 +421,52 @@ def check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out):
     np.testing.assert_array_equal(pg[:, other], pre.reshape(w.num_slots, -1)[:, other])
 
 
-@pytest.mark.parametrize("name,kw", REC_CASES, ids=[f"{n}-{'-'.join(f'{k}{v}' for k, v in kw.items())}" for n, kw in REC_CASES])
-def test_recurrent_matches_oracle(lsc, name, kw):
+REC_ALGOS = {"token": L.LSC_RECURRENT_TOKEN, "chunked": L.LSC_RECURRENT_CHUNKED}
+
+# head_k_dim 128 with head_v_dim below 128 for the chunked form: a multiple of 4
+# (16-byte v rows) and an odd one (4-byte v copies, a ragged last row pair)
+REC_CASES_128 = [("s3", {"head_v_dim": 100, "conv_dim": 2 * 2 * 128 + 4 * 100}),
+                 ("s2", {"head_v_dim": 37, "conv_dim": 2 * 2 * 128 + 4 * 37})]
+
+
+def _case_id(n, kw):
+    return f"{n}-{'-'.join(f'{k}{v}' for k, v in kw.items())}"
+
+
+@pytest.mark.parametrize("algo", list(REC_ALGOS))
+@pytest.mark.parametrize("name,kw", REC_CASES + REC_CASES_128, ids=[_case_id(n, kw) for n, kw in REC_CASES + REC_CASES_128])
+def test_recurrent_matches_oracle(lsc, name, kw, algo):
     w = workload(name, **kw)
     lengths = [0, 1, 15, 16, 17, 40, 5][:min(7, w.num_slots)]
     with DevPool(w, seed=12, random_padding=True) as P:
         l = P.gdn_layers[0]
         pre = P.host[l].copy()
         idx, has, cu, q, k, v, a, b = rec_case(w, lengths, seed=5)
-        rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b)
+        rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b, REC_ALGOS[algo])
+        if algo == "chunked" and w.head_k_dim != 128:
+            assert rc == L.LSC_ERR_UNSUPPORTED
+            np.testing.assert_array_equal(P.download(l), pre)
+            return
         assert rc == L.LSC_OK, L.lsc_error_string(rc)
         check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out)
         assert P.status() == L.LSC_OK
 
 
-def test_recurrent_long_sequence_fp32(lsc):
+@pytest.mark.parametrize("algo", list(REC_ALGOS))
+def test_recurrent_long_sequence_fp32(lsc, algo):
     """A few hundred tokens: the recurrence stays within the fp32 bound."""
     w = workload("s3")
     with DevPool(w, seed=13) as P:
         l = P.gdn_layers[0]
         pre = P.host[l].copy()
         idx, has, cu, q, k, v, a, b = rec_case(w, [300, 129], seed=6, pad_seq=False)
-        rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b)
+        rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b, REC_ALGOS[algo])
         assert rc == L.LSC_OK
         check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out)
 
 
-def test_recurrent_equals_decode_free_steps(lsc):
+@pytest.mark.parametrize("algo", list(REC_ALGOS))
+def test_recurrent_equals_decode_free_steps(lsc, algo):
     """alpha = 1, beta = 0 at every token: the state is unchanged bit for bit
     and o_t = S q_t (the closed form of the benchmark spec, on the GPU)."""
     w = workload("s2")
@@ -458,7 +477,36 @@ def test_recurrent_equals_decode_free_steps(lsc):
         has[:] = 1
         a[:] = 1.0
         b[:] = 0.0
-        rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b)
+        rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b, REC_ALGOS[algo])
         assert rc == L.LSC_OK
         np.testing.assert_array_equal(P.download(l), pre)
         check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out)
+
+
+@pytest.mark.parametrize("algo", list(REC_ALGOS))
+def test_recurrent_gate_extremes(lsc, algo):
+    """alpha = 0 (the state restarts from b v k^T), alpha ~ 1e-9 (the decay
+    products underflow inside a chunk) and beta = 1, inside and across chunks."""
+    w = workload("s3")
+    with DevPool(w, seed=15) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, cu, q, k, v, a, b = rec_case(w, [50, 33, 16], seed=8, pad_seq=False)
+        has[:] = 1
+        a[3] = 0.0
+        a[20:27] = 1e-9
+        a[cu[1] + 15] = 0.0
+        b[cu[1]:cu[1] + 10] = 1.0
+        rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b, REC_ALGOS[algo])
+        assert rc == L.LSC_OK
+        check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out)
+
+
+def test_recurrent_rejects(lsc):
+    w = workload("s1")
+    with DevPool(w) as P:
+        idx, has, cu, q, k, v, a, b = rec_case(w, [3], seed=9, pad_seq=False)
+        for algo, rc_want in ((3, L.LSC_ERR_INVALID_ARG), (-1, L.LSC_ERR_INVALID_ARG),
+                              (L.LSC_RECURRENT_CHUNKED, L.LSC_ERR_UNSUPPORTED)):  # s1: head_k_dim 32
+            rc, _ = run_recurrent(P, P.gdn_layers[0], w, idx, has, cu, q, k, v, a, b, algo)
+            assert rc == rc_want
