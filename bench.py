@@ -56,6 +56,24 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(x, device):
+    """The largest of every rank's x (an elapsed time): the job's clock is its
+    slowest replica.  With one rank, x itself."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, elapsed):
+    """Units all ranks processed per second of the slowest rank's clock
+    (replicas: every rank processes the same number of units)."""
+    return world * units_per_rank / elapsed
+
+
 # ---------------------------------------------------------------- clocks
 
 class Clocks:
@@ -257,11 +275,8 @@ def run_lsc(args):
     torch.cuda.synchronize()
     ck = clocks.stop()
     ck["window"] = "warm-up + timed region + trailing untimed steps"
-    elapsed = t0.elapsed_time(t1) / 1e3
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, "cuda")
     if world > 1:
-        tt = torch.tensor([elapsed], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = float(tt.item())
         dist.barrier()
     assert L.lsc_pool_status(pool, fwd) == L.LSC_OK
 
@@ -272,8 +287,8 @@ def run_lsc(args):
     t_decode = statistics.mean(ev["d0"][i].elapsed_time(ev["d1"][i]) for i in range(args.steps)) / 1e3 / n_gdn
     restore_gbs = rb / t_restore / 1e9
     decode_gbs = decode_bytes(v0, w, n) / t_decode / 1e9
-    value = world * step_bytes * args.steps / elapsed / 1e9
-    rows_per_s = world * n * args.steps / elapsed
+    value = whole_job_rate(world, step_bytes * args.steps, elapsed) / 1e9
+    rows_per_s = whole_job_rate(world, n * args.steps, elapsed)
 
     roof_restore = {"bound": "hbm", "kernel": "restore_kernel", "achieved": round(restore_gbs, 1),
                     "peak": hbm_peak, "unit": "GB/s", "frac": round(restore_gbs / hbm_peak, 4),
@@ -372,13 +387,8 @@ def e2e_serving(args, L, torch, pool, w, rows, ops, n, n_gdn, X, CW, A, B, step_
     for _ in range(args.steps):
         step()
     torch.cuda.synchronize()
-    el = time.perf_counter() - t
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([el], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        el = float(tt.item())
-    return {"value": round(world * step_bytes * args.steps / el / 1e9, 2), "unit": UNIT,
+    el = max_over_ranks(time.perf_counter() - t, "cuda")
+    return {"value": round(whole_job_rate(world, step_bytes * args.steps, el) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(el / args.steps * 1e3, 4), "clock": "host wall clock",
             "overlap": "restore inputs on the prepare stream, decode inputs H2D during the restore, per-layer D2H on a copy stream"}
