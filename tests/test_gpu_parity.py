@@ -426,7 +426,8 @@ REC_ALGOS = {"token": L.LSC_RECURRENT_TOKEN, "chunked": L.LSC_RECURRENT_CHUNKED}
 # head_k_dim 128 with head_v_dim below 128 for the chunked form: a multiple of 4
 # (16-byte v rows) and an odd one (4-byte v copies, a ragged last row pair)
 REC_CASES_128 = [("s3", {"head_v_dim": 100, "conv_dim": 2 * 2 * 128 + 4 * 100}),
-                 ("s2", {"head_v_dim": 37, "conv_dim": 2 * 2 * 128 + 4 * 37})]
+                 ("s2", {"head_v_dim": 37, "conv_dim": 2 * 2 * 128 + 4 * 37}),
+                 ("s3", {"head_v_dim": 1, "conv_dim": 2 * 2 * 128 + 4 * 1})]
 
 
 def _case_id(n, kw):
@@ -500,6 +501,42 @@ def test_recurrent_gate_extremes(lsc, algo):
         rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b, REC_ALGOS[algo])
         assert rc == L.LSC_OK
         check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out)
+
+
+@pytest.mark.parametrize("algo", list(REC_ALGOS))
+def test_recurrent_many_sequences(lsc, algo):
+    """More sequences than the CTAs rank by length (256): the plain order."""
+    w = workload("s3", num_slots=320)
+    rng = np.random.default_rng(21)
+    lengths = rng.integers(0, 24, 300).tolist()
+    with DevPool(w, seed=16) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, cu, q, k, v, a, b = rec_case(w, lengths, seed=10)
+        rc, out = run_recurrent(P, l, w, idx, has, cu, q, k, v, a, b, REC_ALGOS[algo])
+        assert rc == L.LSC_OK
+        check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out)
+        assert P.status() == L.LSC_OK
+
+
+@pytest.mark.parametrize("algo", list(REC_ALGOS))
+def test_recurrent_bad_rows_are_skipped_and_reported(lsc, algo):
+    """A slot id past the pool: that sequence's outputs are zero, no state is
+    touched, OUT_OF_RANGE is recorded; the other sequences are unaffected."""
+    w = workload("s3")
+    with DevPool(w, seed=17) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, cu, q, k, v, a, b = rec_case(w, [20, 33, 7], seed=11, pad_seq=False)
+        bad = idx.copy()
+        bad[1] = w.num_slots + 3
+        rc, out = run_recurrent(P, l, w, bad, has, cu, q, k, v, a, b, REC_ALGOS[algo])
+        assert rc == L.LSC_OK
+        assert P.status() == L.LSC_ERR_OUT_OF_RANGE
+        np.testing.assert_array_equal(out[cu[1]:cu[2]], 0.0)
+        ref = idx.copy()
+        ref[1] = -1  # the oracle's view: a padding sequence
+        check_recurrent(w, P, l, pre, ref, has, cu, q, k, v, a, b, out)
 
 
 def test_recurrent_rejects(lsc):

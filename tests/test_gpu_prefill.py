@@ -92,6 +92,35 @@ def test_prefill_conv_matches_oracle(lsc, name, kw, x_offset):
         assert P.status() == L.LSC_OK
 
 
+def with_width(name, width):
+    """A shape with another conv width; the page grows to hold the wider conv state."""
+    w = shape(name)
+    w.conv_width = width
+    conv_bytes = w.conv_dim * (width - 1) * W.ESIZE[w.conv_dtype]
+    ssm_bytes = w.num_v_heads * w.head_v_dim * w.head_k_dim * W.ESIZE[w.ssm_dtype]
+    w.page_bytes = (conv_bytes + 15) // 16 * 16 + ssm_bytes + 256
+    return w
+
+
+@pytest.mark.parametrize("name", ["c0", "s3"], ids=["f32-conv", "bf16-conv"])
+@pytest.mark.parametrize("width", [2, 3, 5, 8])
+@pytest.mark.parametrize("x_offset", [0, 1], ids=["aligned", "x-off-16B"])
+def test_prefill_conv_other_widths(lsc, name, width, x_offset):
+    """Conv widths other than 4: the run-time-width fast path (aligned x) and
+    the two-pass path (x one element off a 16-byte boundary)."""
+    w = with_width(name, width)
+    x_offset *= W.ESIZE[w.conv_dtype]
+    lengths = [0, 1, width - 1, width, 70, 9][:w.num_slots]
+    with DevPool(w, seed=22, random_padding=True) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, cu, xr, cwr = inputs(w, lengths, seed=5)
+        rc, q, k, v = run(P, l, w, idx, has, cu, xr, cwr, x_offset)
+        assert rc == L.LSC_OK, L.lsc_error_string(rc)
+        check(w, P, l, pre, idx, has, cu, xr, cwr, q, k, v)
+        assert P.status() == L.LSC_OK
+
+
 def test_prefill_then_decode_continues(lsc):
     """After a prefill the slot's conv state is the one a decode continues from:
     prefill of T tokens then one decode token equals the oracle doing the same."""
