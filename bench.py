@@ -409,6 +409,62 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3 / k
 
+    # context, not a target: the pages' own restore mechanism on c1 ([XN] §4.3),
+    # per hit row and GDN layer a torch copy_ of the conv slot and a
+    # narrow().copy_() of the ssm slot, enqueued on a prepare stream; beside it
+    # the persistent restore launch on the same pool and rows
+    w = W.get("c1")
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    rows = W.restore_rows("c1", seed=0)
+    hits = [(int(d), int(s)) for d, s in zip(rows.live, rows.src) if s >= 0]
+    tviews = []
+    for l in w.gdn_layers:
+        v = views[l]
+        pages = buf[v.region - buf.data_ptr():][:v.region_bytes].view(w.num_slots, w.page_bytes)
+        conv = pages[:, :v.conv_bytes].view(torch.bfloat16)
+        ssm = pages[:, v.ssm_offset_bytes:v.ssm_offset_bytes + v.ssm_bytes].view(torch.float32)
+        tviews.append((conv, ssm))
+    prep = torch.cuda.Stream()
+
+    def torch_loop():
+        with torch.cuda.stream(prep):
+            for conv, ssm in tviews:
+                for d, s_ in hits:
+                    conv[d].copy_(conv[s_])
+                    ssm.narrow(0, d, 1).copy_(ssm.narrow(0, s_, 1))
+
+    def timed_on(stream, fn, k):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / k
+
+    t_loop = timed_on(prep, torch_loop, 3)
+    ops = L.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
+    hs = torch.empty(len(rows.live), dtype=torch.uint8, device="cuda")
+
+    def lsc_call():
+        rc, _ = L.lsc_restore(pool, ops, rows.nkv, rows.block_size, rows.initialized, hs, prep, None)
+        assert rc == L.LSC_OK
+
+    t_lsc = timed_on(prep, lsc_call, 3)
+    v0 = views[w.gdn_layers[0]]
+    nb = 2 * len(hits) * len(w.gdn_layers) * (v0.conv_bytes + v0.ssm_bytes)
+    parts["restore_torch_loop_c1"] = {
+        "workload": f"c1: {len(hits)} hit rows x {len(w.gdn_layers)} GDN layers, the pages' loop of torch copies "
+                    f"({2 * len(hits) * len(w.gdn_layers)} copy_ calls per restore)",
+        "kind": "context (the pages' mechanism), not a target", "launch_ms": round(t_loop * 1e3, 3),
+        "GB/s": round(nb / t_loop / 1e9, 1), "frac": round(nb / t_loop / 1e9 / hbm_peak, 4),
+        "restore_kernel_ms": round(t_lsc * 1e3, 3), "speedup_of_restore_kernel": round(t_loop / t_lsc, 2)}
+    L.lsc_pool_destroy(pool)
+    del buf, tviews, hs
+    torch.cuda.empty_cache()
+
     # decode step at 256 rows, bf16 state, one launch per layer over 36 layers
     w = W.get("c2")
     buf, pool, views = make_pool(L, W, w, seed=0)
