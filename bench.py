@@ -515,7 +515,7 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     parts["restore_c3"] = {"workload": "c3: 512 rows over 1024 slots, 205 hit / 154 miss / 153 no-op, hot source",
                            "kernel": "restore_kernel", "launch_ms": round(t * 1e3, 4), "bytes_per_launch": bytes_,
                            "GB/s": round(bytes_ / t / 1e9, 1), "frac": round(bytes_ / t / 1e9 / hbm_peak, 4),
-                           "rows_per_s": round(512 / t, 1)}
+                           "rows_per_s": round(512 / t, 1), "traffic": kernel_traffic("restore_kernel c3")}
     L.lsc_pool_destroy(pool)
     del buf, hs
     torch.cuda.empty_cache()
@@ -857,6 +857,7 @@ NCU_CASES = {
     "decode_f32": ("c1", 64, "decode"),      # serving-step decode: fp32 state, 64 rows, 277 MB per launch
     "decode_bf16": ("c2", 256, "decode"),    # bf16 state, 256 rows, 571 MB per launch
     "restore": ("c1", 64, "restore"),        # 64 hits x 2 layers, 549 MB per launch
+    "restore_c3": ("c3", 512, "restore"),    # the c3 storm on 2 of its 36 layers (4.4 GB pool, 1.76 GB algorithmic)
     "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer (token by token)
     "recurrent_chunked": ("c4", 16, "recurrent_chunked"),  # the same, 16-token chunks
     "prefill": ("c4", 32, "prefill"),        # prefill conv: 32 sequences of 64..2048 tokens, one layer
@@ -890,7 +891,7 @@ def run_ncu_case(args):
         def launch(i):
             assert L.lsc_copy_prefix(kpool, kops, fwd)[0] == L.LSC_OK
     elif kind == "restore":
-        rows = W.restore_rows("c1")
+        rows = W.restore_rows(name)
         ops = L.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
         hs = torch.from_numpy(rows.hs_prefill.copy()).cuda()
 
