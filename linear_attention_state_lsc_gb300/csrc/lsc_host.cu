@@ -207,6 +207,7 @@ int lsc_pool_required_bytes(const lsc_pool_desc *desc, size_t *total_bytes) {
 }
 
 int lsc_pool_create(const lsc_pool_desc *desc, void *device_base, size_t base_bytes, lsc_pool **out) {
+  lsc::TraceRange trace_("lsc_pool_create");
   if (!out) return LSC_ERR_INVALID_ARG;
   *out = nullptr;
   lsc_pool *p = new (std::nothrow) lsc_pool();
@@ -319,6 +320,7 @@ int lsc_pool_layer_view(const lsc_pool *p, int32_t layer, lsc_layer_view *v) {
 }
 
 int lsc_pool_status(lsc_pool *p, void *stream, int32_t *host_status) {
+  lsc::TraceRange trace_("lsc_pool_status");
   if (!p || !host_status) return LSC_ERR_INVALID_ARG;
   int rc = check_device(p);
   if (rc != LSC_OK) return rc;
@@ -345,6 +347,7 @@ int lsc_restore_classify(const lsc_pool *p, const LinearStateCacheOp *ops, int32
 int lsc_restore(lsc_pool *p, const LinearStateCacheOp *ops, int32_t n_rows, const int32_t *nkv,
                 int32_t block_size, const uint8_t *init, uint8_t *has_initial_state, void *prepare_stream,
                 void *done_event, lsc_restore_report *report) {
+  lsc::TraceRange trace_("lsc_restore");
   if (!p) return LSC_ERR_INVALID_ARG;
   std::vector<int8_t> act;
   lsc_restore_report rep{};
@@ -435,6 +438,7 @@ static int access_params(lsc_pool *p, int32_t layer, const int32_t *idx, int32_t
 
 int lsc_gather(lsc_pool *p, int32_t layer, const int32_t *idx, const uint8_t *has_init, int32_t n,
                void *conv_dense, void *ssm_dense, void *stream) {
+  lsc::TraceRange trace_("lsc_gather");
   lsc::AccessParams a;
   int rc = access_params(p, layer, idx, n, &a);
   if (rc != LSC_OK) return rc;
@@ -452,6 +456,7 @@ int lsc_gather(lsc_pool *p, int32_t layer, const int32_t *idx, const uint8_t *ha
 
 int lsc_scatter(lsc_pool *p, int32_t layer, const int32_t *idx, int32_t n, const void *conv_dense,
                 const void *ssm_dense, void *stream) {
+  lsc::TraceRange trace_("lsc_scatter");
   lsc::AccessParams a;
   int rc = access_params(p, layer, idx, n, &a);
   if (rc != LSC_OK) return rc;
@@ -467,6 +472,7 @@ int lsc_scatter(lsc_pool *p, int32_t layer, const int32_t *idx, int32_t n, const
 }
 
 int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, void *stream) {
+  lsc::TraceRange trace_("lsc_gdn_decode");
   if (!p || !a) return LSC_ERR_INVALID_ARG;
   uint8_t *region;
   int rc = layer_base(p, layer, &region);
@@ -522,6 +528,7 @@ int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, voi
 }
 
 int lsc_gdn_prefill_conv(lsc_pool *p, int32_t layer, const lsc_gdn_prefill_conv_args *a, void *stream) {
+  lsc::TraceRange trace_("lsc_gdn_prefill_conv");
   if (!p || !a) return LSC_ERR_INVALID_ARG;
   uint8_t *region;
   int rc = layer_base(p, layer, &region);
@@ -576,6 +583,7 @@ int lsc_gdn_prefill_conv(lsc_pool *p, int32_t layer, const lsc_gdn_prefill_conv_
 }
 
 int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *a, void *stream) {
+  lsc::TraceRange trace_("lsc_gdn_recurrent");
   if (!p || !a) return LSC_ERR_INVALID_ARG;
   uint8_t *region;
   int rc = layer_base(p, layer, &region);

@@ -2,11 +2,23 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "lsc.h"
 
 namespace lsc {
+
+// An NVTX range named after a public call, open for the call's duration, so
+// that a timeline profiler shows each lsc_* call beside the kernels it
+// enqueued.  NVTX v3 is header-only: without a profiler attached the push and
+// pop return at once.
+struct TraceRange {
+  explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange &) = delete;
+  TraceRange &operator=(const TraceRange &) = delete;
+};
 
 // Byte geometry of one GDN layer region; the same for every GDN layer.
 struct Geom {

@@ -159,6 +159,7 @@ int lsc_kv_pool_layer_view(const lsc_kv_pool *p, int32_t layer, lsc_kv_layer_vie
 
 int lsc_copy_prefix(lsc_kv_pool *p, const lsc_kv_copy_op *ops, int32_t n_ops, void *stream, void *done_event,
                     int64_t *bytes_copied) {
+  lsc::TraceRange trace_("lsc_copy_prefix");
   if (!p || n_ops < 0 || (n_ops > 0 && !ops)) return LSC_ERR_INVALID_ARG;
   const int32_t B = p->d.num_blocks;
   // validate every copying op before enqueueing anything

@@ -23,6 +23,7 @@
 #include <vector>
 
 #include "lsc.h"
+#include "lsc_internal.h"
 #include "lsc_store.h"
 
 namespace {
@@ -486,6 +487,7 @@ int lsc_store_stats_get(const lsc_store *s, lsc_store_stats *o) {
 }
 
 int lsc_store_save_state(lsc_store *s, uint64_t key, lsc_pool *pool, int32_t slot, void *stream) {
+  lsc::TraceRange trace_("lsc_store_save_state");
   if (!s || !pool) return LSC_ERR_INVALID_ARG;
   SlotViews sv;
   int rc = slot_views(pool, slot, &sv);
@@ -512,6 +514,7 @@ int lsc_store_save_state(lsc_store *s, uint64_t key, lsc_pool *pool, int32_t slo
 }
 
 int lsc_store_load_state(lsc_store *s, uint64_t key, lsc_pool *pool, int32_t slot, void *stream) {
+  lsc::TraceRange trace_("lsc_store_load_state");
   if (!s || !pool) return LSC_ERR_INVALID_ARG;
   SlotViews sv;
   int rc = slot_views(pool, slot, &sv);
