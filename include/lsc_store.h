@@ -13,6 +13,7 @@
  *        depend on them; make_room removes unreferenced blocks first, then
  *        unpinned entries least recently used; pin / unpin; dropping an entry
  *        unreferences its blocks, shared blocks stay; no room = the write fails)
+ *        and "读取成本与重新计算成本" (the read path uses up to four threads)
  *
  * File format (little-endian), one file per blob or entry:
  *   bytes 0..7    "LSCSNAP1"
@@ -43,6 +44,13 @@
  *
  * Return codes of lsc.h; on an error nothing changed unless stated.  A store
  * is not thread-safe.
+ *
+ * Parallel I/O: a payload of at least two parts is written and read by up to
+ * four threads, each on one contiguous part (pwrite / pread at its offset)
+ * and checksumming it; the payload CRC is joined from the parts' CRCs
+ * (crc(A || B) = crc(A) x^(8|B|) + crc(B) mod the polynomial), so the file
+ * format does not change.  The part size is 4 MiB, or LSC_STORE_IO_PART bytes
+ * (a positive multiple of 4096) when that is set as the store is opened.
  */
 #ifndef LSC_STORE_H
 #define LSC_STORE_H

@@ -16,9 +16,11 @@
 #include <cerrno>
 #include <cinttypes>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
+#include <thread>
 #include <unordered_map>
 #include <vector>
 
@@ -64,6 +66,85 @@ const Crc32c &crc() {
   return c;
 }
 
+// ---- CRC-32C of a concatenation from the CRCs of its parts ----
+// The CRC register is an affine function of the input bits, and joining two
+// messages cancels the pre- and post-inversion, so
+//   crc(A || B) = crc(A) * x^(8 |B|) + crc(B)   (mod P, over GF(2)),
+// with polynomials in the reflected representation the table CRC uses: bit 31
+// holds the coefficient of x^0, bit 0 that of x^31, and multiplying by x is
+// one zero-input step of the register.
+uint32_t gf2_mulmod(uint32_t a, uint32_t b) {
+  uint32_t prod = 0, bxk = b;  // bxk = b * x^k
+  for (int k = 0; k < 32; ++k) {
+    if (a & (0x80000000u >> k)) prod ^= bxk;
+    bxk = (bxk >> 1) ^ ((bxk & 1) ? 0x82F63B78u : 0u);
+  }
+  return prod;
+}
+uint32_t x_pow_8n(uint64_t n) {  // x^(8 n) mod P by repeated squaring
+  uint32_t r = 0x80000000u, sq = 0x80000000u >> 8;  // x^0, x^8
+  for (; n; n >>= 1) {
+    if (n & 1) r = gf2_mulmod(r, sq);
+    sq = gf2_mulmod(sq, sq);
+  }
+  return r;
+}
+uint32_t crc_join(uint32_t crc_a, uint32_t crc_b, uint64_t len_b) { return gf2_mulmod(crc_a, x_pow_8n(len_b)) ^ crc_b; }
+
+// ---- parallel file I/O ([KP]: the disk tier reads with up to four threads) ----
+constexpr int kIoThreads = 4;
+constexpr int64_t kIoPart = 4 << 20;  // default part size: payloads below two parts stay on one thread
+
+// The part size: LSC_STORE_IO_PART (bytes, a positive multiple of 4096) when
+// set, else kIoPart.
+int64_t io_part_from_env() {
+  const char *e = getenv("LSC_STORE_IO_PART");
+  if (!e) return kIoPart;
+  const long long v = atoll(e);
+  return v > 0 && v % 4096 == 0 ? (int64_t)v : kIoPart;
+}
+
+struct Part {
+  int64_t off, len;
+  uint32_t crc;
+  bool ok;
+};
+
+// Splits [0, n) into up to kIoThreads contiguous parts of at least `part`
+// bytes (4 KiB-aligned boundaries) and runs fn(part) for each, the first on
+// the calling thread.
+template <typename F>
+std::vector<Part> run_parts(int64_t n, int64_t part, F fn) {
+  int t = (int)std::min<int64_t>(kIoThreads, std::max<int64_t>(1, n / part));
+  std::vector<Part> parts((size_t)t);
+  for (int i = 0; i < t; ++i) {
+    const int64_t a = (n * i / t) & ~(int64_t)4095, b = i + 1 == t ? n : (n * (i + 1) / t) & ~(int64_t)4095;
+    parts[(size_t)i] = Part{a, b - a, 0, false};
+  }
+  std::vector<std::thread> th;
+  for (int i = 1; i < t; ++i) {
+    try {
+      th.emplace_back([&fn, &parts, i] { fn(parts[(size_t)i]); });
+    } catch (...) {  // no thread: run the part here
+      fn(parts[(size_t)i]);
+    }
+  }
+  fn(parts[0]);
+  for (auto &x : th) x.join();
+  return parts;
+}
+
+// The CRC of the parts in order, or false when a part failed.
+bool joined_crc(const std::vector<Part> &parts, uint32_t *out) {
+  uint32_t c = 0;
+  for (size_t i = 0; i < parts.size(); ++i) {
+    if (!parts[i].ok) return false;
+    c = i == 0 ? parts[i].crc : crc_join(c, parts[i].crc, (uint64_t)parts[i].len);
+  }
+  *out = c;
+  return true;
+}
+
 constexpr int kHeader = 64;
 constexpr uint32_t kVersion = 1;
 constexpr int32_t kEntryKind = 255;
@@ -98,20 +179,6 @@ int64_t check_header(const uint8_t *h, uint64_t ns, uint64_t key, int32_t *kind)
   return (int64_t)get_le(h + 32, 8);
 }
 
-bool write_all(int fd, const void *p, size_t n) {
-  const uint8_t *c = (const uint8_t *)p;
-  while (n) {
-    const ssize_t w = ::write(fd, c, n);
-    if (w < 0) {
-      if (errno == EINTR) continue;
-      return false;
-    }
-    c += w;
-    n -= (size_t)w;
-  }
-  return true;
-}
-
 bool read_all(int fd, void *p, size_t n) {
   uint8_t *c = (uint8_t *)p;
   while (n) {
@@ -123,6 +190,37 @@ bool read_all(int fd, void *p, size_t n) {
     if (r == 0) return false;
     c += r;
     n -= (size_t)r;
+  }
+  return true;
+}
+
+bool pread_all(int fd, void *p, size_t n, int64_t at) {
+  uint8_t *c = (uint8_t *)p;
+  while (n) {
+    const ssize_t r = ::pread(fd, c, n, (off_t)at);
+    if (r < 0) {
+      if (errno == EINTR) continue;
+      return false;
+    }
+    if (r == 0) return false;
+    c += r;
+    at += r;
+    n -= (size_t)r;
+  }
+  return true;
+}
+
+bool pwrite_all(int fd, const void *p, size_t n, int64_t at) {
+  const uint8_t *c = (const uint8_t *)p;
+  while (n) {
+    const ssize_t w = ::pwrite(fd, c, n, (off_t)at);
+    if (w < 0) {
+      if (errno == EINTR) continue;
+      return false;
+    }
+    c += w;
+    at += w;
+    n -= (size_t)w;
   }
   return true;
 }
@@ -147,6 +245,7 @@ struct lsc_store {
   uint64_t clock = 0;
   std::unordered_map<uint64_t, Blob> blobs;
   std::unordered_map<uint64_t, Entry> entries;
+  int64_t io_part = kIoPart;  // parallel I/O part size
   void *pinned = nullptr;  // host staging of save/load_state
   size_t pinned_bytes = 0;
 
@@ -156,17 +255,24 @@ struct lsc_store {
     return dir + name;
   }
 
-  // temporary file + CRCs + rename ([KP]: a failed write removes the temporary file)
+  // temporary file + CRCs + rename ([KP]: a failed write removes the temporary
+  // file); a large payload is checksummed and written by up to four threads
   int write_file(const char *sub, uint64_t key, int32_t kind, const void *data, int64_t bytes) {
     const std::string tmp = path("tmp", key), fin = path(sub, key);
     uint8_t h[kHeader];
     make_header(h, kind, ns, key, (uint64_t)bytes);
-    uint8_t c[4];
-    put_le(c, crc()((const uint8_t *)data, (size_t)bytes), 4);
     const int fd = ::open(tmp.c_str(), O_WRONLY | O_CREAT | O_TRUNC, 0644);
     if (fd < 0) return LSC_ERR_IO;
-    const bool ok = write_all(fd, h, kHeader) && write_all(fd, data, (size_t)bytes) && write_all(fd, c, 4) &&
-                    ::fsync(fd) == 0;
+    const uint8_t *d = (const uint8_t *)data;
+    const std::vector<Part> parts = run_parts(bytes, io_part, [fd, d](Part &pt) {
+      pt.crc = crc()(d + pt.off, (size_t)pt.len);
+      pt.ok = pwrite_all(fd, d + pt.off, (size_t)pt.len, kHeader + pt.off);
+    });
+    uint32_t pc = 0;
+    uint8_t c[4];
+    bool ok = joined_crc(parts, &pc);
+    put_le(c, pc, 4);
+    ok = ok && pwrite_all(fd, h, kHeader, 0) && pwrite_all(fd, c, 4, kHeader + bytes) && ::fsync(fd) == 0;
     if (::close(fd) != 0 || !ok || ::rename(tmp.c_str(), fin.c_str()) != 0) {
       ::unlink(tmp.c_str());
       return LSC_ERR_IO;
@@ -296,6 +402,7 @@ int lsc_store_open(const char *dir, uint64_t ns, int64_t quota, lsc_store **out)
     s->dir = std::string(dir) + sub;
     s->ns = ns;
     s->quota = quota;
+    s->io_part = io_part_from_env();
     if (!mkdir_p(dir) || !mkdir_p(s->dir) || !mkdir_p(s->dir + "/b") || !mkdir_p(s->dir + "/e") ||
         !mkdir_p(s->dir + "/tmp")) {
       delete s;
@@ -412,9 +519,17 @@ int lsc_store_get_blob(lsc_store *s, uint64_t key, void *dst, int64_t cap, int64
   uint8_t h[kHeader], c[4];
   int32_t k = 0;
   struct stat st;
-  const bool ok = ::fstat(fd, &st) == 0 && read_all(fd, h, kHeader) && check_header(h, s->ns, key, &k) == n &&
-                  st.st_size == kHeader + n + 4 && read_all(fd, dst, (size_t)n) && read_all(fd, c, 4) &&
-                  get_le(c, 4) == crc()((const uint8_t *)dst, (size_t)n);
+  bool ok = ::fstat(fd, &st) == 0 && pread_all(fd, h, kHeader, 0) && check_header(h, s->ns, key, &k) == n &&
+            st.st_size == kHeader + n + 4 && pread_all(fd, c, 4, kHeader + n);
+  if (ok) {  // the payload, by up to four reader threads, each checksumming its part
+    uint8_t *d = (uint8_t *)dst;
+    const std::vector<Part> parts = run_parts(n, s->io_part, [fd, d](Part &pt) {
+      pt.ok = pread_all(fd, d + pt.off, (size_t)pt.len, kHeader + pt.off);
+      if (pt.ok) pt.crc = crc()(d + pt.off, (size_t)pt.len);
+    });
+    uint32_t pc = 0;
+    ok = joined_crc(parts, &pc) && get_le(c, 4) == pc;
+  }
   ::close(fd);
   if (!ok) {
     s->drop_damaged(key);

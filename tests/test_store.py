@@ -173,3 +173,51 @@ def test_reopen_drops_files_damaged_on_disk(lsc, tmp_path):
     rc, s = L.lsc_store_open(d, 5, 1 << 20)
     assert L.lsc_store_stats_get(s)[1].n_blobs == 2
     L.lsc_store_close(s)
+
+
+@pytest.mark.parametrize("n", [4095, 4096 * 2, 4096 * 3 + 123, 40000, 4096 * 9 + 7])
+def test_payload_in_parallel_parts(lsc, tmp_path, monkeypatch, n):
+    """[KP] reads the disk tier with up to four threads.  With 4 KiB parts a
+    payload is written and read in 1-4 parts by as many threads: the file is
+    byte-equal to the oracle's (the CRC joined from the parts' CRCs is the CRC
+    of the whole payload), it reads back intact, and a damaged byte in any part
+    is found (the blob and its entries are dropped)."""
+    monkeypatch.setenv("LSC_STORE_IO_PART", "4096")
+    d = str(tmp_path)
+    rng = random.Random(n)
+    payload = bytes(rng.randrange(256) for _ in range(n))
+    for where in [None, 0, n // 3, n // 2, n - 1]:
+        rc, s = L.lsc_store_open(d, 0xABC, 1 << 24)
+        assert rc == L.LSC_OK
+        key = 0x100 + (where if where is not None else 0xFFFF)
+        assert L.lsc_store_put_blob(s, key, 2, payload) == L.LSC_OK
+        path = blob_path(d, key, 0xABC)
+        assert open(path, "rb").read() == file_bytes(2, 0xABC, key, payload)
+        if where is None:
+            assert L.lsc_store_get_blob(s, key) == (L.LSC_OK, 2, payload)
+        else:
+            assert L.lsc_store_put_entry(s, 9, [key]) == L.LSC_OK
+            with open(path, "r+b") as f:
+                f.seek(HEADER + where)
+                b = f.read(1)
+                f.seek(HEADER + where)
+                f.write(bytes([b[0] ^ 0x40]))
+            assert L.lsc_store_get_blob(s, key)[0] == L.LSC_ERR_CORRUPT
+            assert not os.path.exists(path)
+            assert L.lsc_store_get_entry(s, 9)[0] == L.LSC_ERR_NOT_FOUND
+        L.lsc_store_close(s)
+
+
+def test_part_size_setting_is_validated(lsc, tmp_path, monkeypatch):
+    """A part size that is not a positive multiple of 4096 falls back to the
+    default (payloads below 8 MiB then stay in one part); files are unchanged."""
+    for i, bad in enumerate(["0", "-4096", "1000", "junk"]):
+        monkeypatch.setenv("LSC_STORE_IO_PART", bad)
+        rc, s = L.lsc_store_open(str(tmp_path), 5, 1 << 20)
+        assert rc == L.LSC_OK
+        payload = bytes(range(256)) * 40
+        key = 0x500 + i
+        assert L.lsc_store_put_blob(s, key, 1, payload) == L.LSC_OK
+        assert open(blob_path(str(tmp_path), key, 5), "rb").read() == file_bytes(1, 5, key, payload)
+        assert L.lsc_store_get_blob(s, key) == (L.LSC_OK, 1, payload)
+        L.lsc_store_close(s)
