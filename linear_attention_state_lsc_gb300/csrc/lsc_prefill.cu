@@ -50,27 +50,6 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int n_seq, int t) {
   return lo;
 }
 
-// Eight conv-dtype values from shared memory (16-byte aligned), as floats.
-template <typename TC> struct Smem8;
-template <> struct Smem8<__nv_bfloat16> {
-  __device__ __forceinline__ static void unpack(const uint4 *q, float *f) {
-    const uint4 u = q[0];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-  }
-};
-template <> struct Smem8<float> {
-  __device__ __forceinline__ static void unpack(const uint4 *q, float *f) {
-    const uint4 a = q[0], b = q[1];
-    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
-    f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
-  }
-};
-
 // Eight floats, passed by value.
 struct F8 {
   float v[8];
