@@ -26,8 +26,22 @@
 // values in the order (value index) XOR (its lane index): row r of the group
 // sits in register slot r ^ (l >> 1) and odd lanes form the q products first,
 // so every round keeps the lower half and sends the upper one, with no
-// lane-dependent selects.  The scalars of each token (alpha gamma, beta,
-// 1 / gamma', the fold) depend on alpha alone and are formed once per tile.
+// lane-dependent selects.
+//
+// Tokens go in pairs (a, b): one pass over the state forms both tokens' dot
+// products against the state before the pair, and b's are corrected with the
+// pair's Gram scalars (true state S = gamma Shat; gamma_a' = alpha_a gamma,
+// gamma_b' = alpha_b gamma_a'):
+//   d_a = beta_a (v_a - gamma_a' Shat.k_a),  o_a = gamma_a' Shat.q_a + d_a (k_a.q_a)
+//   u_b = gamma_a' Shat.k_b + d_a (k_a.k_b), d_b = beta_b (v_b - alpha_b u_b)
+//   o_b = gamma_b' Shat.q_b + alpha_b d_a (k_a.q_b) + d_b (k_b.q_b)
+//   Shat += (d_a / gamma_a') k_a + (d_b / gamma_b') k_b
+// which is the token recurrence applied twice.  When gamma_a' or gamma_b'
+// falls below 2^-32 the pair folds the scale into the state instead:
+// Shat = gamma_b' Shat + alpha_b d_a k_a + d_b k_b, gamma = 1 (no division).
+// An odd tile ends with a pair whose second token is empty (k = q = v = 0,
+// alpha = 1, beta = 0).  The pair scalars depend on alpha alone and are
+// formed once per tile; k.q, k_a.k_b and k_a.q_b by the other warps.
 //
 // CTA = one (sequence, v head), 256 threads = 16 groups, two CTAs per SM;
 // tokens staged 32 at a time with cp.async, double-buffered, k.q formed once
@@ -42,8 +56,9 @@ constexpr int kThreads = 256;
 constexpr int kDK = 128;
 
 __host__ __device__ inline int rec128_buf_floats(int dv) {
-  // one buffer: q, k [TT][dk], per-token scalars float4 [TT], v [TT][dv], alpha, beta, k.q [TT]
-  return kTT * (2 * kDK + 4 + dv) + 3 * kTT;
+  // one buffer: q, k [TT][dk], per-pair scalars float4 [TT] (two per pair),
+  // v [TT][dv], alpha, beta, k.q [TT], per-pair Gram scalars [TT] (two per pair)
+  return kTT * (2 * kDK + 4 + dv) + 4 * kTT;
 }
 __host__ __device__ inline int64_t rec128_smem_bytes(int dv) { return 2 * (int64_t)rec128_buf_floats(dv) * 4; }
 
@@ -84,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent128_kernel(const __grid_
   auto a_s = [&](int b) { return rsm + b * buf_floats + kTT * (2 * kDK + 4 + dv); };
   auto b_s = [&](int b) { return a_s(b) + kTT; };
   auto kq_s = [&](int b) { return a_s(b) + 2 * kTT; };
+  auto gr_s = [&](int b) { return reinterpret_cast<float2 *>(a_s(b) + 3 * kTT); };
 
   const int i = ranked_sequence(p.cu, p.n_seq, s_len, &s_seq);
   const int32_t slot = p.idx[i];
@@ -172,84 +188,145 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent128_kernel(const __grid_
     if (tb + kTT < t1) issue_tile(tb + kTT, bsel ^ 1);
     cp_async_commit();
     cp_async_wait<1>();  // this thread's copies of the current tile have landed
+    const int np = (nt + 1) / 2;  // token pairs; an odd tile ends with a pair whose second token is empty
+    if (nt & 1) {                 // the empty token: k = q = v = 0, alpha = 1, beta = 0
+      for (int e = tid; e < kDK; e += kThreads) {
+        q_s(bsel)[nt * kDK + e] = 0.f;
+        k_s(bsel)[nt * kDK + e] = 0.f;
+      }
+      for (int e = tid; e < dv; e += kThreads) v_s(bsel)[nt * dv + e] = 0.f;
+      if (tid == 0) {
+        a_s(bsel)[nt] = 1.f;
+        b_s(bsel)[nt] = 0.f;
+      }
+    }
     __syncthreads();
     const float *qd = q_s(bsel), *kd = k_s(bsel), *vd = v_s(bsel);
-    float4 *sc = sc_s(bsel);
+    float4 *sp = sc_s(bsel);
+    float2 *gr = gr_s(bsel);
     if (warp == 0) {
-      // per token: {alpha gamma, beta, 1 / gamma', fold}; gamma' = alpha gamma is
-      // folded into the state below 2^-32 (fold = gamma', then gamma' = 1);
-      // fold is NaN when there is none
+      // per pair (tokens a, b): {gamma_a', gamma_b', beta_a, beta_b} and
+      // {alpha_b, e-scale of a, e-scale of b, fold}; gamma_a' = alpha_a gamma,
+      // gamma_b' = alpha_b gamma_a'.  Below 2^-32 the pair folds the scale into
+      // the state (fold = gamma_b', e-scales alpha_b and 1, gamma restarts at 1);
+      // otherwise the e-scales are 1 / gamma_a', 1 / gamma_b' and fold is NaN
       if (lane == 0) {
         const float *al = a_s(bsel), *be = b_s(bsel);
-        for (int tt = 0; tt < nt; ++tt) {
-          const float ag = al[tt] * gam;
-          const bool fold = ag < 0x1p-32f;
-          sc[tt] = make_float4(ag, be[tt], 0.f, fold ? ag : __int_as_float(0x7fffffff));
-          gam = fold ? 1.f : ag;
+        for (int pp = 0; pp < np; ++pp) {
+          const float aa = al[2 * pp], ab = al[2 * pp + 1];
+          const float ga = aa * gam, gb = ab * ga;
+          const bool fold = fminf(ga, gb) < 0x1p-32f;
+          sp[2 * pp] = make_float4(ga, gb, be[2 * pp], be[2 * pp + 1]);
+          sp[2 * pp + 1] = make_float4(ab, fold ? ab : 0.f, 1.f, fold ? gb : __int_as_float(0x7fffffff));
+          gam = fold ? 1.f : gb;
         }
       }
       __syncwarp();
-      if (lane < nt) {
-        const float4 c = sc[lane];
-        sc[lane].z = c.w == c.w ? 1.f : 1.f / c.x;
+      if (lane < np) {
+        const float4 c0 = sp[2 * lane], c1 = sp[2 * lane + 1];
+        if (c1.w != c1.w) {
+          sp[2 * lane + 1].y = 1.f / c0.x;
+          sp[2 * lane + 1].z = 1.f / c0.y;
+        }
       }
     } else {
-      for (int tt = warp - 1; tt < nt; tt += kThreads / 32 - 1) {
-        float acc = 0.f;
-        for (int c = lane; c < kDK; c += 32) acc = fmaf(qd[tt * kDK + c], kd[tt * kDK + c], acc);
+      // k.q of each token, and per pair k_a.k_b and k_a.q_b
+      for (int it = warp - 1; it < nt + np; it += kThreads / 32 - 1) {
+        const bool pair = it >= nt;
+        const int ta = pair ? 2 * (it - nt) : it;
+        const float *x = kd + ta * kDK;
+        const float *y0 = pair ? kd + (ta + 1) * kDK : qd + ta * kDK;
+        const float *y1 = qd + (ta + 1) * kDK;
+        float acc0 = 0.f, acc1 = 0.f;
+        for (int c = lane; c < kDK; c += 32) {
+          acc0 = fmaf(x[c], y0[c], acc0);
+          if (pair) acc1 = fmaf(x[c], y1[c], acc1);
+        }
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (lane == 0) kq_s(bsel)[tt] = acc;
+        for (int m = 16; m >= 1; m >>= 1) {
+          acc0 += __shfl_xor_sync(0xffffffffu, acc0, m);
+          acc1 += __shfl_xor_sync(0xffffffffu, acc1, m);
+        }
+        if (lane == 0) {
+          if (pair) gr[it - nt] = make_float2(acc0, acc1);
+          else kq_s(bsel)[it] = acc0;
+        }
       }
     }
     __syncthreads();
     const float *kq = kq_s(bsel);
     // odd lanes form their q products in the slots of the k products
     const float *x0 = odd ? qd : kd, *x1 = odd ? kd : qd;
-    for (int tt = 0; tt < nt; ++tt) {
-      uint64_t xa[4], xb[4];
-      {
-        const ulonglong2 a0 = *reinterpret_cast<const ulonglong2 *>(x0 + tt * kDK + 4 * lc);
-        const ulonglong2 a1 = *reinterpret_cast<const ulonglong2 *>(x0 + tt * kDK + 64 + 4 * lc);
-        const ulonglong2 b0 = *reinterpret_cast<const ulonglong2 *>(x1 + tt * kDK + 4 * lc);
-        const ulonglong2 b1 = *reinterpret_cast<const ulonglong2 *>(x1 + tt * kDK + 64 + 4 * lc);
-        xa[0] = a0.x; xa[1] = a0.y; xa[2] = a1.x; xa[3] = a1.y;
-        xb[0] = b0.x; xb[1] = b0.y; xb[2] = b1.x; xb[3] = b1.y;
-      }
-      float v16v[16];  // local index 2 slot + {0: xa, 1: xb}
+    auto load_x = [&](int tt, uint64_t *xa, uint64_t *xb) {
+      const ulonglong2 a0 = *reinterpret_cast<const ulonglong2 *>(x0 + tt * kDK + 4 * lc);
+      const ulonglong2 a1 = *reinterpret_cast<const ulonglong2 *>(x0 + tt * kDK + 64 + 4 * lc);
+      const ulonglong2 b0 = *reinterpret_cast<const ulonglong2 *>(x1 + tt * kDK + 4 * lc);
+      const ulonglong2 b1 = *reinterpret_cast<const ulonglong2 *>(x1 + tt * kDK + 64 + 4 * lc);
+      xa[0] = a0.x; xa[1] = a0.y; xa[2] = a1.x; xa[3] = a1.y;
+      xb[0] = b0.x; xb[1] = b0.y; xb[2] = b1.x; xb[3] = b1.y;
+    };
+    for (int pp = 0; pp < np; ++pp) {
+      const int ta = 2 * pp, tb2 = ta + 1;
+      uint64_t xaa[4], xba[4], xab[4], xbb[4];  // tokens a and b: slot products xa / xb
+      load_x(ta, xaa, xba);
+      load_x(tb2, xab, xbb);
+      // both tokens' dot products with the state before the pair
+      float va[16], vb[16];  // local index 2 slot + {0: xa, 1: xb}
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        v16v[2 * r] = dot8(S[r], xa);
-        v16v[2 * r + 1] = dot8(S[r], xb);
+        va[2 * r] = dot8(S[r], xaa);
+        va[2 * r + 1] = dot8(S[r], xba);
+        vb[2 * r] = dot8(S[r], xab);
+        vb[2 * r + 1] = dot8(S[r], xbb);
       }
-      float v8[8], v4[4], v2[2], v1[1];
-      reduce_half<16>(v16v, v8, 8);
-      reduce_half<8>(v8, v4, 4);
-      reduce_half<4>(v4, v2, 2);
-      reduce_half<2>(v2, v1, 1);
-      // even lanes hold u-hat of my_row, odd lanes w-hat
-      const float4 c = sc[tt];  // alpha gamma, beta, 1 / gamma', fold
-      const float vr = my_row < dv ? vd[tt * dv + my_row] : 0.f;
-      const float d = c.y * (vr - c.x * v1[0]);                // meaningful on even lanes
-      const float d_row = __shfl_xor_sync(0xffffffffu, d, 1);  // odd lanes: their row's d
-      if (odd && my_row < dv) p.out[((int64_t)(tb + tt) * p.Hv + h) * dv + my_row] = fmaf(c.x, v1[0], d_row * kq[tt]);
-      if (c.w == c.w) {  // fold the scale into Shat (uniform over the CTA)
-        const uint64_t g2 = f2_pack(c.w, c.w);
+      float a8[8], a4[4], a2[2], a1[1], b8[8], b4[4], b2[2], b1[1];
+      reduce_half<16>(va, a8, 8);
+      reduce_half<16>(vb, b8, 8);
+      reduce_half<8>(a8, a4, 4);
+      reduce_half<8>(b8, b4, 4);
+      reduce_half<4>(a4, a2, 2);
+      reduce_half<4>(b4, b2, 2);
+      reduce_half<2>(a2, a1, 1);
+      reduce_half<2>(b2, b1, 1);
+      // even lanes: u-hat of my_row for a and b (b against the old state);
+      // odd lanes: the w-hats
+      const float4 c0 = sp[2 * pp], c1 = sp[2 * pp + 1];
+      const float2 g = gr[pp];  // k_a.k_b, k_a.q_b
+      const float vra = my_row < dv ? vd[ta * dv + my_row] : 0.f;
+      const float vrb = my_row < dv ? vd[tb2 * dv + my_row] : 0.f;
+      const float da = c0.z * (vra - c0.x * a1[0]);
+      const float ub = fmaf(c0.x, b1[0], da * g.x);  // token b's prediction after a's update
+      const float db = c0.w * (vrb - c1.x * ub);
+      const float da_row = __shfl_xor_sync(0xffffffffu, da, 1);  // odd lanes: their row's d's
+      const float db_row = __shfl_xor_sync(0xffffffffu, db, 1);
+      if (odd && my_row < dv) {
+        float *o = p.out + ((int64_t)(tb + ta) * p.Hv + h) * dv + my_row;
+        o[0] = fmaf(c0.x, a1[0], da_row * kq[ta]);
+        if (tb2 < nt)
+          o[(int64_t)p.Hv * dv] = fmaf(c0.y, b1[0], fmaf(c1.x * da_row, g.y, db_row * kq[tb2]));
+      }
+      if (c1.w == c1.w) {  // fold the scale into Shat (uniform over the CTA)
+        const uint64_t g2 = f2_pack(c1.w, c1.w);
 #pragma unroll
         for (int r = 0; r < 8; ++r)
 #pragma unroll
           for (int q = 0; q < 4; ++q) S[r][q] = f2_mul(S[r][q], g2);
       }
-      const float e = d * c.z;  // d / gamma'
-      uint64_t kr[4];           // k for the update
+      const float ea = da * c1.y, eb = db * c1.z;
+      uint64_t ka[4], kb[4];  // k of tokens a and b
 #pragma unroll
-      for (int q = 0; q < 4; ++q) kr[q] = odd ? xb[q] : xa[q];
+      for (int q = 0; q < 4; ++q) {
+        ka[q] = odd ? xba[q] : xaa[q];
+        kb[q] = odd ? xbb[q] : xab[q];
+      }
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        const float er = __shfl_sync(0xffffffffu, e, gbase + 2 * (r ^ rb));  // slot r's row
-        const uint64_t e2 = f2_pack(er, er);
+        const int src = gbase + 2 * (r ^ rb);  // the lane holding slot r's row
+        const float era = __shfl_sync(0xffffffffu, ea, src);
+        const float erb = __shfl_sync(0xffffffffu, eb, src);
+        const uint64_t ea2 = f2_pack(era, era), eb2 = f2_pack(erb, erb);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) S[r][q] = f2_fma(e2, kr[q], S[r][q]);
+        for (int q = 0; q < 4; ++q) S[r][q] = f2_fma(eb2, kb[q], f2_fma(ea2, ka[q], S[r][q]));
       }
     }
     __syncthreads();  // the next iteration refills this buffer
