@@ -1,6 +1,7 @@
 // lsc_ptx.h -- inline-PTX helpers of liblsc for sm_103a: 1-D TMA bulk copies
-// (cp.async.bulk), shared-memory mbarriers with bounded waits, proxy fences and
-// cluster barriers.  No multicast, no tensor maps.
+// (cp.async.bulk) with L2 cache policies, shared-memory mbarriers with bounded
+// waits, proxy fences, cp.async and programmatic dependent launch.  No
+// clusters, no multicast, no tensor maps.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -124,11 +125,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Cluster-wide barrier without a release fence: orders execution only.
-__device__ __forceinline__ void cluster_barrier_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // Programmatic dependent launch.  A kernel launched with programmatic stream

@@ -212,9 +212,9 @@ def test_gather_scatter_out_of_range_index_sets_status(lsc):
 DECODE_CASES = [
     ("c0", {}), ("c0p", {}), ("s1", {}), ("s2", {}), ("s3", {}), ("s4", {}),
     ("s4", {"conv_width": 2}), ("c0", {"conv_width": 8}),
-    # eight v heads share one q/k head: a cluster of eight CTAs
+    # eight v heads share one q/k head: one work item holds all eight
     ("c0", {"num_v_heads": 8, "conv_dim": 2 * 16 + 8 * 16}),
-    # Hk = Hv: clusters of one
+    # Hk = Hv: one v head per work item
     ("s1", {"num_k_heads": 4, "conv_dim": 2 * 4 * 32 + 4 * 32}),
     # dk = 64 with fp32 state
     ("s3", {"head_k_dim": 64, "head_v_dim": 96, "conv_dim": 2 * 2 * 64 + 4 * 96}),
