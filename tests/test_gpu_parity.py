@@ -539,6 +539,24 @@ def test_recurrent_bad_rows_are_skipped_and_reported(lsc, algo):
         check_recurrent(w, P, l, pre, ref, has, cu, q, k, v, a, b, out)
 
 
+@pytest.mark.parametrize("algo", list(REC_ALGOS))
+def test_recurrent_null_has_init_means_all_warm(lsc, algo):
+    """has_init = NULL: every sequence starts from its slot's state."""
+    w = workload("s3")
+    with DevPool(w, seed=18) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, cu, q, k, v, a, b = rec_case(w, [17, 5, 40], seed=12, pad_seq=False)
+        T = int(cu[-1])
+        out = torch.full((T, w.num_v_heads, w.head_v_dim), float("nan"), device="cuda")
+        t = [dev(z) for z in (idx, cu, q, k, v, a, b)]
+        args = L.recurrent_args(len(idx), w.num_k_heads, T, t[0], None, *t[1:], out, algorithm=REC_ALGOS[algo])
+        assert L.lsc_gdn_recurrent(P.pool, l, args, torch.cuda.current_stream()) == L.LSC_OK
+        torch.cuda.synchronize()
+        has[:] = 1
+        check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out.cpu().numpy())
+
+
 def test_recurrent_rejects(lsc):
     w = workload("s1")
     with DevPool(w) as P:

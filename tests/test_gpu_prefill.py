@@ -121,6 +121,31 @@ def test_prefill_conv_other_widths(lsc, name, width, x_offset):
         assert P.status() == L.LSC_OK
 
 
+@pytest.mark.parametrize("x_offset", [0, 1], ids=["aligned", "x-off-16B"])
+def test_prefill_null_has_init_means_all_warm(lsc, x_offset):
+    """has_init = NULL: every sequence's window starts from its slot's conv state."""
+    w = shape("s3")
+    x_offset *= W.ESIZE[w.conv_dtype]
+    lengths = [1, 2, 70, 5]
+    with DevPool(w, seed=23, random_padding=True) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, cu, xr, cwr = inputs(w, lengths, seed=6, pad=False)
+        T = int(cu[-1])
+        q = torch.full((T, w.num_k_heads, w.head_k_dim), float("nan"), device="cuda")
+        k = torch.full_like(q, float("nan"))
+        v = torch.full((T, w.num_v_heads, w.head_v_dim), float("nan"), device="cuda")
+        xbuf = torch.zeros(xr.size + x_offset, dtype=torch.uint8, device="cuda")
+        xbuf[x_offset:] = dev(xr.reshape(-1))
+        args = L.prefill_conv_args(len(idx), w.num_k_heads, T, dev(idx), None, dev(cu), xbuf[x_offset:],
+                                   dev(cwr.reshape(-1)), q, k, v)
+        assert L.lsc_gdn_prefill_conv(P.pool, l, args, torch.cuda.current_stream()) == L.LSC_OK
+        torch.cuda.synchronize()
+        has[:] = 1
+        check(w, P, l, pre, idx, has, cu, xr, cwr, q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy())
+        assert P.status() == L.LSC_OK
+
+
 def test_prefill_then_decode_continues(lsc):
     """After a prefill the slot's conv state is the one a decode continues from:
     prefill of T tokens then one decode token equals the oracle doing the same."""
