@@ -71,3 +71,23 @@ def test_recurrent_random_shape(lsc, kw, algo):
         assert rc == L.LSC_OK, L.lsc_error_string(rc)
         check_recurrent(w, P, l, pre, idx, has, cu, q, k, v, a, b, out)
         assert P.status() == L.LSC_OK
+
+
+@pytest.mark.parametrize("x_offset", [0, 1], ids=["aligned", "x-off-16B"])
+@pytest.mark.parametrize("kw", SHAPES, ids=[_id(k) for k in SHAPES])
+def test_prefill_conv_random_shape(lsc, kw, x_offset):
+    """The fused 8-channel path where the shape allows it (channel counts and
+    head dims that are multiples of 8, dk/8 a power of two), the two-pass path
+    otherwise or with x off a 16-byte boundary."""
+    from test_gpu_prefill import check, inputs, run
+    w = workload("s1", **kw)
+    x_offset *= W.ESIZE[w.conv_dtype]
+    lengths = [0, 1, w.conv_width - 1, w.conv_width, 70, 9]
+    with DevPool(w, seed=35, random_padding=True) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, cu, xr, cwr = inputs(w, lengths, seed=36)
+        rc, q, k, v = run(P, l, w, idx, has, cu, xr, cwr, x_offset)
+        assert rc == L.LSC_OK, L.lsc_error_string(rc)
+        check(w, P, l, pre, idx, has, cu, xr, cwr, q, k, v)
+        assert P.status() == L.LSC_OK
