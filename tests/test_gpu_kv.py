@@ -125,3 +125,33 @@ def test_copy_prefix_full_size_sampled(lsc):
     assert torch.equal(pages[:, :, untouched], keep)
     assert nbytes == sum(nt) * row * 2 * 12
     assert L.lsc_kv_pool_destroy(pool) == L.LSC_OK
+
+
+def random_kv_shapes(seed, n):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        out.append((int(rng.integers(1, 4)), int(rng.integers(8, 40)), int(rng.choice([1, 2, 3, 8, 16, 64])),
+                    int(rng.integers(1, 5)), int(rng.choice([3, 8, 16, 64, 128, 256])),
+                    int(rng.choice([L.LSC_BF16, L.LSC_F32, L.LSC_F16])), 16 * int(rng.integers(0, 9))))
+    return out
+
+
+KV_RANDOM = random_kv_shapes(2027, 12)
+
+
+@pytest.mark.parametrize("shape", KV_RANDOM,
+                         ids=["L{}-B{}-bt{}-h{}-d{}-t{}-pad{}".format(*s) for s in KV_RANDOM])
+def test_copy_prefix_random_shape(lsc, shape):
+    """Seeded random pools (layers, blocks, block tokens, kv heads, head dims,
+    dtypes, page padding): every byte equals the oracle's after the copy."""
+    kv = DevKv(*shape, seed=5)
+    rng = np.random.default_rng(6)
+    src, dst, nt = random_ops(rng, shape[1], shape[2], min(8, shape[1] // 2))
+    rc, _ = L.lsc_copy_prefix(kv.pool, L.kv_ops(src, dst, nt), torch.cuda.current_stream())
+    assert rc == L.LSC_OK
+    torch.cuda.synchronize()
+    rc_o, want = kv.oracle_copy(src, dst, nt)
+    assert rc_o == oracle.OK
+    np.testing.assert_array_equal(kv.buf.cpu().numpy(), want)
+    kv.close()
