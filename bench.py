@@ -546,7 +546,7 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
         rec[algo] = timed(lambda: rec_all(ra), 2)
     t, t_ch = rec[L.LSC_RECURRENT_TOKEN], rec[L.LSC_RECURRENT_CHUNKED]
     parts["recurrent_c4"] = {"workload": f"c4: 64 sequences, {T} tokens, 36 layers, state [32,128,128] f32",
-                             "kernel": "recurrent128_kernel<f32> (token by token, the default)",
+                             "kernel": "recurrent128_kernel<f32> (token order, two tokens per pass over the state; the default)",
                              "ms_per_36_layers": round(t * 1e3, 3),
                              "token_layers_per_s": round(T * nl / t, 1),
                              "TFLOP/s": round(flops / t / 1e12, 2),
@@ -858,7 +858,7 @@ NCU_CASES = {
     "decode_bf16": ("c2", 256, "decode"),    # bf16 state, 256 rows, 571 MB per launch
     "restore": ("c1", 64, "restore"),        # 64 hits x 2 layers, 549 MB per launch
     "restore_c3": ("c3", 512, "restore"),    # the c3 storm on 2 of its 36 layers (4.4 GB pool, 1.76 GB algorithmic)
-    "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer (token by token)
+    "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer (token order)
     "recurrent_chunked": ("c4", 16, "recurrent_chunked"),  # the same, 16-token chunks
     "prefill": ("c4", 32, "prefill"),        # prefill conv: 32 sequences of 64..2048 tokens, one layer
     "copy_prefix": ("c1", 4, "copy_prefix"), # K/V copy: 12 layers x 512 blocks of 64 KiB, 4 prefixes of 32 blocks
