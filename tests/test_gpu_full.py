@@ -10,7 +10,7 @@ import oracle
 from linear_attention_state_lsc_gb300 import lsc as L
 from linear_attention_state_lsc_gb300 import workloads as W
 
-from _gpu import DevPool, conv_bytes_dev, dev, tol
+from _gpu import DevPool, dev, tol
 from _util import oracle_layout, oracle_pool
 from test_gpu_parity import check_decode, run_decode, run_restore
 

@@ -5,8 +5,6 @@ base address that is never dereferenced.
 
 Sources: vLLM-Ascend "非连续 KV Cache" §3, §3.4; Kapitsa figure 2.
 """
-import numpy as np
-import pytest
 
 import oracle
 from linear_attention_state_lsc_gb300 import lsc as L

@@ -5,7 +5,6 @@ of copy_prefix with every other byte unchanged, a whole prefix copied block by
 block read back as token rows, and the rejections.  CPU only.
 """
 import numpy as np
-import pytest
 
 import oracle
 

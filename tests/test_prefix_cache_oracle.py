@@ -9,7 +9,7 @@ import random
 
 import pytest
 
-from oracle.prefix_cache import CHECKPOINT, FREE, LIVE, RESERVED, PrefixCache, PrefixCacheError
+from oracle.prefix_cache import CHECKPOINT, LIVE, RESERVED, PrefixCache, PrefixCacheError
 
 from _util import golden_kv
 
