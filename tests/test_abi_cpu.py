@@ -302,3 +302,25 @@ def test_headers_compile_as_c_and_link(tmp_path):
     # 1 GDN layer x 4 slots x 128 B, as the library reports it through Python too
     desc = L.make_pool_desc([L.LSC_LAYER_GDN, L.LSC_LAYER_ATTENTION], 4, 16, 4, L.LSC_BF16, 1, 2, 2, L.LSC_F32, 128)
     assert int(run.stdout) == L.lsc_pool_required_bytes(desc)
+
+
+def test_algorithmic_bytes_of_the_bench(lsc):
+    """The byte counts bench.py divides by (roofline 'achieved') against the
+    per-unit figures derived from the workload shapes: c1 restore = 2 payloads
+    per (hit row, GDN layer) = 2 x 2 146 304 B; a decode row = state read and
+    written + x + alpha, beta + out + idx + has_init, plus the conv weights once
+    per launch (c2: 2 228 485 B per row, 65 536 B of weights)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    views = {}
+    for name in ("c1", "c2"):
+        w = W.get(name)
+        rc, pool = L.lsc_pool_create(lib_desc(w), FAKE_BASE, 1 << 44)
+        assert rc == L.LSC_OK
+        views[name] = (w, L.lsc_pool_layer_view(pool, w.gdn_layers[0])[1])
+        L.lsc_pool_destroy(pool)
+    w1, v1 = views["c1"]
+    assert bench.restore_bytes(v1, 64, 36, 64) == 64 * 36 * 4_292_608 + 64          # 9.890 GB per serving-step restore
+    assert bench.decode_bytes(v1, w1, 64) == 64 * 4_325_637 + 65_536               # 276.9 MB per serving-step decode
+    w2, v2 = views["c2"]
+    assert bench.decode_bytes(v2, w2, 256) == 256 * 2_228_485 + 65_536              # 570.56 MB per c2 decode launch
