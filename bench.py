@@ -34,7 +34,7 @@ FALLBACK_HBM = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["lsc", "reference"], default="lsc")
     ap.add_argument("--no-parts", action="store_true", help="headline step only")
@@ -77,7 +77,7 @@ def whole_job_rate(world, units_per_rank, elapsed):
 # ---------------------------------------------------------------- clocks
 
 class Clocks:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -85,6 +85,7 @@ class Clocks:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.window = None  # (start, end) host time.time() of the timed region
 
     def start(self):
         try:
@@ -92,36 +93,56 @@ class Clocks:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark(self, t_start, t_end):
+        self.window = (t_start, t_end)
+
+    @staticmethod
+    def _ts(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
 
     def stop(self):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         self.proc.wait()
-        sm, mx, reasons = [], [], set()
+        samples = []  # (time, sm, max, reasons)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                sm, mx = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
+            samples.append((self._ts(f[0]), sm, mx, {n for n, v in zip(names, f[6:10]) if v.lower() == "active"}))
         os.unlink(self.path)
-        if not sm:
+        if not samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        timed = []
+        if self.window:
+            a, b = self.window
+            timed = [x for x in samples if x[0] is not None and a <= x[0] <= b]
+        top = max(x[1] for x in samples)
+        loaded = [x for x in samples if x[1] >= 0.5 * top] or samples
+        use = timed or loaded
+        reasons = set().union(*(x[3] for x in use))
+        return {"sm_mhz": statistics.median(x[1] for x in use), "sm_max_mhz": max(x[2] for x in samples),
+                "reasons": sorted(reasons), "samples": len(samples), "samples_in_timed_region": len(timed),
+                "sm_mhz_basis": "median of the samples inside the timed region" if timed else
+                                "median of the samples under load (none fell inside the timed region)",
+                "sample_period_ms": 50}
 
 
 # ---------------------------------------------------------------- pools
@@ -265,16 +286,18 @@ def run_lsc(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    wall0 = time.time()
     t0.record(fwd)
     for i in range(args.steps):
         step(i)
     t1.record(fwd)
     torch.cuda.synchronize()
+    clocks.mark(wall0, time.time())
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     ck = clocks.stop()
-    ck["window"] = "warm-up + timed region + trailing untimed steps"
+    ck["window"] = "sampler ran over the warm-up, the timed region and trailing untimed steps"
     elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, "cuda")
     if world > 1:
         dist.barrier()
@@ -495,6 +518,40 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     del buf
     torch.cuda.empty_cache()
 
+    # standalone gather and scatter on c2's pool: 256 rows, bf16 ssm, dense
+    # conv [256, 8192, 3] bf16 (12.6 MB) and ssm [256, 32, 128, 128] bf16 (268 MB)
+    w = W.get("c2")
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    v = views[w.gdn_layers[0]]
+    n = 256
+    idx = torch.from_numpy(np.random.default_rng(1).permutation(w.num_slots).astype(np.int32)).cuda()
+    conv_d = torch.empty((n, v.conv_bytes), dtype=torch.uint8, device="cuda")
+    ssm_d = torch.empty((n, v.ssm_bytes), dtype=torch.uint8, device="cuda")
+    i_l = [0]
+
+    def gather_one():
+        i_l[0] += 1
+        l = w.gdn_layers[i_l[0] % len(w.gdn_layers)]
+        assert L.lsc_gather(pool, l, idx, None, n, conv_d, ssm_d, fwd) == L.LSC_OK
+
+    def scatter_one():
+        i_l[0] += 1
+        l = w.gdn_layers[i_l[0] % len(w.gdn_layers)]
+        assert L.lsc_scatter(pool, l, idx, n, conv_d, ssm_d, fwd) == L.LSC_OK
+
+    gs_bytes = 2 * n * (v.conv_bytes + v.ssm_bytes)
+    for name, fn, kern in (("gather_c2", gather_one, "gather_kernel"), ("scatter_c2", scatter_one, "scatter_kernel")):
+        t = timed(fn, 36)
+        parts[name] = {"workload": "c2 pool: 256 rows (a permutation of the 256 slots), conv [8192,3] bf16 + ssm "
+                                   "[32,128,128] bf16 per row, one GDN layer per launch, layers in turn",
+                       "kernel": kern, "launch_ms": round(t * 1e3, 4), "bytes_per_launch": gs_bytes,
+                       "GB/s": round(gs_bytes / t / 1e9, 1), "frac": round(gs_bytes / t / 1e9 / hbm_peak, 4),
+                       "rows_per_s": round(n / t, 1), "bytes_basis": "conv + ssm views read and written per row",
+                       "traffic": kernel_traffic(kern)}
+    L.lsc_pool_destroy(pool)
+    del buf, conv_d, ssm_d
+    torch.cuda.empty_cache()
+
     # restore storm
     w = W.get("c3")
     rows = W.restore_rows("c3")
@@ -516,6 +573,14 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
                            "kernel": "restore_kernel", "launch_ms": round(t * 1e3, 4), "bytes_per_launch": bytes_,
                            "GB/s": round(bytes_ / t / 1e9, 1), "frac": round(bytes_ / t / 1e9 / hbm_peak, 4),
                            "rows_per_s": round(512 / t, 1), "traffic": kernel_traffic("restore_kernel c3")}
+    tr = parts["restore_c3"]["traffic"]
+    parts["restore_c3"]["frac_basis"] = ("algorithmic: every hit's read counted, though the hot source's re-reads "
+                                         "hit L2, so frac can exceed 1")
+    parts["restore_c3"]["dram_frac"] = round(tr / t / 1e9 / hbm_peak, 4) if tr else None
+    parts["restore_c3"]["dram_frac_basis"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch / launch "
+                                              "time / peak; a lower bound, since lines still dirty in L2 when the "
+                                              "kernel ends are not counted; null when the kernel changed since the "
+                                              "counters were taken")
     L.lsc_pool_destroy(pool)
     del buf, hs
     torch.cuda.empty_cache()
@@ -553,7 +618,9 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
                              "roofline": {"bound": "alu", "peak_TFLOP/s": round(fp32_peak / 1e12, 1),
                                           "frac": round(flops / t / fp32_peak, 4),
                                           "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 flop x 2070 MHz"},
-                             "flops_basis": "6 dk dv per (token, head): S k, the rank-1 update, S q",
+                             "flops_basis": "6 dk dv per (token, head): S k, the rank-1 update, S q; "
+                                            "frac_7dkdv counts 7 dk dv (with the decay of S)",
+                             "frac_7dkdv": round(flops * 7 / 6 / t / fp32_peak, 4),
                              "chunked": {"kernel": "recurrent_chunked_kernel<f32> (16-token chunks)",
                                          "ms_per_36_layers": round(t_ch * 1e3, 3),
                                          "frac": round(flops / t_ch / fp32_peak, 4)}}

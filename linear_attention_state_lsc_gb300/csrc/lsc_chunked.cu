@@ -400,14 +400,10 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_chunked_kernel(const __
 template <typename TS>
 int launch_chunked_t(const RecurrentParams &p, cudaStream_t s) {
   const int64_t smem = chunk_smem_bytes(p.dv);
-  static int configured = 0;
-  if (configured < smem) {
-    if (cudaFuncSetAttribute(recurrent_chunked_kernel<TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return LSC_ERR_UNSUPPORTED;
-    }
-    configured = (int)smem;
+  static SmemLimit limit;  // per instantiation and device
+  if (limit.ensure((const void *)recurrent_chunked_kernel<TS>, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return LSC_ERR_UNSUPPORTED;
   }
   recurrent_chunked_kernel<TS><<<dim3(p.Hv, p.n_seq, 1), kThreads, (size_t)smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;

@@ -189,14 +189,17 @@ int blocks_per_sm(const void *kernel) {
   return b;
 }
 
+// resident CTAs per SM of each copy kernel, per device
+PerDeviceInt g_bps_restore, g_bps_gather, g_bps_scatter, g_bps_kv;
+
 int grid_for(const void *kernel, int num_sms, int64_t units) {
-  static int cached[4] = {0, 0, 0, 0};
-  const int slot = kernel == (const void *)restore_kernel  ? 0
-                   : kernel == (const void *)gather_kernel ? 1
-                   : kernel == (const void *)kv_copy_kernel ? 3
-                                                            : 2;
-  if (!cached[slot]) cached[slot] = blocks_per_sm(kernel);
-  int64_t g = (int64_t)num_sms * cached[slot];
+  PerDeviceInt &rec = kernel == (const void *)restore_kernel  ? g_bps_restore
+                      : kernel == (const void *)gather_kernel ? g_bps_gather
+                      : kernel == (const void *)kv_copy_kernel ? g_bps_kv
+                                                               : g_bps_scatter;
+  int bps = rec.get([kernel](int) { return blocks_per_sm(kernel); });
+  if (bps < 1) bps = 1;
+  int64_t g = (int64_t)num_sms * bps;
   if (units < g) g = units;
   return (int)(g < 1 ? 1 : g);
 }

@@ -533,15 +533,17 @@ template <int DK, typename TS, typename TC, int CW>
 int launch_decode_t(const DecodeParams &p0, cudaStream_t stream) {
   DecodeParams p = p0;
   const int esc = (int)sizeof(TC);
-  static int optin = 0;  // per process: the opt-in shared-memory limit of a block
-  if (!optin) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+  // the opt-in shared-memory limit of a block, per device
+  static PerDeviceInt optin_limit;
+  const int optin = optin_limit.get([](int dev) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
       cudaGetLastError();
-      return LSC_ERR_CUDA;
+      return 0;
     }
-  }
+    return v;
+  });
+  if (optin <= 0) return LSC_ERR_CUDA;
   const DecodeGeom probe(DK, (int)sizeof(TS), p.dv, p.group, p.conv_width, esc, 0);
   const int64_t fixed = probe.total + 1024;  // conv, y and item buffers, static shared memory
   int64_t ns = (optin - fixed) / probe.stage_stride;
@@ -549,14 +551,10 @@ int launch_decode_t(const DecodeParams &p0, cudaStream_t stream) {
   if (ns < 2) return LSC_ERR_UNSUPPORTED;
   p.stages = (int)ns;
   const DecodeGeom D(DK, (int)sizeof(TS), p.dv, p.group, p.conv_width, esc, p.stages);
-  static int configured = 0;  // per instantiation
-  if (configured < D.total) {
-    if (cudaFuncSetAttribute(decode_kernel<DK, TS, TC, CW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)D.total) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return LSC_ERR_UNSUPPORTED;
-    }
-    configured = (int)D.total;
+  static SmemLimit limit;  // per instantiation and device
+  if (limit.ensure((const void *)decode_kernel<DK, TS, TC, CW>, (int)D.total) != cudaSuccess) {
+    cudaGetLastError();
+    return LSC_ERR_UNSUPPORTED;
   }
   // one CTA per SM; rows are split into launches so that no CTA holds more than
   // kDecodeMaxItems items

@@ -268,14 +268,10 @@ int launch_recurrent_t(const RecurrentParams &p, cudaStream_t s) {
   using R = RecShape<DK>;
   if ((p.dv + 1) / 2 * R::TPR > kRecThreads) return LSC_ERR_UNSUPPORTED;
   const int64_t smem = rec_smem_bytes(DK, p.dv);
-  static int configured = 0;
-  if (configured < smem) {
-    if (cudaFuncSetAttribute(recurrent_kernel<DK, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return LSC_ERR_UNSUPPORTED;
-    }
-    configured = (int)smem;
+  static SmemLimit limit;  // per instantiation and device
+  if (limit.ensure((const void *)recurrent_kernel<DK, TS>, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return LSC_ERR_UNSUPPORTED;
   }
   recurrent_kernel<DK, TS><<<dim3(p.Hv, p.n_seq, 1), kRecThreads, (size_t)smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;

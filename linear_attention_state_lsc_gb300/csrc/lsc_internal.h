@@ -5,6 +5,9 @@
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "lsc.h"
 
 namespace lsc {
@@ -18,6 +21,65 @@ struct TraceRange {
   ~TraceRange() { nvtxRangePop(); }
   TraceRange(const TraceRange &) = delete;
   TraceRange &operator=(const TraceRange &) = delete;
+};
+
+// ---- per-device launch state -------------------------------------------------
+// A kernel's dynamic shared-memory limit (cudaFuncSetAttribute) and figures
+// such as its occupancy belong to the device that is current at the call, and
+// pools on different devices -- or several streams of one device -- may be
+// driven from several host threads at once.  These records hold such values
+// per device ordinal, read lock-free and written under a mutex.
+constexpr int kMaxDevices = 64;
+
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`, once per device (the limit only ever grows, so a launch that
+// checked it never sees it lowered by another thread).
+class SmemLimit {
+ public:
+  cudaError_t ensure(const void *fn, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (set_[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (set_[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) set_[dev].store(bytes, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::atomic<int> set_[kMaxDevices] = {};
+  std::mutex mu_;
+};
+
+// A positive integer computed once per device (on the device current at the
+// first call from that device).  get() returns 0 when the current device
+// cannot be read or `compute` returns a value below 1.
+class PerDeviceInt {
+ public:
+  template <typename F>
+  int get(F compute) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return compute(dev);
+    int v = val_[dev].load(std::memory_order_acquire);
+    if (v > 0) return v;
+    std::lock_guard<std::mutex> lock(mu_);
+    v = val_[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    v = compute(dev);
+    if (v > 0) val_[dev].store(v, std::memory_order_release);
+    return v > 0 ? v : 0;
+  }
+
+ private:
+  std::atomic<int> val_[kMaxDevices] = {};
+  std::mutex mu_;
 };
 
 // Byte geometry of one GDN layer region; the same for every GDN layer.

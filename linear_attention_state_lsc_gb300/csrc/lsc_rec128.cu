@@ -361,14 +361,10 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent128_kernel(const __grid_
 template <typename TS>
 int launch_rec128_t(const RecurrentParams &p, cudaStream_t s) {
   const int64_t smem = rec128_smem_bytes(p.dv);
-  static int configured = 0;
-  if (configured < smem) {
-    if (cudaFuncSetAttribute(recurrent128_kernel<TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return LSC_ERR_UNSUPPORTED;
-    }
-    configured = (int)smem;
+  static SmemLimit limit;  // per instantiation and device
+  if (limit.ensure((const void *)recurrent128_kernel<TS>, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return LSC_ERR_UNSUPPORTED;
   }
   recurrent128_kernel<TS><<<dim3(p.Hv, p.n_seq, 1), kThreads, (size_t)smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;

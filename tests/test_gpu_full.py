@@ -109,3 +109,70 @@ def test_c4_resume_prefill_sampled_sequences(lsc, algorithm):
         unsel = sorted(set(range(w.num_slots)) - set(idx.tolist()))
         np.testing.assert_array_equal(got[unsel], pre.reshape(w.num_slots, -1)[unsel])
         assert P.status() == L.LSC_OK
+
+
+def test_c1_serving_step_back_to_back(lsc):
+    """The benchmarked step as the benchmark issues it: lsc_restore of the 64
+    c1 rows on a prepare stream, an event, then 36 lsc_gdn_decode launches back
+    to back on the forward stream with no host sync, then a second token (36
+    more launches).  Hit rows, has_initial_state, both tokens' outputs and the
+    final states of three sampled layers against the oracle."""
+    w = W.get("c1")
+    rows = W.restore_rows("c1")
+    n = len(rows.live)
+    with DevPool(w, seed=0, device_fill=True) as P:
+        sample = [P.gdn_layers[g] for g in (0, 17, 35)]
+        pre = {l: P.download(l) for l in sample}
+        inputs = {}  # (token, layer) -> x, conv weights, alpha, beta (float32, host)
+        for tok in range(2):
+            for l in P.gdn_layers:
+                x, cw, a, b = W.decode_inputs(w, n, seed=tok, layer=l)
+                inputs[tok, l] = (x, cw, a, b)
+        bf = torch.bfloat16
+        idx = dev(rows.live.astype(np.int32))
+        hs = dev(rows.hs_prefill)
+        dx = {k: torch.from_numpy(v[0]).to(bf).cuda() for k, v in inputs.items()}
+        dw = {l: torch.from_numpy(inputs[0, l][1]).to(bf).cuda() for l in P.gdn_layers}
+        da = {k: dev(v[2]) for k, v in inputs.items()}
+        db = {k: dev(v[3]) for k, v in inputs.items()}
+        out = {k: torch.full((n, w.num_v_heads, w.head_v_dim), float("nan"), device="cuda") for k in inputs}
+        ops = L.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
+        prep, fwd = torch.cuda.Stream(), torch.cuda.current_stream()
+        ev = torch.cuda.Event()
+        ev.record(fwd)
+        torch.cuda.synchronize()
+        prep.wait_stream(fwd)
+        rc, rep = L.lsc_restore(P.pool, ops, rows.nkv, rows.block_size, rows.initialized, hs, prep, ev)
+        assert rc == L.LSC_OK and rep.n_hit == 64 and rep.launches == 1
+        fwd.wait_event(ev)
+        for tok in range(2):
+            for l in P.gdn_layers:
+                args = L.decode_args(n, w.num_k_heads, idx, hs, dx[tok, l], dw[l], da[tok, l], db[tok, l],
+                                     out[tok, l])
+                assert L.lsc_gdn_decode(P.pool, l, args, fwd) == L.LSC_OK
+        torch.cuda.synchronize()
+        hs_o = rows.hs_prefill.copy()
+        Lo = oracle_layout(w)
+        t = tol(w.ssm_dtype)
+        for l in sample:
+            reg = pre[l].copy()
+            h = rows.hs_prefill.copy()
+            assert oracle.restore(_one_layer_pool(w), {0: reg}, rows.live, rows.src, rows.nkv, rows.block_size,
+                                  rows.initialized, h) == oracle.OK
+            hs_o = h
+            for tok in range(2):
+                x, cw, a, b = inputs[tok, l]
+                rc, o = oracle.gdn_decode(oracle_pool(w), reg, rows.live, h, W.to_dtype_bytes(x, w.conv_dtype),
+                                          W.to_dtype_bytes(inputs[0, l][1], w.conv_dtype), w.num_k_heads, a, b)
+                assert rc == oracle.OK
+                np.testing.assert_allclose(out[tok, l].cpu().numpy(), o, **t)
+            got = P.download(l).reshape(w.num_slots, -1)
+            exp = reg.reshape(w.num_slots, -1)
+            np.testing.assert_array_equal(got[:, :Lo["conv_bytes"]], exp[:, :Lo["conv_bytes"]])
+            ssm = slice(Lo["ssm_offset"], Lo["ssm_offset"] + Lo["ssm_bytes"])
+            np.testing.assert_allclose(W.from_dtype_bytes(np.ascontiguousarray(got[:, ssm]), w.ssm_dtype),
+                                       W.from_dtype_bytes(np.ascontiguousarray(exp[:, ssm]), w.ssm_dtype), **t)
+            unsel = sorted(set(range(w.num_slots)) - set(rows.live.tolist()))
+            np.testing.assert_array_equal(got[unsel], pre[l].reshape(w.num_slots, -1)[unsel])
+        np.testing.assert_array_equal(hs.cpu().numpy(), hs_o)
+        assert P.status() == L.LSC_OK

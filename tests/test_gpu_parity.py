@@ -300,6 +300,23 @@ def test_decode_more_items_than_one_launch_holds(lsc):
         assert P.status() == L.LSC_OK
 
 
+def test_decode_fp32_dk128_ring_wraps(lsc):
+    """The benchmarked decode instantiation (head_k_dim 128, fp32 state, bf16
+    conv, width 4) with 512 rows of two q/k heads: 1024 work items, so each CTA
+    holds six or seven items of four 32 KiB tiles and its ring of stages wraps
+    several times; cold rows, a padding row and unselected slots included."""
+    w = workload("s3", num_slots=600)
+    with DevPool(w, seed=41, random_padding=True) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        idx, has, x, cw, a, b = decode_case(w, seed=42, n=512, cold_frac=0.1)
+        assert len(idx) * w.num_k_heads >= 6 * torch.cuda.get_device_properties(0).multi_processor_count
+        rc, out = run_decode(P, l, w, idx, has, x, cw, a, b, torch.cuda.current_stream())
+        assert rc == L.LSC_OK, L.lsc_error_string(rc)
+        check_decode(w, P, l, pre, idx, has, x, cw, a, b, out)
+        assert P.status() == L.LSC_OK
+
+
 def test_decode_two_steps_all_warm(lsc):
     """Two consecutive tokens on the same slots (the second reads what the first
     wrote), has_init NULL."""
