@@ -1,0 +1,790 @@
+// lsc_chunked_tc.cu -- the resumed-prefill GDN recurrence evaluated 64 tokens
+// at a time on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
+// Same token-ordered result as the token-by-token kernels (per token
+// S' = a S (I - b k k^T) + b v k^T, o = S' q), rearranged so that the work of
+// a chunk is a handful of matrix products plus a small triangular solve.
+//
+// Sources, cited by page title and section:
+//   [VA] "非连续 KV Cache" §6 (recurrent_gated_delta_rule, the token recurrence)
+//   [KP] "Kapitsa 源码拆解 05：前缀缓存与模型状态恢复", "Attention 与 Gated
+//        DeltaNet 保存的历史不同" (gate, predict S k, correct with v, read with
+//        q); "相同前缀不一定能全部复用" (continue from the restored checkpoint)
+// The pages give the token recurrence only; the chunked form is its algebraic
+// rearrangement, exact up to rounding.
+//
+// One chunk, tokens 0..C-1, from state S (dv x dk, rows r):
+//   Gam(j,t) = a_(j+1) ... a_t,  E_t = a_0 ... a_t
+//   P = S K^T, R = S Q^T (dv x C),  G_jt = k_j.k_t,  M_jt = k_j.q_t
+//   d_t = x_t - sum_(j<t) A_tj d_j,  A_tj = b_t Gam(j,t) G_jt,
+//   x_t = b_t (v_t - E_t P_t)                      (per row; a forward solve)
+//   o_t = E_t R_t + sum_(j<=t) Gam(j,t) M_jt d_j
+//   S'  = E_(C-1) S + sum_j Gam(j,C-1) d_j k_j^T
+// Gam is formed from a per-chunk running sum of log2|a| (zeros and signs of a
+// tracked apart), so no product of gates under- or overflows on the way.
+//
+// Products on the tensor cores, in tf32 with an fp32 accumulator.  Every
+// operand x is split as x = hi + lo (hi = tf32(x), lo = tf32(x - hi)) and each
+// product is formed as hi.hi + hi.lo + lo.hi: about 22 significant bits per
+// operand, so the products carry fp32-level error (the dropped lo.lo term is
+// below 2^-21 of the product).  Per chunk and v head:
+//   Gram   [K;Q] K^T       M 128 (k rows, q rows), N 64, K 128     (G and M)
+//   P      S K^T           M 128 (state rows), N 64, K 128   A = S from TMEM
+//   R      S Q^T           the same with Q
+//   update S += W K        M 128, N 128 (channels), K 64     A = W from TMEM
+// (W = d Gam(., C-1)); the state lives in TMEM as the update's accumulator
+// and is decayed by E_(C-1) in place each chunk.  The forward solve and the
+// outputs run on the CUDA cores, one thread per state row.
+//
+// CTA = one (sequence, v head), 256 threads, one CTA per SM (TMEM: all 512
+// columns; shared memory: ~220 KB):
+//   warps 0-3   row warps: thread r owns state row r (TMEM lane r): splits S
+//               for the A operands, forms the chunk's A and B (Gam-weighted
+//               Gram) matrices from the Gram accumulator, x, the solve, the
+//               outputs and W; warp 0 allocates the TMEM and thread 0 issues
+//               every MMA and commit, each once the operands it reads are in
+//               place (two warps per SM sub-partition leave each thread up to
+//               255 registers);
+//   warps 4-7   producers: load the next chunk's k and q from global memory
+//               into registers while the current chunk runs, split them and
+//               store them as tf32 operands (token-major [K; Q] once the R
+//               product of the current chunk is done, channel-major K once its
+//               update is done), and form the next chunk's gate scan.
+// Hand-offs go through mbarriers: producer -> MMA (operands in shared
+// memory), row warps -> MMA (TMEM operands written, TMEM results read), MMA
+// -> row warps / producers (tcgen05.commit).  Every wait is bounded: on
+// expiry the thread records LSC_ERR_DEV_TIMEOUT, the CTA stops issuing work,
+// waits (bounded) for the MMAs it issued and frees its TMEM.
+//
+// Shared-memory operands (no swizzle, 8 x 16-byte core matrices):
+//   [K; Q] token-major: element (row i, channel c) at (i/8)*4112 + (c/4)*128 +
+//   (i%8)*16 + (c%4)*4 -- K-major with LBO 128, SBO 4112 (rows 0-63 k, 64-127 q);
+//   K channel-major: element (channel c, token j) at (c/8)*2304 + (j/4)*144 +
+//   (c%8)*16 + (j%4)*4 -- K-major with LBO 144, SBO 2304.
+// The 16 bytes beyond each 4096 (resp. 128) spread the producers' 16-byte
+// stores over all banks.
+#include "lsc_gdn_common.cuh"
+#include "lsc_tc.h"
+
+namespace lsc {
+namespace {
+
+constexpr int kC = 64;        // tokens per chunk
+constexpr int kDK = 128;      // head_k_dim of this kernel
+constexpr int kThreads = 256;
+constexpr int kRowThreads = 128;
+constexpr int kProd0 = 128;   // first producer thread
+constexpr uint32_t kTmemCols = 512;
+
+// TMEM columns (lane = state row for every accumulator)
+constexpr uint32_t T_S = 0;      // state, fp32 (128)
+constexpr uint32_t T_SHI = 128;  // tf32 hi of S (128); then W hi (64)
+constexpr uint32_t T_SLO = 256;  // tf32 lo of S (128)
+constexpr uint32_t T_WHI = 128;
+constexpr uint32_t T_WLO = 192;  // W lo (64)
+constexpr uint32_t T_P = 384;    // P (64)
+constexpr uint32_t T_R = 448;    // Gram, then R (64)
+
+// shared-memory layout (bytes)
+constexpr uint32_t kKqRg = 4096 + 16;      // one 8-row group of the token-major tile
+constexpr uint32_t kKqBytes = 16 * kKqRg;  // 128 rows
+constexpr uint32_t kQRow0 = 8 * kKqRg;     // q rows start at row 64
+constexpr uint32_t kKtLbo = 128 + 16;      // one 4-token core-matrix column of the channel-major tile
+constexpr uint32_t kKtRg = 16 * kKtLbo;    // one 8-channel group (64 tokens)
+constexpr uint32_t kKtBytes = 16 * kKtRg;  // 128 channels
+
+// packed triangles: A by columns (column j: rows t in [a0(j), 64), zero for
+// t <= j), B by rows (row t: columns j in [0, b1(t)), zero for j > t); each
+// segment a multiple of 4 floats, 16-byte aligned
+__host__ __device__ constexpr int a0_of(int j) { return 4 * ((j + 1) / 4); }
+__host__ __device__ constexpr int b1_of(int t) { return 4 * ((t + 4) / 4); }
+// sum over m = 1..n of floor(m / 4)
+__host__ __device__ constexpr int quarter_sum(int n) {
+  return n <= 0 ? 0 : 2 * (n / 4) * (n / 4 - 1) + (n / 4) * (n % 4 + 1);
+}
+__host__ __device__ constexpr int a_off(int j) { return kC * j - 4 * quarter_sum(j); }
+__host__ __device__ constexpr int b_off(int t) { return 4 * t + 4 * quarter_sum(t - 1); }
+static_assert(a_off(1) == 64 && a_off(4) == 64 * 3 + 60 && b_off(1) == 4 && b_off(5) == 4 * 4 + 8, "packing");
+constexpr int kAFloats = a_off(kC);
+constexpr int kBFloats = b_off(kC);
+
+// per-chunk gate quantities, formed by the producers (double-buffered)
+struct ChunkGates {
+  float beta[kC];
+  float cum[kC];   // running sum of log2|a_t| over the chunk (0 where a_t = 0)
+  float E[kC];     // a_0 ... a_t
+  float F[kC];     // Gam(t, C-1)
+  int32_t seg[kC];   // last t' <= t with a_t' = 0, or -1
+  int32_t nneg[kC];  // number of negative a_t' for t' <= t
+  float e_last;
+  int32_t pad[3];
+};
+
+constexpr uint32_t OFF_KQHI = 0;
+constexpr uint32_t OFF_KQLO = OFF_KQHI + kKqBytes;
+constexpr uint32_t OFF_KTHI = OFF_KQLO + kKqBytes;
+constexpr uint32_t OFF_KTLO = OFF_KTHI + kKtBytes;
+constexpr uint32_t OFF_A = OFF_KTLO + kKtBytes;
+constexpr uint32_t OFF_B = OFF_A + 4 * kAFloats;
+constexpr uint32_t OFF_GATES = OFF_B + 4 * kBFloats;
+constexpr uint32_t kSmemBytes = OFF_GATES + 2 * sizeof(ChunkGates);
+static_assert(OFF_A % 16 == 0 && OFF_B % 16 == 0 && OFF_GATES % 16 == 0, "alignment");
+static_assert(kSmemBytes <= 225 * 1024, "shared memory budget (one CTA per SM)");
+
+// Gam(j, t) for j <= t (j = -1: E_t)
+__device__ __forceinline__ float gam(const ChunkGates &G, int j, int t) {
+  if (G.seg[t] > j) return 0.f;
+  const float c0 = j >= 0 ? G.cum[j] : 0.f;
+  const int n0 = j >= 0 ? G.nneg[j] : 0;
+  const float m = exp2f(G.cum[t] - c0);
+  return ((G.nneg[t] - n0) & 1) ? -m : m;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, uint64_t limit, int32_t *status,
+                                              volatile int *abort_flag) {
+  if (mbar_wait_bounded(bar, parity, limit)) return true;
+  report(status, LSC_ERR_DEV_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+// Row warps (warps 0-3) synchronise among themselves on named barrier 1, in
+// the non-aligned forms (thread 0 may arrive apart from its warp), and leave
+// with the warp reconverged for the warp-wide .sync.aligned TMEM loads and
+// stores that follow.
+__device__ __forceinline__ void named_sync_rows() {
+  asm volatile("barrier.sync 1, 128;" ::: "memory");
+  __syncwarp();
+}
+// true on every row thread when v is true on any of them
+__device__ __forceinline__ bool named_any_rows(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "barrier.red.or.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  __syncwarp();
+  return r != 0;
+}
+
+struct Bars {
+  uint64_t kq, kt, gates, split, ab, w;  // arrivals
+  uint64_t g, p, r, u;                    // MMA commits
+};
+
+template <typename TS>
+__global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_constant__ RecurrentParams p) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ Bars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int32_t s_len[kRankedSeqs];
+  __shared__ int32_t s_seq;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, g = h / p.group;
+  const int dv = p.dv;
+
+  const int i = ranked_sequence(p.cu, p.n_seq, s_len, &s_seq);
+  const int32_t slot = p.idx[i];
+  const bool bad = slot >= p.num_slots;
+  const bool valid = slot >= 0 && !bad;
+  const bool warm = valid && (p.has_init == nullptr || p.has_init[i] != 0);
+  const int t0 = p.cu[i], t1 = p.cu[i + 1];
+  if (bad && tid == 0 && h == 0) report(p.status, LSC_ERR_OUT_OF_RANGE);
+  if (t0 < 0 || t1 < t0 || t1 > p.total_tokens) {  // inconsistent cu_seqlens: touch nothing
+    if (tid == 0 && h == 0) report(p.status, LSC_ERR_INVALID_ARG);
+    return;
+  }
+  if (!valid) {  // uniform over the CTA
+    for (int64_t e = tid; e < (int64_t)(t1 - t0) * dv; e += kThreads) {
+      const int64_t t = t0 + e / dv;
+      p.out[(t * p.Hv + h) * dv + e % dv] = 0.f;
+    }
+    return;
+  }
+  const int nch = (t1 - t0 + kC - 1) / kC;
+  ChunkGates *gates = reinterpret_cast<ChunkGates *>(sm + OFF_GATES);
+  TS *Sg = reinterpret_cast<TS *>(p.layer + (int64_t)slot * p.page + p.ssm_off) + (int64_t)h * dv * kDK;
+
+  if (tid == 0) {
+    mbar_init(&bars.kq, kThreads - kProd0);  // every producer thread
+    mbar_init(&bars.kt, kThreads - kProd0);
+    mbar_init(&bars.gates, 1);
+    mbar_init(&bars.split, kRowThreads);
+    mbar_init(&bars.ab, kRowThreads);
+    mbar_init(&bars.w, kRowThreads);
+    mbar_init(&bars.g, 1);
+    mbar_init(&bars.p, 1);
+    mbar_init(&bars.r, 1);
+    mbar_init(&bars.u, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tc::tmem_alloc(&s_tmem, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  volatile int *abort_flag = &s_abort;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (warp < 4) {
+    // ======================================================= row warps
+    const int r = tid;
+    // MMA issue (thread 0): three tf32 passes (hi.hi, hi.lo, lo.hi) per product
+    const uint32_t kqhi = smem_u32(sm + OFF_KQHI), kqlo = smem_u32(sm + OFF_KQLO);
+    const uint32_t kthi = smem_u32(sm + OFF_KTHI), ktlo = smem_u32(sm + OFF_KTLO);
+    constexpr uint32_t id64 = tc::idesc_tf32(128, 64, false);
+    constexpr uint32_t id128 = tc::idesc_tf32(128, 128, false);
+    uint64_t *last = nullptr;  // the last commit's barrier and phase (thread 0)
+    uint32_t last_par = 0;
+    auto issue_gram = [&](uint32_t par) {  // [K;Q] (128 rows) x K (64 rows)^T -> T_R
+#pragma unroll 1
+      for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t a = ps == 2 ? kqlo : kqhi, b = ps == 1 ? kqlo : kqhi;
+#pragma unroll
+        for (int s = 0; s < kDK / 8; ++s)
+          tc::mma_ss(tmem + T_R, tc::smem_desc(a + 256 * s, 128, kKqRg), tc::smem_desc(b + 256 * s, 128, kKqRg), id64,
+                     (ps | s) != 0);
+      }
+      tc::mma_commit(&bars.g);
+      last = &bars.g, last_par = par;
+    };
+    auto issue_sk = [&](uint32_t d, uint32_t b_off_bytes, uint64_t *bar, uint32_t par) {  // S x (K or Q)^T -> d
+#pragma unroll 1
+      for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t a = ps == 2 ? T_SLO : T_SHI, b = (ps == 1 ? kqlo : kqhi) + b_off_bytes;
+#pragma unroll
+        for (int s = 0; s < kDK / 8; ++s)
+          tc::mma_ts(tmem + d, tmem + a + 8 * s, tc::smem_desc(b + 256 * s, 128, kKqRg), id64, (ps | s) != 0);
+      }
+      tc::mma_commit(bar);
+      last = bar, last_par = par;
+    };
+    auto issue_update = [&](uint32_t par) {  // S += W K (N = 128 channels, K = 64 tokens)
+#pragma unroll 1
+      for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t a = ps == 2 ? T_WLO : T_WHI, b = ps == 1 ? ktlo : kthi;
+#pragma unroll
+        for (int s = 0; s < kC / 8; ++s)
+          tc::mma_ts(tmem + T_S, tmem + a + 8 * s, tc::smem_desc(b + 2 * kKtLbo * s, kKtLbo, kKtRg), id128, 1);
+      }
+      tc::mma_commit(&bars.u);
+      last = &bars.u, last_par = par;
+    };
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
+    const bool row_ok = r < dv;
+    // initial state -> TMEM (zero when cold; rows >= dv stay zero)
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = 0u;
+      if (warm && row_ok) {
+        if constexpr (sizeof(TS) == 4) {
+          const float4 *src = reinterpret_cast<const float4 *>(Sg + (int64_t)r * kDK + 32 * q);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 f = __ldg(src + e);
+            v[4 * e] = __float_as_uint(f.x);
+            v[4 * e + 1] = __float_as_uint(f.y);
+            v[4 * e + 2] = __float_as_uint(f.z);
+            v[4 * e + 3] = __float_as_uint(f.w);
+          }
+        } else {
+          const uint4 *src = reinterpret_cast<const uint4 *>(Sg + (int64_t)r * kDK + 32 * q);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint4 b = __ldg(src + e);
+            const uint32_t w4[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              v[8 * e + 2 * k] = w4[k] << 16;
+              v[8 * e + 2 * k + 1] = w4[k] & 0xffff0000u;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      tc::tmem_st32(tl + T_S + 32 * q, v);
+    }
+    tc::tmem_wait_st();
+
+    for (int c = 0; c < nch; ++c) {
+      const ChunkGates &G = gates[c & 1];
+      const uint32_t par = c & 1;
+      const int nt = min(kC, t1 - t0 - c * kC);
+      const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
+      // ---- 0: (thread 0) the Gram product once the chunk's operands are stored
+      bool ok0 = true;
+      if (r == 0 && (ok0 = wait_or_abort(&bars.kq, par, lim, p.status, abort_flag))) {
+        tc::fence_after_sync();
+        issue_gram(par);
+      }
+      __syncwarp();
+      // ---- 1: split S into the tf32 A operands, decay S in place
+      bool ok = ok0 && (c == 0 || wait_or_abort(&bars.u, par ^ 1, lim, p.status, abort_flag)) &&
+                wait_or_abort(&bars.gates, par, lim, p.status, abort_flag);
+      if (named_any_rows(!ok)) break;
+      tc::fence_after_sync();
+      const float e_last = G.e_last;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t v[32], hi[32], lo[32];
+        tc::tmem_ld32(tl + T_S + 32 * q, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float s = __uint_as_float(v[e]);
+          tc::split_tf32(s, hi[e], lo[e]);
+          v[e] = __float_as_uint(s * e_last);
+        }
+        tc::tmem_st32(tl + T_SHI + 32 * q, hi);
+        tc::tmem_st32(tl + T_SLO + 32 * q, lo);
+        tc::tmem_st32(tl + T_S + 32 * q, v);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(&bars.split);
+      if (r == 0 && (ok0 = wait_or_abort(&bars.split, par, lim, p.status, abort_flag))) {
+        tc::fence_after_sync();
+        issue_sk(T_P, 0, &bars.p, par);  // P = S K^T
+      }
+      __syncwarp();
+
+      // v_t[r] for this chunk, in flight while A and B are formed
+      float vr[kC];
+#pragma unroll
+      for (int t = 0; t < kC; ++t)
+        vr[t] = (t < nt && row_ok) ? __ldg(p.v + ((tb + t) * p.Hv + h) * dv + r) : 0.f;
+
+      // ---- 2: A (by columns, threads 0-63) and B (by rows, threads 64-127),
+      // 16 Gram columns at a time
+      ok = ok0 && wait_or_abort(&bars.g, par, lim, p.status, abort_flag);
+      if (named_any_rows(!ok)) break;
+      tc::fence_after_sync();
+      {
+        float *As = reinterpret_cast<float *>(sm + OFF_A);
+        float *Bs = reinterpret_cast<float *>(sm + OFF_B);
+        const bool is_a = r < kC;
+        const int j = r, t = r - kC;  // A column j / B row t of this thread
+#pragma unroll 1
+        for (int cb = 0; cb < kC / 16; ++cb) {
+          uint32_t gv[16];
+          tc::tmem_ld16(tl + T_R + 16 * cb, gv);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e4 = 0; e4 < 16; e4 += 4) {
+            const int n0 = 16 * cb + e4;  // the Gram column (token) of gv[e4]
+            float f[4];
+            if (is_a) {
+              if (n0 < a0_of(j)) continue;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int tt = n0 + e;
+                f[e] = tt > j ? G.beta[tt] * gam(G, j, tt) * __uint_as_float(gv[e4 + e]) : 0.f;
+              }
+              *reinterpret_cast<float4 *>(As + a_off(j) + (n0 - a0_of(j))) = make_float4(f[0], f[1], f[2], f[3]);
+            } else {
+              if (n0 >= b1_of(t)) continue;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int jj = n0 + e;
+                f[e] = jj <= t ? gam(G, jj, t) * __uint_as_float(gv[e4 + e]) : 0.f;
+              }
+              *reinterpret_cast<float4 *>(Bs + b_off(t) + n0) = make_float4(f[0], f[1], f[2], f[3]);
+            }
+          }
+        }
+        tc::fence_before_sync();
+        mbar_arrive(&bars.ab);  // every Gram column read: free for R
+      }
+      named_sync_rows();  // A and B visible to every row thread
+      if (r == 0 && (ok0 = wait_or_abort(&bars.ab, par, lim, p.status, abort_flag))) {
+        tc::fence_after_sync();
+        issue_sk(T_R, kQRow0, &bars.r, par);  // R = S Q^T
+      }
+      __syncwarp();
+
+      // ---- 3: x_t = b_t (v_t - E_t P_t) in place of P, then the forward
+      // solve by 16-token blocks: d_b = x_b - A_bb d_b (unit lower triangular
+      // block), then x_b' -= A_b'b d_b for the later blocks b'
+      ok = ok0 && wait_or_abort(&bars.p, par, lim, p.status, abort_flag);
+      if (named_any_rows(!ok)) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int b = 0; b < kC / 16; ++b) {
+        uint32_t pv[16];
+        tc::tmem_ld16(tl + T_P + 16 * b, pv);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int t = 16 * b + e;
+          pv[e] = __float_as_uint(G.beta[t] * (vr[t] - G.E[t] * __uint_as_float(pv[e])));
+        }
+        tc::tmem_st16(tl + T_P + 16 * b, pv);
+      }
+      tc::tmem_wait_st();
+      {
+        const float *As = reinterpret_cast<const float *>(sm + OFF_A);
+#pragma unroll 1
+        for (int b = 0; b < kC / 16; ++b) {
+          uint32_t xw[16];
+          tc::tmem_ld16(tl + T_P + 16 * b, xw);
+          tc::tmem_wait_ld();
+          float xb[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) xb[e] = __uint_as_float(xw[e]);
+          // column j = 16 b + jj holds A(t, j) at a_off(j) + t - a0(j), t >= a0(j)
+#pragma unroll
+          for (int jj = 0; jj < 15; ++jj) {
+            const int j = 16 * b + jj;
+            const float *col = As + a_off(j) - a0_of(j) + 16 * b;  // + tt gives A(16 b + tt, j)
+            const float dj = xb[jj];
+#pragma unroll
+            for (int t4 = 4 * ((jj + 1) / 4); t4 < 16; t4 += 4) {
+              const float4 a4 = *reinterpret_cast<const float4 *>(col + t4);
+              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (t4 + e > jj) xb[t4 + e] = fmaf(-av[e], dj, xb[t4 + e]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) xw[e] = __float_as_uint(xb[e]);
+          tc::tmem_st16(tl + T_P + 16 * b, xw);
+          tc::tmem_wait_st();
+#pragma unroll 1
+          for (int b2 = b + 1; b2 < kC / 16; ++b2) {
+            uint32_t yw[16];
+            tc::tmem_ld16(tl + T_P + 16 * b2, yw);
+            tc::tmem_wait_ld();
+            float yb[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) yb[e] = __uint_as_float(yw[e]);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = 16 * b + jj;
+              const float *col = As + a_off(j) - a0_of(j) + 16 * b2;  // + tt gives A(16 b2 + tt, j)
+              const float dj = xb[jj];
+#pragma unroll
+              for (int t4 = 0; t4 < 16; t4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(col + t4);
+                yb[t4] = fmaf(-a4.x, dj, yb[t4]);
+                yb[t4 + 1] = fmaf(-a4.y, dj, yb[t4 + 1]);
+                yb[t4 + 2] = fmaf(-a4.z, dj, yb[t4 + 2]);
+                yb[t4 + 3] = fmaf(-a4.w, dj, yb[t4 + 3]);
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) yw[e] = __float_as_uint(yb[e]);
+            tc::tmem_st16(tl + T_P + 16 * b2, yw);
+            tc::tmem_wait_st();
+          }
+        }
+      }
+      // the P columns now hold d
+
+      // ---- 4: outputs o_t = E_t R_t + sum_(j<=t) B_tj d_j, 16 tokens at a time
+      ok = ok0 && wait_or_abort(&bars.r, par, lim, p.status, abort_flag);
+      if (named_any_rows(!ok)) break;
+      tc::fence_after_sync();
+      {
+        const float *Bs = reinterpret_cast<const float *>(sm + OFF_B);
+#pragma unroll 1
+        for (int b2 = 0; b2 < kC / 16; ++b2) {
+          uint32_t rw[16];
+          tc::tmem_ld16(tl + T_R + 16 * b2, rw);
+          tc::tmem_wait_ld();
+          float o[16];
+#pragma unroll
+          for (int tt = 0; tt < 16; ++tt) o[tt] = G.E[16 * b2 + tt] * __uint_as_float(rw[tt]);
+#pragma unroll 1
+          for (int b = 0; b <= b2; ++b) {
+            uint32_t dw[16];
+            tc::tmem_ld16(tl + T_P + 16 * b, dw);
+            tc::tmem_wait_ld();
+            if (b < b2) {
+#pragma unroll
+              for (int tt = 0; tt < 16; ++tt) {
+                const int t = 16 * b2 + tt;
+                const float4 *row = reinterpret_cast<const float4 *>(Bs + b_off(t) + 16 * b);
+                float acc = o[tt];
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4) {
+                  const float4 b4 = row[j4];
+                  acc = fmaf(b4.x, __uint_as_float(dw[4 * j4]), acc);
+                  acc = fmaf(b4.y, __uint_as_float(dw[4 * j4 + 1]), acc);
+                  acc = fmaf(b4.z, __uint_as_float(dw[4 * j4 + 2]), acc);
+                  acc = fmaf(b4.w, __uint_as_float(dw[4 * j4 + 3]), acc);
+                }
+                o[tt] = acc;
+              }
+            } else {
+#pragma unroll
+              for (int tt = 0; tt < 16; ++tt) {
+                const int t = 16 * b2 + tt;
+                const float4 *row = reinterpret_cast<const float4 *>(Bs + b_off(t) + 16 * b);
+                float acc = o[tt];
+#pragma unroll
+                for (int j4 = 0; j4 <= tt / 4; ++j4) {  // B_tj = 0 for j > t
+                  const float4 b4 = row[j4];
+                  acc = fmaf(b4.x, __uint_as_float(dw[4 * j4]), acc);
+                  acc = fmaf(b4.y, __uint_as_float(dw[4 * j4 + 1]), acc);
+                  acc = fmaf(b4.z, __uint_as_float(dw[4 * j4 + 2]), acc);
+                  acc = fmaf(b4.w, __uint_as_float(dw[4 * j4 + 3]), acc);
+                }
+                o[tt] = acc;
+              }
+            }
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int tt = 0; tt < 16; ++tt)
+              if (16 * b2 + tt < nt) p.out[((tb + 16 * b2 + tt) * p.Hv + h) * dv + r] = o[tt];
+          }
+        }
+      }
+
+      // ---- 5: W = d Gam(., C-1) as tf32 hi / lo -> TMEM (A of the update)
+#pragma unroll 1
+      for (int b = 0; b < kC / 16; ++b) {
+        uint32_t dw[16], hi[16], lo[16];
+        tc::tmem_ld16(tl + T_P + 16 * b, dw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) tc::split_tf32(__uint_as_float(dw[e]) * G.F[16 * b + e], hi[e], lo[e]);
+        tc::tmem_st16(tl + T_WHI + 16 * b, hi);
+        tc::tmem_st16(tl + T_WLO + 16 * b, lo);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(&bars.w);
+      if (r == 0 && wait_or_abort(&bars.w, par, lim, p.status, abort_flag) &&
+          wait_or_abort(&bars.kt, par, lim, p.status, abort_flag)) {
+        tc::fence_after_sync();
+        issue_update(par);
+      }
+      __syncwarp();
+    }
+    // ---- final state -> the slot
+    const bool fin = nch == 0 || wait_or_abort(&bars.u, (nch - 1) & 1, lim, p.status, abort_flag);
+    if (!named_any_rows(!fin || *abort_flag)) {
+      tc::fence_after_sync();
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t v[32];
+        __syncwarp();
+        tc::tmem_ld32(tl + T_S + 32 * q, v);
+        tc::tmem_wait_ld();
+        if (row_ok) {
+          if constexpr (sizeof(TS) == 4) {
+            float4 *dst = reinterpret_cast<float4 *>(Sg + (int64_t)r * kDK + 32 * q);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+          } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(Sg + (int64_t)r * kDK + 32 * q);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * e + 2 * k]),
+                                                          __uint_as_float(v[8 * e + 2 * k + 1]));
+                w4[k] = *reinterpret_cast<uint32_t *>(&b2);
+              }
+              dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+      }
+    }
+    // every MMA issued must be complete before the TMEM is freed
+    if (r == 0 && last) mbar_wait_bounded(last, last_par, p.drain_limit_ns);
+    tc::fence_before_sync();
+  } else {
+    // ======================================================= producers
+    const int pt = tid - kProd0, pw = pt >> 5;
+    const int al = lane & 7, bl = lane >> 3;
+    const float *qg = p.q, *kg = p.k;
+    float4 kr[2][2][4];  // next chunk's k: [token block half][channel block half][token in block]
+    // this thread's 4 x 4 blocks: tokens 4a..4a+3, channels 4b..4b+3 with
+    // a = al + 8 ah, b = bl + 4 pw + 16 bh
+    auto load_rows = [&](const float *src, int c, float4 (&dst)[2][2][4]) {
+      const int nt = min(kC, t1 - t0 - c * kC);
+      const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
+#pragma unroll
+      for (int ah = 0; ah < 2; ++ah)
+#pragma unroll
+        for (int bh = 0; bh < 2; ++bh)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int tok = 4 * (al + 8 * ah) + u, b = bl + 4 * pw + 16 * bh;
+            dst[ah][bh][u] = tok < nt ? __ldg(reinterpret_cast<const float4 *>(src + ((tb + tok) * p.Hk + g) * kDK + 4 * b))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+    };
+    auto st_split4 = [&](uint32_t off_hi, uint32_t off_lo, float4 f) {
+      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+      tc::split_tf32(f.x, h0, l0);
+      tc::split_tf32(f.y, h1, l1);
+      tc::split_tf32(f.z, h2, l2);
+      tc::split_tf32(f.w, h3, l3);
+      *reinterpret_cast<uint4 *>(sm + off_hi) = make_uint4(h0, h1, h2, h3);
+      *reinterpret_cast<uint4 *>(sm + off_lo) = make_uint4(l0, l1, l2, l3);
+    };
+    // token-major rows: k at row j, q at row 64 + j
+    auto store_rows = [&](const float4 (&src)[2][2][4], int row0) {
+#pragma unroll
+      for (int ah = 0; ah < 2; ++ah)
+#pragma unroll
+        for (int bh = 0; bh < 2; ++bh)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = row0 + 4 * (al + 8 * ah) + u, b = bl + 4 * pw + 16 * bh;
+            const uint32_t o = (uint32_t)(j / 8) * kKqRg + (uint32_t)b * 128 + (uint32_t)(j % 8) * 16;
+            st_split4(OFF_KQHI + o, OFF_KQLO + o, src[ah][bh][u]);
+          }
+    };
+    auto store_kq = [&](int c) {
+      store_rows(kr, 0);
+      float4 qr[2][2][4];
+      load_rows(qg, c, qr);
+      store_rows(qr, kC);
+    };
+    auto store_kt = [&]() {
+#pragma unroll
+      for (int ah = 0; ah < 2; ++ah)
+#pragma unroll
+        for (int bh = 0; bh < 2; ++bh) {
+          const int a = al + 8 * ah, b = bl + 4 * pw + 16 * bh;
+          const float4 *k4 = kr[ah][bh];
+          const float col[4][4] = {{k4[0].x, k4[1].x, k4[2].x, k4[3].x},
+                                   {k4[0].y, k4[1].y, k4[2].y, k4[3].y},
+                                   {k4[0].z, k4[1].z, k4[2].z, k4[3].z},
+                                   {k4[0].w, k4[1].w, k4[2].w, k4[3].w}};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int ch = 4 * b + e;
+            const uint32_t o = (uint32_t)(ch / 8) * kKtRg + (uint32_t)a * kKtLbo + (uint32_t)(ch % 8) * 16;
+            st_split4(OFF_KTHI + o, OFF_KTLO + o, make_float4(col[e][0], col[e][1], col[e][2], col[e][3]));
+          }
+        }
+    };
+    // gate scan of chunk c by producer warp 0: two tokens per lane
+    auto form_gates = [&](int c) {
+      ChunkGates &G = gates[c & 1];
+      const int nt = min(kC, t1 - t0 - c * kC);
+      const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
+      float la[2], bb[2];
+      int zi[2], ng[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = 2 * lane + e;
+        const float a = t < nt ? __ldg(p.alpha + (tb + t) * p.Hv + h) : 1.f;
+        bb[e] = t < nt ? __ldg(p.beta + (tb + t) * p.Hv + h) : 0.f;
+        la[e] = a != 0.f ? log2f(fabsf(a)) : 0.f;
+        zi[e] = a == 0.f ? t : -1;
+        ng[e] = a < 0.f ? 1 : 0;
+      }
+      // inclusive scans over the 64 tokens (lane holds tokens 2 lane, 2 lane + 1)
+      float cs = la[0] + la[1];
+      int zs = max(zi[0], zi[1]), ns = ng[0] + ng[1];
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const float cu = __shfl_up_sync(0xffffffffu, cs, m);
+        const int zu = __shfl_up_sync(0xffffffffu, zs, m), nu = __shfl_up_sync(0xffffffffu, ns, m);
+        if (lane >= m) {
+          cs += cu;
+          zs = max(zs, zu);
+          ns += nu;
+        }
+      }
+      // exclusive prefix for this lane's first token
+      float cx = __shfl_up_sync(0xffffffffu, cs, 1);
+      int nx = __shfl_up_sync(0xffffffffu, ns, 1), zx = __shfl_up_sync(0xffffffffu, zs, 1);
+      if (lane == 0) {
+        cx = 0.f;
+        nx = 0;
+        zx = -1;
+      }
+      G.cum[2 * lane] = cx + la[0];
+      G.cum[2 * lane + 1] = cs;
+      G.seg[2 * lane] = max(zx, zi[0]);
+      G.seg[2 * lane + 1] = zs;
+      G.nneg[2 * lane] = nx + ng[0];
+      G.nneg[2 * lane + 1] = ns;
+      G.beta[2 * lane] = bb[0];
+      G.beta[2 * lane + 1] = bb[1];
+      __syncwarp();
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = 2 * lane + e;
+        G.E[t] = gam(G, -1, t);
+        G.F[t] = gam(G, t, kC - 1);
+      }
+      if (lane == 0) G.e_last = gam(G, -1, kC - 1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.gates);
+    };
+
+    if (nch > 0) {
+      load_rows(kg, 0, kr);
+      store_kq(0);
+      fence_proxy_async_smem();
+      mbar_arrive(&bars.kq);
+      if (pw == 0) form_gates(0);
+      store_kt();
+      fence_proxy_async_smem();
+      mbar_arrive(&bars.kt);
+    }
+    for (int c = 0; c + 1 < nch; ++c) {
+      const uint32_t par = c & 1;
+      load_rows(kg, c + 1, kr);
+      if (*abort_flag || !wait_or_abort(&bars.r, par, lim, p.status, abort_flag)) break;
+      store_kq(c + 1);
+      fence_proxy_async_smem();
+      mbar_arrive(&bars.kq);
+      if (pw == 0) form_gates(c + 1);
+      if (!wait_or_abort(&bars.u, par, lim, p.status, abort_flag)) break;
+      store_kt();
+      fence_proxy_async_smem();
+      mbar_arrive(&bars.kt);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <typename TS>
+int launch_chunked_tc_t(const RecurrentParams &p, cudaStream_t s) {
+  static SmemLimit limit;  // per instantiation and device
+  if (limit.ensure((const void *)chunked_tc_kernel<TS>, (int)kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return LSC_ERR_UNSUPPORTED;
+  }
+  chunked_tc_kernel<TS><<<dim3(p.Hv, p.n_seq, 1), kThreads, kSmemBytes, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;
+  return LSC_OK;
+}
+
+}  // namespace
+
+int launch_recurrent_chunked_tc(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t s) {
+  if (dk != kDK || p.dv > kMaxDv || p.dv < 1) return LSC_ERR_UNSUPPORTED;
+  return ssm_dtype == LSC_BF16 ? launch_chunked_tc_t<__nv_bfloat16>(p, s) : launch_chunked_tc_t<float>(p, s);
+}
+
+}  // namespace lsc

@@ -626,7 +626,9 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
   r.beta = a->beta;
   r.out = a->out;
   r.status = g.status;
-  return chunked ? lsc::launch_recurrent_chunked(r, g.dk, g.ssm_dtype, (cudaStream_t)stream)
+  r.wait_limit_ns = fault("timeout0") ? 0 : kWaitLimitNs;
+  r.drain_limit_ns = kWaitLimitNs;
+  return chunked ? lsc::launch_recurrent_chunked_tc(r, g.dk, g.ssm_dtype, (cudaStream_t)stream)
                  : lsc::launch_recurrent(r, g.dk, g.ssm_dtype, (cudaStream_t)stream);
 }
 

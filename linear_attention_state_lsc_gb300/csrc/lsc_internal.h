@@ -171,12 +171,16 @@ struct RecurrentParams {
   const float *q, *k, *v, *alpha, *beta;
   float *out;
   int32_t *status;
+  uint64_t wait_limit_ns;   // bound of each mbarrier wait (tensor-core form; 0: give up at once)
+  uint64_t drain_limit_ns;  // bound of the wait for issued MMAs after a timeout
 };
 int launch_recurrent(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
 // the token recurrence for head_k_dim 128 (lsc_rec128.cu)
 int launch_recurrent128(const RecurrentParams &p, int ssm_dtype, cudaStream_t stream);
 // the chunked evaluation (lsc_chunked.cu): head_k_dim 128, head_v_dim <= 128
 int launch_recurrent_chunked(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
+// the chunked evaluation on the tensor cores (lsc_chunked_tc.cu): head_k_dim 128, head_v_dim <= 128
+int launch_recurrent_chunked_tc(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
 
 struct PrefillConvParams {
   uint8_t *layer;
