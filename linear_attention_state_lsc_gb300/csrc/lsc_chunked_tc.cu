@@ -2,7 +2,7 @@
 // at a time on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
 // Same token-ordered result as the token-by-token kernels (per token
 // S' = a S (I - b k k^T) + b v k^T, o = S' q), rearranged so that the work of
-// a chunk is a handful of matrix products plus a small triangular solve.
+// a chunk is a handful of matrix products plus a small triangular inverse.
 //
 // Sources, cited by page title and section:
 //   [VA] "非连续 KV Cache" §6 (recurrent_gated_delta_rule, the token recurrence)
@@ -13,12 +13,12 @@
 // rearrangement, exact up to rounding.
 //
 // One chunk, tokens 0..C-1, from state S (dv x dk, rows r):
-//   Gam(j,t) = a_(j+1) ... a_t,  E_t = a_0 ... a_t
+//   Gam(j,t) = a_(j+1) ... a_t,  E_t = a_0 ... a_t,  F_j = Gam(j, C-1)
 //   P = S K^T, R = S Q^T (dv x C),  G_jt = k_j.k_t,  M_jt = k_j.q_t
-//   d_t = x_t - sum_(j<t) A_tj d_j,  A_tj = b_t Gam(j,t) G_jt,
-//   x_t = b_t (v_t - E_t P_t)                      (per row; a forward solve)
-//   o_t = E_t R_t + sum_(j<=t) Gam(j,t) M_jt d_j
-//   S'  = E_(C-1) S + sum_j Gam(j,C-1) d_j k_j^T
+//   A_tj = b_t Gam(j,t) G_jt (j < t),  T = (I + A)^-1 (unit lower triangular)
+//   X_rt = b_t (v_t[r] - E_t P_rt),  D = X T^T    (d_t = x_t - sum_(j<t) A_tj d_j)
+//   B_tj = Gam(j,t) M_jt (j <= t),   O = E o R + D B^T   (o_t of every row)
+//   S' = E_(C-1) S + D (F o K)                     (the rank-C update)
 // Gam is formed from a per-chunk running sum of log2|a| (zeros and signs of a
 // tracked apart), so no product of gates under- or overflows on the way.
 //
@@ -26,29 +26,30 @@
 // operand x is split as x = hi + lo (hi = tf32(x), lo = tf32(x - hi)) and each
 // product is formed as hi.hi + hi.lo + lo.hi: about 22 significant bits per
 // operand, so the products carry fp32-level error (the dropped lo.lo term is
-// below 2^-21 of the product).  Per chunk and v head:
-//   Gram   [K;Q] K^T       M 128 (k rows, q rows), N 64, K 128     (G and M)
-//   P      S K^T           M 128 (state rows), N 64, K 128   A = S from TMEM
-//   R      S Q^T           the same with Q
-//   update S += W K        M 128, N 128 (channels), K 64     A = W from TMEM
-// (W = d Gam(., C-1)); the state lives in TMEM as the update's accumulator
-// and is decayed by E_(C-1) in place each chunk.  The forward solve and the
-// outputs run on the CUDA cores, one thread per state row.
+// below 2^-21 of the product).  Per chunk and v head (M 128 = state rows):
+//   Gram    [K;Q] K^T   M 128 (k rows, q rows), N 64, K 128  (both from smem)
+//   P, R    S K^T, S Q^T                N 64, K 128   A = S from TMEM
+//   D       X T^T                       N 64, K 64    A = X from TMEM
+//   O       E o R + D B^T               N 64, K 64    A = D from TMEM
+//   update  S += D (F o K)              N 128, K 64   A = D from TMEM
+// The state lives in TMEM as the update's accumulator and is decayed by
+// E_(C-1) in place each chunk.  The CUDA cores form A and B from the Gram
+// accumulator, invert I + A (one column per thread, forward substitution),
+// and split the TMEM operands; one thread per state row.
 //
 // CTA = one (sequence, v head), 256 threads, one CTA per SM (TMEM: all 512
 // columns; shared memory: ~220 KB):
-//   warps 0-3   row warps: thread r owns state row r (TMEM lane r): splits S
-//               for the A operands, forms the chunk's A and B (Gam-weighted
-//               Gram) matrices from the Gram accumulator, x, the solve, the
-//               outputs and W; warp 0 allocates the TMEM and thread 0 issues
-//               every MMA and commit, each once the operands it reads are in
-//               place (two warps per SM sub-partition leave each thread up to
-//               255 registers);
+//   warps 0-3   row warps: thread r owns state row r (TMEM lane r); threads
+//               0-63 also own column r of T; warp 0 allocates the TMEM and
+//               thread 0 issues every MMA and commit once the operands it
+//               reads are in place (two warps per SM sub-partition leave each
+//               thread up to 255 registers);
 //   warps 4-7   producers: load the next chunk's k and q from global memory
 //               into registers while the current chunk runs, split them and
-//               store them as tf32 operands (token-major [K; Q] once the R
-//               product of the current chunk is done, channel-major K once its
-//               update is done), and form the next chunk's gate scan.
+//               store them as tf32 operands (token-major [K; Q] once the
+//               current chunk's products that overlay that tile are done,
+//               channel-major F o K once its update is done), and form the
+//               next chunk's gate scan.
 // Hand-offs go through mbarriers: producer -> MMA (operands in shared
 // memory), row warps -> MMA (TMEM operands written, TMEM results read), MMA
 // -> row warps / producers (tcgen05.commit).  Every wait is bounded: on
@@ -58,10 +59,13 @@
 // Shared-memory operands (no swizzle, 8 x 16-byte core matrices):
 //   [K; Q] token-major: element (row i, channel c) at (i/8)*4112 + (c/4)*128 +
 //   (i%8)*16 + (c%4)*4 -- K-major with LBO 128, SBO 4112 (rows 0-63 k, 64-127 q);
-//   K channel-major: element (channel c, token j) at (c/8)*2304 + (j/4)*144 +
-//   (c%8)*16 + (j%4)*4 -- K-major with LBO 144, SBO 2304.
-// The 16 bytes beyond each 4096 (resp. 128) spread the producers' 16-byte
-// stores over all banks.
+//   F o K channel-major: element (channel c, token j) at (c/8)*2304 +
+//   (j/4)*144 + (c%8)*16 + (j%4)*4 -- K-major with LBO 144, SBO 2304;
+//   T and B (64 x 64, row t, column j) at (t/8)*2304 + (j/4)*144 + (t%8)*16 +
+//   (j%4)*4: T over the k rows of the [K; Q] tiles once P has read them, B
+//   over the q rows once R has.
+// The 16 bytes beyond each 4096 (resp. 128) spread the threads' stores over
+// all banks.
 #include "lsc_gdn_common.cuh"
 #include "lsc_tc.h"
 
@@ -75,26 +79,27 @@ constexpr int kRowThreads = 128;
 constexpr int kProd0 = 128;   // first producer thread
 constexpr uint32_t kTmemCols = 512;
 
-// TMEM columns (lane = state row for every accumulator)
+// TMEM columns (lane = state row for every accumulator and A operand)
 constexpr uint32_t T_S = 0;      // state, fp32 (128)
-constexpr uint32_t T_SHI = 128;  // tf32 hi of S (128); then W hi (64)
-constexpr uint32_t T_SLO = 256;  // tf32 lo of S (128)
-constexpr uint32_t T_WHI = 128;
-constexpr uint32_t T_WLO = 192;  // W lo (64)
-constexpr uint32_t T_P = 384;    // P (64)
-constexpr uint32_t T_R = 448;    // Gram, then R (64)
+constexpr uint32_t T_SHI = 128;  // tf32 hi of S (128)      -> X hi (64), X lo (64)
+constexpr uint32_t T_SLO = 256;  // tf32 lo of S (128)      -> D (64), D hi (64)
+constexpr uint32_t T_P = 384;    // P (64)                  -> D lo (64)
+constexpr uint32_t T_R = 448;    // Gram (64)  -> R -> O (64)
+constexpr uint32_t T_XHI = 128, T_XLO = 192;
+constexpr uint32_t T_D = 256, T_DHI = 320, T_DLO = 384;
 
 // shared-memory layout (bytes)
 constexpr uint32_t kKqRg = 4096 + 16;      // one 8-row group of the token-major tile
 constexpr uint32_t kKqBytes = 16 * kKqRg;  // 128 rows
 constexpr uint32_t kQRow0 = 8 * kKqRg;     // q rows start at row 64
-constexpr uint32_t kKtLbo = 128 + 16;      // one 4-token core-matrix column of the channel-major tile
-constexpr uint32_t kKtRg = 16 * kKtLbo;    // one 8-channel group (64 tokens)
-constexpr uint32_t kKtBytes = 16 * kKtRg;  // 128 channels
+constexpr uint32_t kLbo = 128 + 16;        // one 4-column core-matrix column of a 64-column tile
+constexpr uint32_t kRg64 = 16 * kLbo;      // one 8-row group of a 64-column tile
+constexpr uint32_t kKtBytes = 16 * kRg64;  // channel-major K: 128 channel rows
+constexpr uint32_t kSqBytes = 8 * kRg64;   // T or B: 64 rows
 
-// packed triangles: A by columns (column j: rows t in [a0(j), 64), zero for
-// t <= j), B by rows (row t: columns j in [0, b1(t)), zero for j > t); each
-// segment a multiple of 4 floats, 16-byte aligned
+// packed triangles (fp32): A by columns (column j: rows t in [a0(j), 64),
+// zero for t <= j), B by rows (row t: columns j in [0, b1(t)), zero for
+// j > t); each segment a multiple of 4 floats, 16-byte aligned
 __host__ __device__ constexpr int a0_of(int j) { return 4 * ((j + 1) / 4); }
 __host__ __device__ constexpr int b1_of(int t) { return 4 * ((t + 4) / 4); }
 // sum over m = 1..n of floor(m / 4)
@@ -127,15 +132,27 @@ constexpr uint32_t OFF_A = OFF_KTLO + kKtBytes;
 constexpr uint32_t OFF_B = OFF_A + 4 * kAFloats;
 constexpr uint32_t OFF_GATES = OFF_B + 4 * kBFloats;
 constexpr uint32_t kSmemBytes = OFF_GATES + 2 * sizeof(ChunkGates);
+// T and B operands (hi, lo) over the [K; Q] tiles: T over the k rows (free
+// once P is done, while R still reads the q rows), B over the q rows (free
+// once R is done)
+constexpr uint32_t OFF_THI = OFF_KQHI, OFF_TLO = OFF_KQLO;
+constexpr uint32_t OFF_BHI = OFF_KQHI + kQRow0, OFF_BLO = OFF_KQLO + kQRow0;
+static_assert(kSqBytes <= kQRow0 && kQRow0 + kSqBytes <= kKqBytes, "T over the k rows, B over the q rows");
 static_assert(OFF_A % 16 == 0 && OFF_B % 16 == 0 && OFF_GATES % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 225 * 1024, "shared memory budget (one CTA per SM)");
+
+// byte offset of (row, col) in a 64-column operand tile
+__host__ __device__ constexpr uint32_t sq_off(int row, int col) {
+  return (uint32_t)(row / 8) * kRg64 + (uint32_t)(col / 4) * kLbo + (uint32_t)(row % 8) * 16 + (uint32_t)(col % 4) * 4;
+}
 
 // Gam(j, t) for j <= t (j = -1: E_t)
 __device__ __forceinline__ float gam(const ChunkGates &G, int j, int t) {
   if (G.seg[t] > j) return 0.f;
   const float c0 = j >= 0 ? G.cum[j] : 0.f;
   const int n0 = j >= 0 ? G.nneg[j] : 0;
-  const float m = exp2f(G.cum[t] - c0);
+  float m;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(m) : "f"(G.cum[t] - c0));  // Gam < 2^-126 flushes to 0
   return ((G.nneg[t] - n0) & 1) ? -m : m;
 }
 
@@ -169,9 +186,26 @@ __device__ __forceinline__ bool named_any_rows(bool v) {
 }
 
 struct Bars {
-  uint64_t kq, kt, gates, split, ab, w;  // arrivals
-  uint64_t g, p, r, u;                    // MMA commits
+  uint64_t kq, kt, gates, split, ab, xt, dd;  // arrivals
+  uint64_t g, p, r, d, o, u;                  // MMA commits
 };
+
+// 64 TMEM columns of this thread's lane as floats, one wait
+__device__ __forceinline__ void ld64(uint32_t taddr, float (&x)[kC]) {
+  uint32_t a[16], b[16], c[16], d[16];
+  tc::tmem_ld16(taddr, a);
+  tc::tmem_ld16(taddr + 16, b);
+  tc::tmem_ld16(taddr + 32, c);
+  tc::tmem_ld16(taddr + 48, d);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    x[e] = __uint_as_float(a[e]);
+    x[16 + e] = __uint_as_float(b[e]);
+    x[32 + e] = __uint_as_float(c[e]);
+    x[48 + e] = __uint_as_float(d[e]);
+  }
+}
 
 template <typename TS>
 __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_constant__ RecurrentParams p) {
@@ -214,10 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
     mbar_init(&bars.gates, 1);
     mbar_init(&bars.split, kRowThreads);
     mbar_init(&bars.ab, kRowThreads);
-    mbar_init(&bars.w, kRowThreads);
+    mbar_init(&bars.xt, kRowThreads);
+    mbar_init(&bars.dd, kRowThreads);
     mbar_init(&bars.g, 1);
     mbar_init(&bars.p, 1);
     mbar_init(&bars.r, 1);
+    mbar_init(&bars.d, 1);
+    mbar_init(&bars.o, 1);
     mbar_init(&bars.u, 1);
     fence_mbar_init();
     s_abort = 0;
@@ -240,43 +277,52 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
     // MMA issue (thread 0): three tf32 passes (hi.hi, hi.lo, lo.hi) per product
     const uint32_t kqhi = smem_u32(sm + OFF_KQHI), kqlo = smem_u32(sm + OFF_KQLO);
     const uint32_t kthi = smem_u32(sm + OFF_KTHI), ktlo = smem_u32(sm + OFF_KTLO);
+    const uint32_t thi = smem_u32(sm + OFF_THI), tlo = smem_u32(sm + OFF_TLO);
+    const uint32_t bhi = smem_u32(sm + OFF_BHI), blo = smem_u32(sm + OFF_BLO);
     constexpr uint32_t id64 = tc::idesc_tf32(128, 64, false);
     constexpr uint32_t id128 = tc::idesc_tf32(128, 128, false);
     uint64_t *last = nullptr;  // the last commit's barrier and phase (thread 0)
     uint32_t last_par = 0;
-    auto issue_gram = [&](uint32_t par) {  // [K;Q] (128 rows) x K (64 rows)^T -> T_R
-#pragma unroll 1
-      for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 2 ? kqlo : kqhi, b = ps == 1 ? kqlo : kqhi;
-#pragma unroll
-        for (int s = 0; s < kDK / 8; ++s)
-          tc::mma_ss(tmem + T_R, tc::smem_desc(a + 256 * s, 128, kKqRg), tc::smem_desc(b + 256 * s, 128, kKqRg), id64,
-                     (ps | s) != 0);
-      }
-      tc::mma_commit(&bars.g);
-      last = &bars.g, last_par = par;
-    };
-    auto issue_sk = [&](uint32_t d, uint32_t b_off_bytes, uint64_t *bar, uint32_t par) {  // S x (K or Q)^T -> d
-#pragma unroll 1
-      for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 2 ? T_SLO : T_SHI, b = (ps == 1 ? kqlo : kqhi) + b_off_bytes;
-#pragma unroll
-        for (int s = 0; s < kDK / 8; ++s)
-          tc::mma_ts(tmem + d, tmem + a + 8 * s, tc::smem_desc(b + 256 * s, 128, kKqRg), id64, (ps | s) != 0);
-      }
+    auto commit = [&](uint64_t *bar, uint32_t par) {
       tc::mma_commit(bar);
       last = bar, last_par = par;
     };
-    auto issue_update = [&](uint32_t par) {  // S += W K (N = 128 channels, K = 64 tokens)
+    // The issue loops stay rolled and advance the descriptors by constants
+    // (the start address sits in the descriptor's low bits): a k step of 8
+    // tf32 columns is 256 bytes along a 128-column tile, 288 bytes along a
+    // 64-column tile, 8 columns of a TMEM operand.
+    // [K;Q] (128 rows) x K (64 rows)^T -> T_R
+    auto issue_gram = [&]() {
 #pragma unroll 1
       for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 2 ? T_WLO : T_WHI, b = ps == 1 ? ktlo : kthi;
-#pragma unroll
-        for (int s = 0; s < kC / 8; ++s)
-          tc::mma_ts(tmem + T_S, tmem + a + 8 * s, tc::smem_desc(b + 2 * kKtLbo * s, kKtLbo, kKtRg), id128, 1);
+        uint64_t ad = tc::smem_desc(ps == 2 ? kqlo : kqhi, 128, kKqRg);
+        uint64_t bd = tc::smem_desc(ps == 1 ? kqlo : kqhi, 128, kKqRg);
+#pragma unroll 1
+        for (int s = 0; s < kDK / 8; ++s, ad += 256 >> 4, bd += 256 >> 4)
+          tc::mma_ss(tmem + T_R, ad, bd, id64, (ps | s) != 0);
       }
-      tc::mma_commit(&bars.u);
-      last = &bars.u, last_par = par;
+    };
+    // S x (K or Q)^T -> d  (K = 128 channels)
+    auto issue_sk = [&](uint32_t d, uint32_t b_off_bytes) {
+#pragma unroll 1
+      for (int ps = 0; ps < 3; ++ps) {
+        uint32_t a = tmem + (ps == 2 ? T_SLO : T_SHI);
+        uint64_t bd = tc::smem_desc((ps == 1 ? kqlo : kqhi) + b_off_bytes, 128, kKqRg);
+#pragma unroll 1
+        for (int s = 0; s < kDK / 8; ++s, a += 8, bd += 256 >> 4) tc::mma_ts(tmem + d, a, bd, id64, (ps | s) != 0);
+      }
+    };
+    // (a_hi, a_lo: TMEM, 64 columns) x (b_hi, b_lo: 64-column smem tiles, N rows)^T -> d
+    auto issue_t64 = [&](uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo, uint32_t idesc,
+                         bool acc) {
+#pragma unroll 1
+      for (int ps = 0; ps < 3; ++ps) {
+        uint32_t a = tmem + (ps == 2 ? a_lo : a_hi);
+        uint64_t bd = tc::smem_desc(ps == 1 ? b_lo : b_hi, kLbo, kRg64);
+#pragma unroll 1
+        for (int s = 0; s < kC / 8; ++s, a += 8, bd += (2 * kLbo) >> 4)
+          tc::mma_ts(tmem + d, a, bd, idesc, acc || (ps | s) != 0);
+      }
     };
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     const bool row_ok = r < dv;
@@ -325,47 +371,49 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       bool ok0 = true;
       if (r == 0 && (ok0 = wait_or_abort(&bars.kq, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
-        issue_gram(par);
+        issue_gram();
+        commit(&bars.g, par);
       }
       __syncwarp();
-      // ---- 1: split S into the tf32 A operands, decay S in place
+      // ---- 1: split S into the tf32 A operands of P and R, decay S in place
       bool ok = ok0 && (c == 0 || wait_or_abort(&bars.u, par ^ 1, lim, p.status, abort_flag)) &&
                 wait_or_abort(&bars.gates, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
       const float e_last = G.e_last;
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t v[32], hi[32], lo[32];
-        tc::tmem_ld32(tl + T_S + 32 * q, v);
+      for (int q = 0; q < kDK / 16; ++q) {
+        uint32_t v[16], hi[16], lo[16];
+        tc::tmem_ld16(tl + T_S + 16 * q, v);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 16; ++e) {
           const float s = __uint_as_float(v[e]);
           tc::split_tf32(s, hi[e], lo[e]);
           v[e] = __float_as_uint(s * e_last);
         }
-        tc::tmem_st32(tl + T_SHI + 32 * q, hi);
-        tc::tmem_st32(tl + T_SLO + 32 * q, lo);
-        tc::tmem_st32(tl + T_S + 32 * q, v);
+        tc::tmem_st16(tl + T_SHI + 16 * q, hi);
+        tc::tmem_st16(tl + T_SLO + 16 * q, lo);
+        tc::tmem_st16(tl + T_S + 16 * q, v);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(&bars.split);
       if (r == 0 && (ok0 = wait_or_abort(&bars.split, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
-        issue_sk(T_P, 0, &bars.p, par);  // P = S K^T
+        issue_sk(T_P, 0);  // P = S K^T
+        commit(&bars.p, par);
       }
       __syncwarp();
 
-      // v_t[r] for this chunk, in flight while A and B are formed
-      float vr[kC];
+      // v_t[r] of this chunk, in flight while A and B are formed
+      float x[kC];
 #pragma unroll
       for (int t = 0; t < kC; ++t)
-        vr[t] = (t < nt && row_ok) ? __ldg(p.v + ((tb + t) * p.Hv + h) * dv + r) : 0.f;
+        x[t] = (t < nt && row_ok) ? __ldg(p.v + ((tb + t) * p.Hv + h) * dv + r) : 0.f;
 
       // ---- 2: A (by columns, threads 0-63) and B (by rows, threads 64-127),
-      // 16 Gram columns at a time
+      // packed fp32, 16 Gram columns at a time
       ok = ok0 && wait_or_abort(&bars.g, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
@@ -375,32 +423,27 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
         const bool is_a = r < kC;
         const int j = r, t = r - kC;  // A column j / B row t of this thread
 #pragma unroll 1
-        for (int cb = 0; cb < kC / 16; ++cb) {
-          uint32_t gv[16];
-          tc::tmem_ld16(tl + T_R + 16 * cb, gv);
+        for (int n0 = 0; n0 < kC; n0 += 4) {  // Gram columns (tokens) n0 .. n0 + 3
+          uint32_t gv[4];
+          tc::tmem_ld4(tl + T_R + n0, gv);
           tc::tmem_wait_ld();
+          float f[4];
+          if (is_a && n0 >= a0_of(j)) {
 #pragma unroll
-          for (int e4 = 0; e4 < 16; e4 += 4) {
-            const int n0 = 16 * cb + e4;  // the Gram column (token) of gv[e4]
-            float f[4];
-            if (is_a) {
-              if (n0 < a0_of(j)) continue;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int tt = n0 + e;
-                f[e] = tt > j ? G.beta[tt] * gam(G, j, tt) * __uint_as_float(gv[e4 + e]) : 0.f;
-              }
-              *reinterpret_cast<float4 *>(As + a_off(j) + (n0 - a0_of(j))) = make_float4(f[0], f[1], f[2], f[3]);
-            } else {
-              if (n0 >= b1_of(t)) continue;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int jj = n0 + e;
-                f[e] = jj <= t ? gam(G, jj, t) * __uint_as_float(gv[e4 + e]) : 0.f;
-              }
-              *reinterpret_cast<float4 *>(Bs + b_off(t) + n0) = make_float4(f[0], f[1], f[2], f[3]);
+            for (int e = 0; e < 4; ++e) {
+              const int tt = n0 + e;
+              f[e] = tt > j ? G.beta[tt] * gam(G, j, tt) * __uint_as_float(gv[e]) : 0.f;
             }
+            *reinterpret_cast<float4 *>(As + a_off(j) + (n0 - a0_of(j))) = make_float4(f[0], f[1], f[2], f[3]);
+          } else if (!is_a && n0 < b1_of(t)) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int jj = n0 + e;
+              f[e] = jj <= t ? gam(G, jj, t) * __uint_as_float(gv[e]) : 0.f;
+            }
+            *reinterpret_cast<float4 *>(Bs + b_off(t) + n0) = make_float4(f[0], f[1], f[2], f[3]);
           }
+          __syncwarp();  // reconverged for the next warp-wide TMEM load
         }
         tc::fence_before_sync();
         mbar_arrive(&bars.ab);  // every Gram column read: free for R
@@ -408,170 +451,190 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       named_sync_rows();  // A and B visible to every row thread
       if (r == 0 && (ok0 = wait_or_abort(&bars.ab, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
-        issue_sk(T_R, kQRow0, &bars.r, par);  // R = S Q^T
+        issue_sk(T_R, kQRow0);  // R = S Q^T
+        commit(&bars.r, par);
       }
       __syncwarp();
 
-      // ---- 3: x_t = b_t (v_t - E_t P_t) in place of P, then the forward
-      // solve by 16-token blocks: d_b = x_b - A_bb d_b (unit lower triangular
-      // block), then x_b' -= A_b'b d_b for the later blocks b'
+      // ---- 3: x_t = b_t (v_t - E_t P_t), once P is done (P is also the last
+      // reader of the k rows, which T then overlays)
       ok = ok0 && wait_or_abort(&bars.p, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
-#pragma unroll
-      for (int b = 0; b < kC / 16; ++b) {
-        uint32_t pv[16];
-        tc::tmem_ld16(tl + T_P + 16 * b, pv);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int t = 16 * b + e;
-          pv[e] = __float_as_uint(G.beta[t] * (vr[t] - G.E[t] * __uint_as_float(pv[e])));
-        }
-        tc::tmem_st16(tl + T_P + 16 * b, pv);
-      }
-      tc::tmem_wait_st();
       {
+        // x replaces P in TMEM until R is done (X then goes out as tf32 hi / lo)
+        float pv[kC];
+        ld64(tl + T_P, pv);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int t = 16 * q + e;
+            w[e] = __float_as_uint(G.beta[t] * (x[t] - G.E[t] * pv[t]));
+          }
+          tc::tmem_st16(tl + T_P + 16 * q, w);
+        }
+      }
+      // column r of T = (I + A)^-1 (threads 0-63), 16 rows at a time:
+      // T_tr = [t == r] - sum_(n<t) A_tn T_nr, the rows of earlier blocks read
+      // back from the operand (hi + lo), the block's own rows by forward
+      // substitution; each block is stored as tf32 hi / lo as soon as it is done
+      if (r < kC) {
         const float *As = reinterpret_cast<const float *>(sm + OFF_A);
+        const uint32_t cj = (uint32_t)(r / 4) * kLbo + (uint32_t)(r % 4) * 4;  // column r within a row
 #pragma unroll 1
-        for (int b = 0; b < kC / 16; ++b) {
-          uint32_t xw[16];
-          tc::tmem_ld16(tl + T_P + 16 * b, xw);
-          tc::tmem_wait_ld();
-          float xb[16];
+        for (int tb = 0; tb < kC / 16; ++tb) {
+          float acc[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) xb[e] = __uint_as_float(xw[e]);
-          // column j = 16 b + jj holds A(t, j) at a_off(j) + t - a0(j), t >= a0(j)
+          for (int tt = 0; tt < 16; ++tt) acc[tt] = 16 * tb + tt == r ? 1.f : 0.f;
+#pragma unroll 1
+          for (int nb = 0; nb < tb; ++nb) {
+            float tn[16];
 #pragma unroll
-          for (int jj = 0; jj < 15; ++jj) {
-            const int j = 16 * b + jj;
-            const float *col = As + a_off(j) - a0_of(j) + 16 * b;  // + tt gives A(16 b + tt, j)
-            const float dj = xb[jj];
+            for (int nn = 0; nn < 16; ++nn) {
+              const uint32_t o = (uint32_t)(2 * nb + nn / 8) * kRg64 + (uint32_t)(nn % 8) * 16 + cj;
+              tn[nn] = __uint_as_float(*reinterpret_cast<const uint32_t *>(sm + OFF_THI + o)) +
+                       __uint_as_float(*reinterpret_cast<const uint32_t *>(sm + OFF_TLO + o));
+            }
 #pragma unroll
-            for (int t4 = 4 * ((jj + 1) / 4); t4 < 16; t4 += 4) {
+            for (int nn = 0; nn < 16; ++nn) {
+              const int n = 16 * nb + nn;
+              const float *col = As + a_off(n) - a0_of(n) + 16 * tb;  // + tt gives A(16 tb + tt, n)
+#pragma unroll
+              for (int t4 = 0; t4 < 16; t4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(col + t4);
+                acc[t4] = fmaf(-a4.x, tn[nn], acc[t4]);
+                acc[t4 + 1] = fmaf(-a4.y, tn[nn], acc[t4 + 1]);
+                acc[t4 + 2] = fmaf(-a4.z, tn[nn], acc[t4 + 2]);
+                acc[t4 + 3] = fmaf(-a4.w, tn[nn], acc[t4 + 3]);
+              }
+            }
+          }
+#pragma unroll
+          for (int nn = 0; nn < 15; ++nn) {
+            const int n = 16 * tb + nn;
+            const float *col = As + a_off(n) - a0_of(n) + 16 * tb;
+            const float tv = acc[nn];
+#pragma unroll
+            for (int t4 = 4 * ((nn + 1) / 4); t4 < 16; t4 += 4) {
               const float4 a4 = *reinterpret_cast<const float4 *>(col + t4);
               const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                if (t4 + e > jj) xb[t4 + e] = fmaf(-av[e], dj, xb[t4 + e]);
+                if (t4 + e > nn) acc[t4 + e] = fmaf(-av[e], tv, acc[t4 + e]);
             }
           }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) xw[e] = __float_as_uint(xb[e]);
-          tc::tmem_st16(tl + T_P + 16 * b, xw);
-          tc::tmem_wait_st();
-#pragma unroll 1
-          for (int b2 = b + 1; b2 < kC / 16; ++b2) {
-            uint32_t yw[16];
-            tc::tmem_ld16(tl + T_P + 16 * b2, yw);
-            tc::tmem_wait_ld();
-            float yb[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) yb[e] = __uint_as_float(yw[e]);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int j = 16 * b + jj;
-              const float *col = As + a_off(j) - a0_of(j) + 16 * b2;  // + tt gives A(16 b2 + tt, j)
-              const float dj = xb[jj];
-#pragma unroll
-              for (int t4 = 0; t4 < 16; t4 += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(col + t4);
-                yb[t4] = fmaf(-a4.x, dj, yb[t4]);
-                yb[t4 + 1] = fmaf(-a4.y, dj, yb[t4 + 1]);
-                yb[t4 + 2] = fmaf(-a4.z, dj, yb[t4 + 2]);
-                yb[t4 + 3] = fmaf(-a4.w, dj, yb[t4 + 3]);
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) yw[e] = __float_as_uint(yb[e]);
-            tc::tmem_st16(tl + T_P + 16 * b2, yw);
-            tc::tmem_wait_st();
+          for (int tt = 0; tt < 16; ++tt) {
+            uint32_t hi, lo;
+            tc::split_tf32(acc[tt], hi, lo);
+            const uint32_t o = (uint32_t)(2 * tb + tt / 8) * kRg64 + (uint32_t)(tt % 8) * 16 + cj;
+            *reinterpret_cast<uint32_t *>(sm + OFF_THI + o) = hi;
+            *reinterpret_cast<uint32_t *>(sm + OFF_TLO + o) = lo;
           }
         }
       }
-      // the P columns now hold d
-
-      // ---- 4: outputs o_t = E_t R_t + sum_(j<=t) B_tj d_j, 16 tokens at a time
+      // once R is done (the last reader of S hi / lo and of the q rows):
+      // X -> TMEM, B -> smem operand, R <- E o R
       ok = ok0 && wait_or_abort(&bars.r, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
-      {
-        const float *Bs = reinterpret_cast<const float *>(sm + OFF_B);
+      tc::tmem_wait_st();
 #pragma unroll 1
-        for (int b2 = 0; b2 < kC / 16; ++b2) {
-          uint32_t rw[16];
-          tc::tmem_ld16(tl + T_R + 16 * b2, rw);
-          tc::tmem_wait_ld();
-          float o[16];
-#pragma unroll
-          for (int tt = 0; tt < 16; ++tt) o[tt] = G.E[16 * b2 + tt] * __uint_as_float(rw[tt]);
-#pragma unroll 1
-          for (int b = 0; b <= b2; ++b) {
-            uint32_t dw[16];
-            tc::tmem_ld16(tl + T_P + 16 * b, dw);
-            tc::tmem_wait_ld();
-            if (b < b2) {
-#pragma unroll
-              for (int tt = 0; tt < 16; ++tt) {
-                const int t = 16 * b2 + tt;
-                const float4 *row = reinterpret_cast<const float4 *>(Bs + b_off(t) + 16 * b);
-                float acc = o[tt];
-#pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4) {
-                  const float4 b4 = row[j4];
-                  acc = fmaf(b4.x, __uint_as_float(dw[4 * j4]), acc);
-                  acc = fmaf(b4.y, __uint_as_float(dw[4 * j4 + 1]), acc);
-                  acc = fmaf(b4.z, __uint_as_float(dw[4 * j4 + 2]), acc);
-                  acc = fmaf(b4.w, __uint_as_float(dw[4 * j4 + 3]), acc);
-                }
-                o[tt] = acc;
-              }
-            } else {
-#pragma unroll
-              for (int tt = 0; tt < 16; ++tt) {
-                const int t = 16 * b2 + tt;
-                const float4 *row = reinterpret_cast<const float4 *>(Bs + b_off(t) + 16 * b);
-                float acc = o[tt];
-#pragma unroll
-                for (int j4 = 0; j4 <= tt / 4; ++j4) {  // B_tj = 0 for j > t
-                  const float4 b4 = row[j4];
-                  acc = fmaf(b4.x, __uint_as_float(dw[4 * j4]), acc);
-                  acc = fmaf(b4.y, __uint_as_float(dw[4 * j4 + 1]), acc);
-                  acc = fmaf(b4.z, __uint_as_float(dw[4 * j4 + 2]), acc);
-                  acc = fmaf(b4.w, __uint_as_float(dw[4 * j4 + 3]), acc);
-                }
-                o[tt] = acc;
-              }
-            }
-          }
-          if (row_ok) {
-#pragma unroll
-            for (int tt = 0; tt < 16; ++tt)
-              if (16 * b2 + tt < nt) p.out[((tb + 16 * b2 + tt) * p.Hv + h) * dv + r] = o[tt];
-          }
-        }
-      }
-
-      // ---- 5: W = d Gam(., C-1) as tf32 hi / lo -> TMEM (A of the update)
-#pragma unroll 1
-      for (int b = 0; b < kC / 16; ++b) {
-        uint32_t dw[16], hi[16], lo[16];
-        tc::tmem_ld16(tl + T_P + 16 * b, dw);
+      for (int q = 0; q < 4; ++q) {
+        // X hi / lo from x, and R <- E o R, 16 columns at a time
+        uint32_t w[16], hi[16], lo[16];
+        tc::tmem_ld16(tl + T_P + 16 * q, w);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) tc::split_tf32(__uint_as_float(dw[e]) * G.F[16 * b + e], hi[e], lo[e]);
-        tc::tmem_st16(tl + T_WHI + 16 * b, hi);
-        tc::tmem_st16(tl + T_WLO + 16 * b, lo);
+        for (int e = 0; e < 16; ++e) tc::split_tf32(__uint_as_float(w[e]), hi[e], lo[e]);
+        tc::tmem_st16(tl + T_XHI + 16 * q, hi);
+        tc::tmem_st16(tl + T_XLO + 16 * q, lo);
+        tc::tmem_ld16(tl + T_R + 16 * q, w);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(G.E[16 * q + e] * __uint_as_float(w[e]));
+        tc::tmem_st16(tl + T_R + 16 * q, w);
+      }
+      if (r >= kC) {
+        // row t of B from its packed row (zero beyond b1(t))
+        const int t = r - kC;
+        const float *row = reinterpret_cast<const float *>(sm + OFF_B) + b_off(t);
+        const int b1 = b1_of(t);
+#pragma unroll 1
+        for (int j4 = 0; j4 < kC; j4 += 4) {
+          const float4 b4 = j4 < b1 ? *reinterpret_cast<const float4 *>(row + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+          tc::split_tf32(b4.x, h0, l0);
+          tc::split_tf32(b4.y, h1, l1);
+          tc::split_tf32(b4.z, h2, l2);
+          tc::split_tf32(b4.w, h3, l3);
+          *reinterpret_cast<uint4 *>(sm + OFF_BHI + sq_off(t, j4)) = make_uint4(h0, h1, h2, h3);
+          *reinterpret_cast<uint4 *>(sm + OFF_BLO + sq_off(t, j4)) = make_uint4(l0, l1, l2, l3);
+        }
+      }
+      tc::tmem_wait_st();
+      fence_proxy_async_smem();  // T and B written by the generic proxy, read by the MMA
+      tc::fence_before_sync();
+      mbar_arrive(&bars.xt);
+      if (r == 0 && (ok0 = wait_or_abort(&bars.xt, par, lim, p.status, abort_flag))) {
+        tc::fence_after_sync();
+        issue_t64(T_D, T_XHI, T_XLO, thi, tlo, id64, false);  // D = X T^T
+        commit(&bars.d, par);
+      }
+      __syncwarp();
+
+      // ---- 4: D -> tf32 hi / lo (A of O and of the update)
+      ok = ok0 && wait_or_abort(&bars.d, par, lim, p.status, abort_flag);
+      if (named_any_rows(!ok)) break;
+      tc::fence_after_sync();
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[16], hi[16], lo[16];
+        tc::tmem_ld16(tl + T_D + 16 * q, w);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) tc::split_tf32(__uint_as_float(w[e]), hi[e], lo[e]);
+        tc::tmem_st16(tl + T_DHI + 16 * q, hi);
+        tc::tmem_st16(tl + T_DLO + 16 * q, lo);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(&bars.w);
-      if (r == 0 && wait_or_abort(&bars.w, par, lim, p.status, abort_flag) &&
-          wait_or_abort(&bars.kt, par, lim, p.status, abort_flag)) {
+      mbar_arrive(&bars.dd);
+      if (r == 0 && (ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
-        issue_update(par);
+        issue_t64(T_R, T_DHI, T_DLO, bhi, blo, id64, true);  // O = E o R + D B^T
+        commit(&bars.o, par);
+        if ((ok0 = wait_or_abort(&bars.kt, par, lim, p.status, abort_flag))) {
+          tc::fence_after_sync();
+          issue_t64(T_S, T_DHI, T_DLO, kthi, ktlo, id128, true);  // S += D (F o K)
+          commit(&bars.u, par);
+        }
       }
       __syncwarp();
+
+      // ---- 5: outputs
+      ok = ok0 && wait_or_abort(&bars.o, par, lim, p.status, abort_flag);
+      if (named_any_rows(!ok)) break;
+      tc::fence_after_sync();
+      {
+        float *o = p.out + (tb * p.Hv + h) * dv + r;
+        const int64_t ostride = (int64_t)p.Hv * dv;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[16];
+          tc::tmem_ld16(tl + T_R + 16 * q, w);
+          tc::tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (16 * q + e < nt) o[(16 * q + e) * ostride] = __uint_as_float(w[e]);
+          }
+        }
+      }
+      tc::fence_before_sync();
+      named_sync_rows();  // every row has read O: the next Gram may overwrite it
     }
     // ---- final state -> the slot
     const bool fin = nch == 0 || wait_or_abort(&bars.u, (nch - 1) & 1, lim, p.status, abort_flag);
@@ -660,24 +723,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       load_rows(qg, c, qr);
       store_rows(qr, kC);
     };
-    auto store_kt = [&]() {
+    // channel-major F o K: K[j][c] F_j at (channel c, token j)
+    auto store_kt = [&](const ChunkGates &G) {
 #pragma unroll
-      for (int ah = 0; ah < 2; ++ah)
+      for (int ah = 0; ah < 2; ++ah) {
+        const int a = al + 8 * ah;
+        const float f0 = G.F[4 * a], f1 = G.F[4 * a + 1], f2 = G.F[4 * a + 2], f3 = G.F[4 * a + 3];
 #pragma unroll
         for (int bh = 0; bh < 2; ++bh) {
-          const int a = al + 8 * ah, b = bl + 4 * pw + 16 * bh;
+          const int b = bl + 4 * pw + 16 * bh;
           const float4 *k4 = kr[ah][bh];
-          const float col[4][4] = {{k4[0].x, k4[1].x, k4[2].x, k4[3].x},
-                                   {k4[0].y, k4[1].y, k4[2].y, k4[3].y},
-                                   {k4[0].z, k4[1].z, k4[2].z, k4[3].z},
-                                   {k4[0].w, k4[1].w, k4[2].w, k4[3].w}};
+          const float col[4][4] = {{k4[0].x * f0, k4[1].x * f1, k4[2].x * f2, k4[3].x * f3},
+                                   {k4[0].y * f0, k4[1].y * f1, k4[2].y * f2, k4[3].y * f3},
+                                   {k4[0].z * f0, k4[1].z * f1, k4[2].z * f2, k4[3].z * f3},
+                                   {k4[0].w * f0, k4[1].w * f1, k4[2].w * f2, k4[3].w * f3}};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int ch = 4 * b + e;
-            const uint32_t o = (uint32_t)(ch / 8) * kKtRg + (uint32_t)a * kKtLbo + (uint32_t)(ch % 8) * 16;
+            const uint32_t o = (uint32_t)(ch / 8) * kRg64 + (uint32_t)a * kLbo + (uint32_t)(ch % 8) * 16;
             st_split4(OFF_KTHI + o, OFF_KTLO + o, make_float4(col[e][0], col[e][1], col[e][2], col[e][3]));
           }
         }
+      }
     };
     // gate scan of chunk c by producer warp 0: two tokens per lane
     auto form_gates = [&](int c) {
@@ -736,26 +803,37 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       if (lane == 0) mbar_arrive(&bars.gates);
     };
 
+    // Chunk c + 1 is prepared during chunk c: its k is loaded first; after
+    // R(c) its gates are formed; after O(c) (the last reader of the tiles
+    // that T and B overlay) the [K; Q] tiles are stored; after the update of
+    // chunk c the channel-major F o K.  Every producer waits for the gates of
+    // chunk c + 1 before it stores the [K; Q] tiles, so the gate barrier is
+    // never two phases ahead of a waiting producer.
     if (nch > 0) {
       load_rows(kg, 0, kr);
-      store_kq(0);
-      fence_proxy_async_smem();
-      mbar_arrive(&bars.kq);
       if (pw == 0) form_gates(0);
-      store_kt();
-      fence_proxy_async_smem();
-      mbar_arrive(&bars.kt);
+      if (wait_or_abort(&bars.gates, 0, lim, p.status, abort_flag)) {
+        store_kq(0);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars.kq);
+        store_kt(gates[0]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars.kt);
+      }
     }
-    for (int c = 0; c + 1 < nch; ++c) {
-      const uint32_t par = c & 1;
+    for (int c = 0; c + 1 < nch && !*abort_flag; ++c) {
+      const uint32_t par = c & 1, npar = par ^ 1;
       load_rows(kg, c + 1, kr);
-      if (*abort_flag || !wait_or_abort(&bars.r, par, lim, p.status, abort_flag)) break;
+      if (!wait_or_abort(&bars.r, par, lim, p.status, abort_flag)) break;
+      if (pw == 0) form_gates(c + 1);
+      if (!wait_or_abort(&bars.gates, npar, lim, p.status, abort_flag) ||
+          !wait_or_abort(&bars.o, par, lim, p.status, abort_flag))
+        break;
       store_kq(c + 1);
       fence_proxy_async_smem();
       mbar_arrive(&bars.kq);
-      if (pw == 0) form_gates(c + 1);
       if (!wait_or_abort(&bars.u, par, lim, p.status, abort_flag)) break;
-      store_kt();
+      store_kt(gates[npar]);
       fence_proxy_async_smem();
       mbar_arrive(&bars.kt);
     }

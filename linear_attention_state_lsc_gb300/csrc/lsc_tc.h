@@ -126,6 +126,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       LSC_TC_W8(0), LSC_TC_W8(8), LSC_TC_W8(16), LSC_TC_W8(24)
       : "memory");
 }
+// 4 consecutive columns of this thread's lane -> v[0..3].
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr)
+               : "memory");
+}
+
 // 16 consecutive columns of this thread's lane -> v[0..15].
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
