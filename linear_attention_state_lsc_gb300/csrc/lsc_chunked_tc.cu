@@ -27,23 +27,25 @@
 // product is formed as hi.hi + hi.lo + lo.hi: about 22 significant bits per
 // operand, so the products carry fp32-level error (the dropped lo.lo term is
 // below 2^-21 of the product).  Per chunk and v head (M 128 = state rows):
-//   Gram    [K;Q] K^T   M 128 (k rows, q rows), N 64, K 128  (both from smem)
-//   P, R    S K^T, S Q^T                N 64, K 128   A = S from TMEM
-//   D       X T^T                       N 64, K 64    A = X from TMEM
-//   O       E o R + D B^T               N 64, K 64    A = D from TMEM
-//   update  S += D (F o K)              N 128, K 64   A = D from TMEM
+//   Gram    [K;Q] K^T           M 128 (k rows, q rows), N 64,  K 128 (smem)
+//   P | R   S [K;Q]^T           N 128, K 128   A = S from TMEM
+//   D       X T^T               N 64,  K 64    A = X from TMEM
+//   O       E o R + D B^T       N 64,  K 64    A = D from TMEM
+//   update  S += D (F o K)      N 128, K 64    A = D from TMEM
 // The state lives in TMEM as the update's accumulator and is decayed by
 // E_(C-1) in place each chunk.  The CUDA cores form A and B from the Gram
-// accumulator, invert I + A (one column per thread, forward substitution),
-// and split the TMEM operands; one thread per state row.
+// accumulator (one row per thread), invert I + A by 16 x 16 blocks (the
+// diagonal blocks by forward substitution, then three levels of block
+// products), and split the TMEM operands; one thread per state row.
 //
 // CTA = one (sequence, v head), 256 threads, one CTA per SM (TMEM: all 512
-// columns; shared memory: ~220 KB):
-//   warps 0-3   row warps: thread r owns state row r (TMEM lane r); threads
-//               0-63 also own column r of T; warp 0 allocates the TMEM and
-//               thread 0 issues every MMA and commit once the operands it
-//               reads are in place (two warps per SM sub-partition leave each
-//               thread up to 255 registers);
+// columns; shared memory: ~224 KB):
+//   warps 0-3   row warps: thread r owns state row r (TMEM lane r) and row r
+//               of A (r < 64) or of B (r >= 64); warp 0 allocates the TMEM
+//               and thread 0 issues the MMAs and commits once the operands
+//               they read are in place, thread 32 the state update beside
+//               thread 0's O product (two warps per SM sub-partition leave
+//               each thread up to 255 registers);
 //   warps 4-7   producers: load the next chunk's k and q from global memory
 //               into registers while the current chunk runs, split them and
 //               store them as tf32 operands (token-major [K; Q] once the
@@ -54,7 +56,9 @@
 // memory), row warps -> MMA (TMEM operands written, TMEM results read), MMA
 // -> row warps / producers (tcgen05.commit).  Every wait is bounded: on
 // expiry the thread records LSC_ERR_DEV_TIMEOUT, the CTA stops issuing work,
-// waits (bounded) for the MMAs it issued and frees its TMEM.
+// waits (bounded) for the MMAs it issued and frees its TMEM.  The per-chunk
+// code runs as rolled loops with small bodies: each chunk executes it once,
+// and straight-line code of that size would be fetched from L2 every chunk.
 //
 // Shared-memory operands (no swizzle, 8 x 16-byte core matrices):
 //   [K; Q] token-major: element (row i, channel c) at (i/8)*4112 + (c/4)*128 +
@@ -62,8 +66,8 @@
 //   F o K channel-major: element (channel c, token j) at (c/8)*2304 +
 //   (j/4)*144 + (c%8)*16 + (j%4)*4 -- K-major with LBO 144, SBO 2304;
 //   T and B (64 x 64, row t, column j) at (t/8)*2304 + (j/4)*144 + (t%8)*16 +
-//   (j%4)*4: T over the k rows of the [K; Q] tiles once P has read them, B
-//   over the q rows once R has.
+//   (j%4)*4: T over the k rows and B over the q rows of the [K; Q] tiles once
+//   P | R has read them.
 // The 16 bytes beyond each 4096 (resp. 128) spread the threads' stores over
 // all banks.
 #include "lsc_gdn_common.cuh"
@@ -83,8 +87,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t T_S = 0;      // state, fp32 (128)
 constexpr uint32_t T_SHI = 128;  // tf32 hi of S (128)      -> X hi (64), X lo (64)
 constexpr uint32_t T_SLO = 256;  // tf32 lo of S (128)      -> D (64), D hi (64)
-constexpr uint32_t T_P = 384;    // P (64)                  -> D lo (64)
-constexpr uint32_t T_R = 448;    // Gram (64)  -> R -> O (64)
+constexpr uint32_t T_P = 384;    // P (64)                  -> x, then D lo (64)
+constexpr uint32_t T_R = 448;    // Gram (64), then R -> E o R -> O (64)
 constexpr uint32_t T_XHI = 128, T_XLO = 192;
 constexpr uint32_t T_D = 256, T_DHI = 320, T_DLO = 384;
 
@@ -97,20 +101,22 @@ constexpr uint32_t kRg64 = 16 * kLbo;      // one 8-row group of a 64-column til
 constexpr uint32_t kKtBytes = 16 * kRg64;  // channel-major K: 128 channel rows
 constexpr uint32_t kSqBytes = 8 * kRg64;   // T or B: 64 rows
 
-// packed triangles (fp32): A by columns (column j: rows t in [a0(j), 64),
-// zero for t <= j), B by rows (row t: columns j in [0, b1(t)), zero for
-// j > t); each segment a multiple of 4 floats, 16-byte aligned
-__host__ __device__ constexpr int a0_of(int j) { return 4 * ((j + 1) / 4); }
+// Packed triangles (fp32), every row a multiple of 4 floats, 16-byte aligned:
+// A by rows (row t: columns j in [0, 4 ceil(t/4)), zero for j >= t), T by
+// rows including the diagonal (row t: columns j in [0, 4 floor(t/4) + 4),
+// zero for j > t).
+__host__ __device__ constexpr int a1_of(int t) { return 4 * ((t + 3) / 4); }
 __host__ __device__ constexpr int b1_of(int t) { return 4 * ((t + 4) / 4); }
 // sum over m = 1..n of floor(m / 4)
 __host__ __device__ constexpr int quarter_sum(int n) {
   return n <= 0 ? 0 : 2 * (n / 4) * (n / 4 - 1) + (n / 4) * (n % 4 + 1);
 }
-__host__ __device__ constexpr int a_off(int j) { return kC * j - 4 * quarter_sum(j); }
-__host__ __device__ constexpr int b_off(int t) { return 4 * t + 4 * quarter_sum(t - 1); }
-static_assert(a_off(1) == 64 && a_off(4) == 64 * 3 + 60 && b_off(1) == 4 && b_off(5) == 4 * 4 + 8, "packing");
-constexpr int kAFloats = a_off(kC);
-constexpr int kBFloats = b_off(kC);
+__host__ __device__ constexpr int a_row(int t) { return 4 * quarter_sum(t + 2); }      // sum of a1_of(i), i < t
+__host__ __device__ constexpr int t_row(int t) { return 4 * t + 4 * quarter_sum(t - 1); }  // sum of b1_of(i), i < t
+static_assert(a_row(1) == 0 && a_row(2) == 4 && a_row(5) == 16 && t_row(1) == 4 && t_row(5) == 4 * 4 + 8, "packing");
+constexpr int kAFloats = a_row(kC);
+constexpr int kTFloats = t_row(kC);
+constexpr int kYFloats = 3 * 16 * 16;  // block-product scratch of the inverse
 
 // per-chunk gate quantities, formed by the producers (double-buffered)
 struct ChunkGates {
@@ -129,21 +135,26 @@ constexpr uint32_t OFF_KQLO = OFF_KQHI + kKqBytes;
 constexpr uint32_t OFF_KTHI = OFF_KQLO + kKqBytes;
 constexpr uint32_t OFF_KTLO = OFF_KTHI + kKtBytes;
 constexpr uint32_t OFF_A = OFF_KTLO + kKtBytes;
-constexpr uint32_t OFF_B = OFF_A + 4 * kAFloats;
-constexpr uint32_t OFF_GATES = OFF_B + 4 * kBFloats;
+constexpr uint32_t OFF_TP = OFF_A + 4 * kAFloats;
+constexpr uint32_t OFF_Y = OFF_TP + 4 * kTFloats;
+constexpr uint32_t OFF_GATES = OFF_Y + 4 * kYFloats;
 constexpr uint32_t kSmemBytes = OFF_GATES + 2 * sizeof(ChunkGates);
-// T and B operands (hi, lo) over the [K; Q] tiles: T over the k rows (free
-// once P is done, while R still reads the q rows), B over the q rows (free
-// once R is done)
+// T and B operands (hi, lo) over the [K; Q] tiles, written once P | R is done
 constexpr uint32_t OFF_THI = OFF_KQHI, OFF_TLO = OFF_KQLO;
 constexpr uint32_t OFF_BHI = OFF_KQHI + kQRow0, OFF_BLO = OFF_KQLO + kQRow0;
 static_assert(kSqBytes <= kQRow0 && kQRow0 + kSqBytes <= kKqBytes, "T over the k rows, B over the q rows");
-static_assert(OFF_A % 16 == 0 && OFF_B % 16 == 0 && OFF_GATES % 16 == 0, "alignment");
-static_assert(kSmemBytes <= 225 * 1024, "shared memory budget (one CTA per SM)");
+static_assert(OFF_A % 16 == 0 && OFF_TP % 16 == 0 && OFF_Y % 16 == 0 && OFF_GATES % 16 == 0, "alignment");
+static_assert(kSmemBytes <= 226 * 1024, "shared memory budget (one CTA per SM)");
 
 // byte offset of (row, col) in a 64-column operand tile
 __host__ __device__ constexpr uint32_t sq_off(int row, int col) {
   return (uint32_t)(row / 8) * kRg64 + (uint32_t)(col / 4) * kLbo + (uint32_t)(row % 8) * 16 + (uint32_t)(col % 4) * 4;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));  // results below 2^-126 flush to 0
+  return y;
 }
 
 // Gam(j, t) for j <= t (j = -1: E_t)
@@ -151,8 +162,7 @@ __device__ __forceinline__ float gam(const ChunkGates &G, int j, int t) {
   if (G.seg[t] > j) return 0.f;
   const float c0 = j >= 0 ? G.cum[j] : 0.f;
   const int n0 = j >= 0 ? G.nneg[j] : 0;
-  float m;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(m) : "f"(G.cum[t] - c0));  // Gam < 2^-126 flushes to 0
+  const float m = ex2(G.cum[t] - c0);
   return ((G.nneg[t] - n0) & 1) ? -m : m;
 }
 
@@ -187,7 +197,7 @@ __device__ __forceinline__ bool named_any_rows(bool v) {
 
 struct Bars {
   uint64_t kq, kt, gates, split, ab, xt, dd;  // arrivals
-  uint64_t g, p, r, d, o, u;                  // MMA commits
+  uint64_t g, pr, d, o, u;                    // MMA commits
 };
 
 // 64 TMEM columns of this thread's lane as floats, one wait
@@ -204,6 +214,105 @@ __device__ __forceinline__ void ld64(uint32_t taddr, float (&x)[kC]) {
     x[16 + e] = __uint_as_float(b[e]);
     x[32 + e] = __uint_as_float(c[e]);
     x[48 + e] = __uint_as_float(d[e]);
+  }
+}
+
+__device__ __forceinline__ void sts_split4(uint8_t *sm, uint32_t off_hi, uint32_t off_lo, float4 f) {
+  uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+  tc::split_tf32(f.x, h0, l0);
+  tc::split_tf32(f.y, h1, l1);
+  tc::split_tf32(f.z, h2, l2);
+  tc::split_tf32(f.w, h3, l3);
+  *reinterpret_cast<uint4 *>(sm + off_hi) = make_uint4(h0, h1, h2, h3);
+  *reinterpret_cast<uint4 *>(sm + off_lo) = make_uint4(l0, l1, l2, l3);
+}
+
+// T = (I + A)^-1 by 16 x 16 blocks, on the 128 row threads (rows and the
+// diagonal of T packed by rows at Tp; A packed by rows at Ap; Y is scratch).
+//   diagonal blocks:  T_bb = (I + A_bb)^-1 by forward substitution, thread
+//                     16 b + jj forming column jj of T_bb;
+//   level L = 1..3:   Y_ab = sum_(b<=m<a) A_am T_mb, then T_ab = -T_aa Y_ab,
+//                     for a = b + L; one work item = (block, row, 4 columns).
+// Row offsets inside a 16-row block: the rows 16 m + i of a packed triangle
+// start at row(16 m) + 16 m i + row(i) (each row of the block is 16 m longer
+// than row i of the first block), so only row(16 m) is formed at run time.
+__device__ __forceinline__ float4 mask_above(float4 v, int col0, int row) {  // zero the entries with col > row
+  if (col0 > row) v.x = 0.f;
+  if (col0 + 1 > row) v.y = 0.f;
+  if (col0 + 2 > row) v.z = 0.f;
+  if (col0 + 3 > row) v.w = 0.f;
+  return v;
+}
+__device__ __forceinline__ void fma4(float4 &acc, float s, const float4 &v) {
+  acc.x = fmaf(s, v.x, acc.x);
+  acc.y = fmaf(s, v.y, acc.y);
+  acc.z = fmaf(s, v.z, acc.z);
+  acc.w = fmaf(s, v.w, acc.w);
+}
+__device__ __forceinline__ void invert_unit_lower(const float *Ap, float *Tp, float *Y, int r) {
+  if (r < kC) {
+    const int b = r / 16, jj = r % 16, b16 = 16 * b;
+    const float *ab = Ap + a_row(b16) + b16;  // + 16 b tt + a_row(tt) + n gives A(16 b + tt, 16 b + n)
+    float acc[16];
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) acc[tt] = tt == jj ? 1.f : 0.f;
+#pragma unroll
+    for (int n = 0; n < 15; ++n) {
+      const float tn = acc[n];
+#pragma unroll
+      for (int tt = n + 1; tt < 16; ++tt) acc[tt] = fmaf(-ab[b16 * tt + a_row(tt) + n], tn, acc[tt]);
+    }
+    float *tb = Tp + t_row(b16) + b16 + jj;  // + 16 b tt + t_row(tt) gives T(16 b + tt, 16 b + jj)
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt)
+      if (tt >= jj) tb[b16 * tt + t_row(tt)] = acc[tt];
+  }
+  named_sync_rows();
+  float4 *Y4 = reinterpret_cast<float4 *>(Y);
+#pragma unroll 1
+  for (int L = 1; L < 4; ++L) {
+    const int nitems = (4 - L) * 64;
+    // Y_ab(i, 4 q .. 4 q + 3) = sum over m in [b, a) and kk of A(16 a + i, 16 m + kk) T(16 m + kk, 16 b + 4 q ..)
+#pragma unroll 1
+    for (int e = r; e < nitems; e += kRowThreads) {
+      const int bb = e / 64, i = (e / 4) % 16, q = e % 4, a = bb + L, col = 16 * bb + 4 * q;
+      const float *arow = Ap + a_row(16 * a + i);
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+      for (int m = bb; m < a; ++m) {
+        const int m16 = 16 * m;
+        const float *tm = Tp + t_row(m16) + col;  // + 16 m kk + t_row(kk) gives T(16 m + kk, col)
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float4 av = *reinterpret_cast<const float4 *>(arow + m16 + 4 * k4);
+          const float as[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int kk = 4 * k4 + e2;
+            const float4 tv = mask_above(*reinterpret_cast<const float4 *>(tm + m16 * kk + t_row(kk)), col, m16 + kk);
+            fma4(y, as[e2], tv);
+          }
+        }
+      }
+      Y4[e] = y;  // [block][row i][4-column group q]
+    }
+    named_sync_rows();
+    // T_ab(i, 4 q ..) = -sum over kk <= i of T(16 a + i, 16 a + kk) Y_ab(kk, 4 q ..)
+#pragma unroll 1
+    for (int e = r; e < nitems; e += kRowThreads) {
+      const int bb = e / 64, i = (e / 4) % 16, q = e % 4, a = bb + L;
+      float *trow = Tp + t_row(16 * a + i);
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 tv = mask_above(*reinterpret_cast<const float4 *>(trow + 16 * a + 4 * k4), 4 * k4, i);
+        const float ts[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) fma4(t, ts[e2], Y4[bb * 64 + (4 * k4 + e2) * 4 + q]);
+      }
+      *reinterpret_cast<float4 *>(trow + 16 * bb + 4 * q) = make_float4(-t.x, -t.y, -t.z, -t.w);
+    }
+    named_sync_rows();
   }
 }
 
@@ -251,8 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
     mbar_init(&bars.xt, kRowThreads);
     mbar_init(&bars.dd, kRowThreads);
     mbar_init(&bars.g, 1);
-    mbar_init(&bars.p, 1);
-    mbar_init(&bars.r, 1);
+    mbar_init(&bars.pr, 1);
     mbar_init(&bars.d, 1);
     mbar_init(&bars.o, 1);
     mbar_init(&bars.u, 1);
@@ -274,23 +382,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
   if (warp < 4) {
     // ======================================================= row warps
     const int r = tid;
-    // MMA issue (thread 0): three tf32 passes (hi.hi, hi.lo, lo.hi) per product
+    // MMA issue (thread 0): three tf32 passes (hi.hi, hi.lo, lo.hi) per
+    // product.  The issue loops stay rolled and advance the descriptors by
+    // constants (the start address sits in the descriptor's low bits): a k
+    // step of 8 tf32 columns is 256 bytes along a 128-column tile, 288 bytes
+    // along a 64-column tile, 8 columns of a TMEM operand.
     const uint32_t kqhi = smem_u32(sm + OFF_KQHI), kqlo = smem_u32(sm + OFF_KQLO);
     const uint32_t kthi = smem_u32(sm + OFF_KTHI), ktlo = smem_u32(sm + OFF_KTLO);
     const uint32_t thi = smem_u32(sm + OFF_THI), tlo = smem_u32(sm + OFF_TLO);
     const uint32_t bhi = smem_u32(sm + OFF_BHI), blo = smem_u32(sm + OFF_BLO);
     constexpr uint32_t id64 = tc::idesc_tf32(128, 64, false);
     constexpr uint32_t id128 = tc::idesc_tf32(128, 128, false);
-    uint64_t *last = nullptr;  // the last commit's barrier and phase (thread 0)
+    uint64_t *last = nullptr;  // the last commit's barrier and phase (threads 0 and 32)
     uint32_t last_par = 0;
     auto commit = [&](uint64_t *bar, uint32_t par) {
       tc::mma_commit(bar);
       last = bar, last_par = par;
     };
-    // The issue loops stay rolled and advance the descriptors by constants
-    // (the start address sits in the descriptor's low bits): a k step of 8
-    // tf32 columns is 256 bytes along a 128-column tile, 288 bytes along a
-    // 64-column tile, 8 columns of a TMEM operand.
     // [K;Q] (128 rows) x K (64 rows)^T -> T_R
     auto issue_gram = [&]() {
 #pragma unroll 1
@@ -298,18 +406,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
         uint64_t ad = tc::smem_desc(ps == 2 ? kqlo : kqhi, 128, kKqRg);
         uint64_t bd = tc::smem_desc(ps == 1 ? kqlo : kqhi, 128, kKqRg);
 #pragma unroll 1
-        for (int s = 0; s < kDK / 8; ++s, ad += 256 >> 4, bd += 256 >> 4)
-          tc::mma_ss(tmem + T_R, ad, bd, id64, (ps | s) != 0);
+        for (int s = 0; s < kDK / 8; s += 4, ad += 4 * (256 >> 4), bd += 4 * (256 >> 4)) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            tc::mma_ss(tmem + T_R, ad + u * (256 >> 4), bd + u * (256 >> 4), id64, (ps | s | u) != 0);
+        }
       }
     };
-    // S x (K or Q)^T -> d  (K = 128 channels)
-    auto issue_sk = [&](uint32_t d, uint32_t b_off_bytes) {
+    // S x [K;Q]^T -> T_P (P) | T_R (R)
+    auto issue_pr = [&]() {
 #pragma unroll 1
       for (int ps = 0; ps < 3; ++ps) {
         uint32_t a = tmem + (ps == 2 ? T_SLO : T_SHI);
-        uint64_t bd = tc::smem_desc((ps == 1 ? kqlo : kqhi) + b_off_bytes, 128, kKqRg);
+        uint64_t bd = tc::smem_desc(ps == 1 ? kqlo : kqhi, 128, kKqRg);
 #pragma unroll 1
-        for (int s = 0; s < kDK / 8; ++s, a += 8, bd += 256 >> 4) tc::mma_ts(tmem + d, a, bd, id64, (ps | s) != 0);
+        for (int s = 0; s < kDK / 8; s += 4, a += 32, bd += 4 * (256 >> 4)) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tc::mma_ts(tmem + T_P, a + 8 * u, bd + u * (256 >> 4), id128, (ps | s | u) != 0);
+        }
       }
     };
     // (a_hi, a_lo: TMEM, 64 columns) x (b_hi, b_lo: 64-column smem tiles, N rows)^T -> d
@@ -320,12 +434,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
         uint32_t a = tmem + (ps == 2 ? a_lo : a_hi);
         uint64_t bd = tc::smem_desc(ps == 1 ? b_lo : b_hi, kLbo, kRg64);
 #pragma unroll 1
-        for (int s = 0; s < kC / 8; ++s, a += 8, bd += (2 * kLbo) >> 4)
-          tc::mma_ts(tmem + d, a, bd, idesc, acc || (ps | s) != 0);
+        for (int s = 0; s < kC / 8; s += 4, a += 32, bd += 4 * ((2 * kLbo) >> 4)) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            tc::mma_ts(tmem + d, a + 8 * u, bd + u * ((2 * kLbo) >> 4), idesc, acc || (ps | s | u) != 0);
+        }
       }
     };
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     const bool row_ok = r < dv;
+    float *Ap = reinterpret_cast<float *>(sm + OFF_A);
+    float *Tp = reinterpret_cast<float *>(sm + OFF_TP);
+    float *Yp = reinterpret_cast<float *>(sm + OFF_Y);
     // initial state -> TMEM (zero when cold; rows >= dv stay zero)
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
@@ -375,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
         commit(&bars.g, par);
       }
       __syncwarp();
-      // ---- 1: split S into the tf32 A operands of P and R, decay S in place
+      // ---- 1: split S into the tf32 A operands of P | R, decay S in place
       bool ok = ok0 && (c == 0 || wait_or_abort(&bars.u, par ^ 1, lim, p.status, abort_flag)) &&
                 wait_or_abort(&bars.gates, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
@@ -399,12 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(&bars.split);
-      if (r == 0 && (ok0 = wait_or_abort(&bars.split, par, lim, p.status, abort_flag))) {
-        tc::fence_after_sync();
-        issue_sk(T_P, 0);  // P = S K^T
-        commit(&bars.p, par);
-      }
-      __syncwarp();
 
       // v_t[r] of this chunk, in flight while A and B are formed
       float x[kC];
@@ -412,167 +526,103 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       for (int t = 0; t < kC; ++t)
         x[t] = (t < nt && row_ok) ? __ldg(p.v + ((tb + t) * p.Hv + h) * dv + r) : 0.f;
 
-      // ---- 2: A (by columns, threads 0-63) and B (by rows, threads 64-127),
-      // packed fp32, 16 Gram columns at a time
+      // ---- 2: row r of A (r < 64: A_rj = b_r Gam(j,r) G_rj, j < r, packed
+      // to smem) or of B (r >= 64: B_tj = Gam(j,t) M_jt, j <= t, t = r - 64,
+      // kept in registers until its operand tile is free), from the Gram
+      // accumulator's lane r (k_r.k_j for r < 64, q_t.k_j for r >= 64)
       ok = ok0 && wait_or_abort(&bars.g, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
+      float brow[kC];
       {
-        float *As = reinterpret_cast<float *>(sm + OFF_A);
-        float *Bs = reinterpret_cast<float *>(sm + OFF_B);
-        const bool is_a = r < kC;
-        const int j = r, t = r - kC;  // A column j / B row t of this thread
-#pragma unroll 1
-        for (int n0 = 0; n0 < kC; n0 += 4) {  // Gram columns (tokens) n0 .. n0 + 3
-          uint32_t gv[4];
-          tc::tmem_ld4(tl + T_R + n0, gv);
-          tc::tmem_wait_ld();
-          float f[4];
-          if (is_a && n0 >= a0_of(j)) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tt = n0 + e;
-              f[e] = tt > j ? G.beta[tt] * gam(G, j, tt) * __uint_as_float(gv[e]) : 0.f;
-            }
-            *reinterpret_cast<float4 *>(As + a_off(j) + (n0 - a0_of(j))) = make_float4(f[0], f[1], f[2], f[3]);
-          } else if (!is_a && n0 < b1_of(t)) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int jj = n0 + e;
-              f[e] = jj <= t ? gam(G, jj, t) * __uint_as_float(gv[e]) : 0.f;
-            }
-            *reinterpret_cast<float4 *>(Bs + b_off(t) + n0) = make_float4(f[0], f[1], f[2], f[3]);
-          }
-          __syncwarp();  // reconverged for the next warp-wide TMEM load
-        }
+        const int t = r < kC ? r : r - kC;
+        const float ct = G.cum[t], bt = G.beta[t];
+        const int st = G.seg[t], nt_neg = G.nneg[t];
+        ld64(tl + T_R, brow);  // the Gram row, weighted in place
         tc::fence_before_sync();
-        mbar_arrive(&bars.ab);  // every Gram column read: free for R
+        mbar_arrive(&bars.ab);  // the Gram columns are read: free for R
+#pragma unroll
+        for (int j = 0; j < kC; ++j) {
+          const float m = ex2(ct - G.cum[j]);
+          const float gm = st > j ? 0.f : (((nt_neg - G.nneg[j]) & 1) ? -m : m);  // Gam(j, t) for j <= t
+          brow[j] *= gm;
+        }
+        if (r < kC) {
+          float *arow = Ap + a_row(t);
+#pragma unroll
+          for (int j4 = 0; j4 < kC; j4 += 4)
+            if (j4 < a1_of(t))
+              *reinterpret_cast<float4 *>(arow + j4) =
+                  make_float4(j4 < t ? bt * brow[j4] : 0.f, j4 + 1 < t ? bt * brow[j4 + 1] : 0.f,
+                              j4 + 2 < t ? bt * brow[j4 + 2] : 0.f, j4 + 3 < t ? bt * brow[j4 + 3] : 0.f);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kC; ++j)
+            if (j > t) brow[j] = 0.f;
+        }
       }
-      named_sync_rows();  // A and B visible to every row thread
-      if (r == 0 && (ok0 = wait_or_abort(&bars.ab, par, lim, p.status, abort_flag))) {
+      named_sync_rows();  // A visible to every row thread
+      if (r == 0 && (ok0 = wait_or_abort(&bars.split, par, lim, p.status, abort_flag) &&
+                           wait_or_abort(&bars.ab, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
-        issue_sk(T_R, kQRow0);  // R = S Q^T
-        commit(&bars.r, par);
+        issue_pr();  // P | R = S [K;Q]^T
+        commit(&bars.pr, par);
       }
       __syncwarp();
 
-      // ---- 3: x_t = b_t (v_t - E_t P_t), once P is done (P is also the last
-      // reader of the k rows, which T then overlays)
-      ok = ok0 && wait_or_abort(&bars.p, par, lim, p.status, abort_flag);
+      // ---- 3: T = (I + A)^-1 (fp32, packed), while P | R runs
+      invert_unit_lower(Ap, Tp, Yp, r);
+
+      // ---- 4: once P | R is done (the last reader of S hi / lo and of the
+      // [K;Q] tiles): X = b o (v - E o P) -> tf32 hi / lo, R <- E o R, T and
+      // B -> tf32 operand tiles
+      ok = ok0 && wait_or_abort(&bars.pr, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
       {
-        // x replaces P in TMEM until R is done (X then goes out as tf32 hi / lo)
         float pv[kC];
         ld64(tl + T_P, pv);
 #pragma unroll
+        for (int t = 0; t < kC; ++t) x[t] = G.beta[t] * (x[t] - G.E[t] * pv[t]);
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
-          uint32_t w[16];
+          uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int t = 16 * q + e;
-            w[e] = __float_as_uint(G.beta[t] * (x[t] - G.E[t] * pv[t]));
-          }
-          tc::tmem_st16(tl + T_P + 16 * q, w);
+          for (int e = 0; e < 16; ++e) tc::split_tf32(x[16 * q + e], hi[e], lo[e]);
+          tc::tmem_st16(tl + T_XHI + 16 * q, hi);
+          tc::tmem_st16(tl + T_XLO + 16 * q, lo);
         }
       }
-      // column r of T = (I + A)^-1 (threads 0-63), 16 rows at a time:
-      // T_tr = [t == r] - sum_(n<t) A_tn T_nr, the rows of earlier blocks read
-      // back from the operand (hi + lo), the block's own rows by forward
-      // substitution; each block is stored as tf32 hi / lo as soon as it is done
-      if (r < kC) {
-        const float *As = reinterpret_cast<const float *>(sm + OFF_A);
-        const uint32_t cj = (uint32_t)(r / 4) * kLbo + (uint32_t)(r % 4) * 4;  // column r within a row
-#pragma unroll 1
-        for (int tb = 0; tb < kC / 16; ++tb) {
-          float acc[16];
-#pragma unroll
-          for (int tt = 0; tt < 16; ++tt) acc[tt] = 16 * tb + tt == r ? 1.f : 0.f;
-#pragma unroll 1
-          for (int nb = 0; nb < tb; ++nb) {
-            float tn[16];
-#pragma unroll
-            for (int nn = 0; nn < 16; ++nn) {
-              const uint32_t o = (uint32_t)(2 * nb + nn / 8) * kRg64 + (uint32_t)(nn % 8) * 16 + cj;
-              tn[nn] = __uint_as_float(*reinterpret_cast<const uint32_t *>(sm + OFF_THI + o)) +
-                       __uint_as_float(*reinterpret_cast<const uint32_t *>(sm + OFF_TLO + o));
-            }
-#pragma unroll
-            for (int nn = 0; nn < 16; ++nn) {
-              const int n = 16 * nb + nn;
-              const float *col = As + a_off(n) - a0_of(n) + 16 * tb;  // + tt gives A(16 tb + tt, n)
-#pragma unroll
-              for (int t4 = 0; t4 < 16; t4 += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(col + t4);
-                acc[t4] = fmaf(-a4.x, tn[nn], acc[t4]);
-                acc[t4 + 1] = fmaf(-a4.y, tn[nn], acc[t4 + 1]);
-                acc[t4 + 2] = fmaf(-a4.z, tn[nn], acc[t4 + 2]);
-                acc[t4 + 3] = fmaf(-a4.w, tn[nn], acc[t4 + 3]);
-              }
-            }
-          }
-#pragma unroll
-          for (int nn = 0; nn < 15; ++nn) {
-            const int n = 16 * tb + nn;
-            const float *col = As + a_off(n) - a0_of(n) + 16 * tb;
-            const float tv = acc[nn];
-#pragma unroll
-            for (int t4 = 4 * ((nn + 1) / 4); t4 < 16; t4 += 4) {
-              const float4 a4 = *reinterpret_cast<const float4 *>(col + t4);
-              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (t4 + e > nn) acc[t4 + e] = fmaf(-av[e], tv, acc[t4 + e]);
-            }
-          }
-#pragma unroll
-          for (int tt = 0; tt < 16; ++tt) {
-            uint32_t hi, lo;
-            tc::split_tf32(acc[tt], hi, lo);
-            const uint32_t o = (uint32_t)(2 * tb + tt / 8) * kRg64 + (uint32_t)(tt % 8) * 16 + cj;
-            *reinterpret_cast<uint32_t *>(sm + OFF_THI + o) = hi;
-            *reinterpret_cast<uint32_t *>(sm + OFF_TLO + o) = lo;
-          }
-        }
-      }
-      // once R is done (the last reader of S hi / lo and of the q rows):
-      // X -> TMEM, B -> smem operand, R <- E o R
-      ok = ok0 && wait_or_abort(&bars.r, par, lim, p.status, abort_flag);
-      if (named_any_rows(!ok)) break;
-      tc::fence_after_sync();
-      tc::tmem_wait_st();
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
-        // X hi / lo from x, and R <- E o R, 16 columns at a time
-        uint32_t w[16], hi[16], lo[16];
-        tc::tmem_ld16(tl + T_P + 16 * q, w);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) tc::split_tf32(__uint_as_float(w[e]), hi[e], lo[e]);
-        tc::tmem_st16(tl + T_XHI + 16 * q, hi);
-        tc::tmem_st16(tl + T_XLO + 16 * q, lo);
+        uint32_t w[16];
         tc::tmem_ld16(tl + T_R + 16 * q, w);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(G.E[16 * q + e] * __uint_as_float(w[e]));
         tc::tmem_st16(tl + T_R + 16 * q, w);
       }
-      if (r >= kC) {
-        // row t of B from its packed row (zero beyond b1(t))
-        const int t = r - kC;
-        const float *row = reinterpret_cast<const float *>(sm + OFF_B) + b_off(t);
-        const int b1 = b1_of(t);
+      // T operand: row r / 2, columns 32 (r % 2) .. + 31, from the packed rows
+      {
+        const int t = r >> 1, j0 = 32 * (r & 1);
+        const float *trow = Tp + t_row(t);
 #pragma unroll 1
-        for (int j4 = 0; j4 < kC; j4 += 4) {
-          const float4 b4 = j4 < b1 ? *reinterpret_cast<const float4 *>(row + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-          tc::split_tf32(b4.x, h0, l0);
-          tc::split_tf32(b4.y, h1, l1);
-          tc::split_tf32(b4.z, h2, l2);
-          tc::split_tf32(b4.w, h3, l3);
-          *reinterpret_cast<uint4 *>(sm + OFF_BHI + sq_off(t, j4)) = make_uint4(h0, h1, h2, h3);
-          *reinterpret_cast<uint4 *>(sm + OFF_BLO + sq_off(t, j4)) = make_uint4(l0, l1, l2, l3);
+        for (int j4 = j0; j4 < j0 + 32; j4 += 4) {
+          // the packed row's slots above the diagonal are never written: zero them here
+          float4 v4 = j4 < b1_of(t) ? *reinterpret_cast<const float4 *>(trow + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j4 > t) v4.x = 0.f;
+          if (j4 + 1 > t) v4.y = 0.f;
+          if (j4 + 2 > t) v4.z = 0.f;
+          if (j4 + 3 > t) v4.w = 0.f;
+          sts_split4(sm, OFF_THI + sq_off(t, j4), OFF_TLO + sq_off(t, j4), v4);
         }
+      }
+      if (r >= kC) {
+        const int t = r - kC;
+#pragma unroll
+        for (int j4 = 0; j4 < kC; j4 += 4)
+          sts_split4(sm, OFF_BHI + sq_off(t, j4), OFF_BLO + sq_off(t, j4),
+                     make_float4(brow[j4], brow[j4 + 1], brow[j4 + 2], brow[j4 + 3]));
       }
       tc::tmem_wait_st();
       fence_proxy_async_smem();  // T and B written by the generic proxy, read by the MMA
@@ -585,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       }
       __syncwarp();
 
-      // ---- 4: D -> tf32 hi / lo (A of O and of the update)
+      // ---- 5: D -> tf32 hi / lo (A of O and of the update)
       ok = ok0 && wait_or_abort(&bars.d, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
@@ -602,19 +652,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(&bars.dd);
+      // O (thread 0) and the update (thread 32) are independent products on
+      // the same A operand: two issuing threads keep the tensor core fed
       if (r == 0 && (ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
         issue_t64(T_R, T_DHI, T_DLO, bhi, blo, id64, true);  // O = E o R + D B^T
         commit(&bars.o, par);
-        if ((ok0 = wait_or_abort(&bars.kt, par, lim, p.status, abort_flag))) {
-          tc::fence_after_sync();
-          issue_t64(T_S, T_DHI, T_DLO, kthi, ktlo, id128, true);  // S += D (F o K)
-          commit(&bars.u, par);
-        }
+      } else if (r == 32 && (ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag) &&
+                                   wait_or_abort(&bars.kt, par, lim, p.status, abort_flag))) {
+        tc::fence_after_sync();
+        issue_t64(T_S, T_DHI, T_DLO, kthi, ktlo, id128, true);  // S += D (F o K)
+        commit(&bars.u, par);
       }
       __syncwarp();
 
-      // ---- 5: outputs
+      // ---- 6: outputs
       ok = ok0 && wait_or_abort(&bars.o, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
@@ -670,17 +722,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
         }
       }
     }
-    // every MMA issued must be complete before the TMEM is freed
-    if (r == 0 && last) mbar_wait_bounded(last, last_par, p.drain_limit_ns);
+    // every MMA issued must be complete before the TMEM is freed (threads 0
+    // and 32 each wait for their own last commit)
+    if ((r == 0 || r == 32) && last) mbar_wait_bounded(last, last_par, p.drain_limit_ns);
     tc::fence_before_sync();
   } else {
     // ======================================================= producers
     const int pt = tid - kProd0, pw = pt >> 5;
     const int al = lane & 7, bl = lane >> 3;
     const float *qg = p.q, *kg = p.k;
-    float4 kr[2][2][4];  // next chunk's k: [token block half][channel block half][token in block]
-    // this thread's 4 x 4 blocks: tokens 4a..4a+3, channels 4b..4b+3 with
-    // a = al + 8 ah, b = bl + 4 pw + 16 bh
+    // the next chunk's k and q: [token block half][channel block half][token in
+    // block]; this thread's 4 x 4 blocks are tokens 4a..4a+3, channels
+    // 4b..4b+3 with a = al + 8 ah, b = bl + 4 pw + 16 bh
+    float4 kr[2][2][4], qr[2][2][4];
     auto load_rows = [&](const float *src, int c, float4 (&dst)[2][2][4]) {
       const int nt = min(kC, t1 - t0 - c * kC);
       const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
@@ -695,15 +749,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
           }
     };
-    auto st_split4 = [&](uint32_t off_hi, uint32_t off_lo, float4 f) {
-      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-      tc::split_tf32(f.x, h0, l0);
-      tc::split_tf32(f.y, h1, l1);
-      tc::split_tf32(f.z, h2, l2);
-      tc::split_tf32(f.w, h3, l3);
-      *reinterpret_cast<uint4 *>(sm + off_hi) = make_uint4(h0, h1, h2, h3);
-      *reinterpret_cast<uint4 *>(sm + off_lo) = make_uint4(l0, l1, l2, l3);
-    };
     // token-major rows: k at row j, q at row 64 + j
     auto store_rows = [&](const float4 (&src)[2][2][4], int row0) {
 #pragma unroll
@@ -714,14 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
           for (int u = 0; u < 4; ++u) {
             const int j = row0 + 4 * (al + 8 * ah) + u, b = bl + 4 * pw + 16 * bh;
             const uint32_t o = (uint32_t)(j / 8) * kKqRg + (uint32_t)b * 128 + (uint32_t)(j % 8) * 16;
-            st_split4(OFF_KQHI + o, OFF_KQLO + o, src[ah][bh][u]);
+            sts_split4(sm, OFF_KQHI + o, OFF_KQLO + o, src[ah][bh][u]);
           }
-    };
-    auto store_kq = [&](int c) {
-      store_rows(kr, 0);
-      float4 qr[2][2][4];
-      load_rows(qg, c, qr);
-      store_rows(qr, kC);
     };
     // channel-major F o K: K[j][c] F_j at (channel c, token j)
     auto store_kt = [&](const ChunkGates &G) {
@@ -741,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
           for (int e = 0; e < 4; ++e) {
             const int ch = 4 * b + e;
             const uint32_t o = (uint32_t)(ch / 8) * kRg64 + (uint32_t)a * kLbo + (uint32_t)(ch % 8) * 16;
-            st_split4(OFF_KTHI + o, OFF_KTLO + o, make_float4(col[e][0], col[e][1], col[e][2], col[e][3]));
+            sts_split4(sm, OFF_KTHI + o, OFF_KTLO + o, make_float4(col[e][0], col[e][1], col[e][2], col[e][3]));
           }
         }
       }
@@ -803,17 +842,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
       if (lane == 0) mbar_arrive(&bars.gates);
     };
 
-    // Chunk c + 1 is prepared during chunk c: its k is loaded first; after
-    // R(c) its gates are formed; after O(c) (the last reader of the tiles
-    // that T and B overlay) the [K; Q] tiles are stored; after the update of
-    // chunk c the channel-major F o K.  Every producer waits for the gates of
-    // chunk c + 1 before it stores the [K; Q] tiles, so the gate barrier is
-    // never two phases ahead of a waiting producer.
+    // Chunk c + 1 is prepared during chunk c: its k and q are loaded first;
+    // after P | R (c) its gates are formed; after O (c) (the last reader of
+    // the tiles that T and B overlay) the [K; Q] tiles are stored; after the
+    // update of chunk c the channel-major F o K.  Every producer waits for
+    // the gates of chunk c + 1 before it stores the [K; Q] tiles, so the gate
+    // barrier is never two phases ahead of a waiting producer.
     if (nch > 0) {
       load_rows(kg, 0, kr);
+      load_rows(qg, 0, qr);
       if (pw == 0) form_gates(0);
       if (wait_or_abort(&bars.gates, 0, lim, p.status, abort_flag)) {
-        store_kq(0);
+        store_rows(kr, 0);
+        store_rows(qr, kC);
         fence_proxy_async_smem();
         mbar_arrive(&bars.kq);
         store_kt(gates[0]);
@@ -824,12 +865,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
     for (int c = 0; c + 1 < nch && !*abort_flag; ++c) {
       const uint32_t par = c & 1, npar = par ^ 1;
       load_rows(kg, c + 1, kr);
-      if (!wait_or_abort(&bars.r, par, lim, p.status, abort_flag)) break;
+      load_rows(qg, c + 1, qr);
+      if (!wait_or_abort(&bars.pr, par, lim, p.status, abort_flag)) break;
       if (pw == 0) form_gates(c + 1);
       if (!wait_or_abort(&bars.gates, npar, lim, p.status, abort_flag) ||
           !wait_or_abort(&bars.o, par, lim, p.status, abort_flag))
         break;
-      store_kq(c + 1);
+      store_rows(kr, 0);
+      store_rows(qr, kC);
       fence_proxy_async_smem();
       mbar_arrive(&bars.kq);
       if (!wait_or_abort(&bars.u, par, lim, p.status, abort_flag)) break;
