@@ -286,14 +286,21 @@ typedef struct {
   const float *alpha;        /* device [T, Hv] */
   const float *beta;         /* device [T, Hv] */
   float *out;                /* device [T, Hv, dv] */
+  void *workspace;           /* CHUNKED only: device scratch of at least workspace_bytes
+                                (lsc_gdn_recurrent_workspace_bytes), 16-byte aligned, free
+                                until the call's work on the stream completes; NULL = the
+                                library takes it from the device's stream-ordered pool
+                                (cudaMallocAsync / cudaFreeAsync on the call's stream) */
+  size_t workspace_bytes;
 } lsc_gdn_recurrent_args;
 
 /* Evaluation order of lsc_gdn_recurrent (both give the token recurrence's
  * result up to fp32 rounding). */
 #define LSC_RECURRENT_AUTO 0    /* the library's choice (currently TOKEN, the faster one) */
 #define LSC_RECURRENT_TOKEN 1   /* one token at a time */
-#define LSC_RECURRENT_CHUNKED 2 /* 16 tokens at a time: the token recurrence rearranged into
-                                   per-chunk products (head_k_dim 128 only) */
+#define LSC_RECURRENT_CHUNKED 2 /* 64 tokens at a time on the tensor cores: the token recurrence
+                                   rearranged into per-chunk products (head_k_dim 128 only);
+                                   needs a workspace (see lsc_gdn_recurrent_workspace_bytes) */
 
 /*
  * Gated delta rule of a resumed prefill ([KP] "相同前缀不一定能全部复用":
@@ -310,6 +317,18 @@ typedef struct {
  */
 int lsc_gdn_recurrent(lsc_pool *pool, int32_t layer, const lsc_gdn_recurrent_args *args,
                       void *stream);
+
+/*
+ * Device scratch that lsc_gdn_recurrent needs for `args` (its n_seq,
+ * total_tokens and algorithm; the pool gives num_v_heads and head_k_dim): 0
+ * for TOKEN; for CHUNKED one 33 344-byte record per (64-token chunk slot,
+ * v head), with (total_tokens + 63) / 64 + n_seq chunk slots -- the records of
+ * the state-free quantities of every chunk (lsc_chunk.h), written by the
+ * call's first kernel and read by its second.  Host only, no device work.
+ * INVALID_ARG for a NULL pointer or a negative size.
+ */
+int lsc_gdn_recurrent_workspace_bytes(const lsc_pool *pool, const lsc_gdn_recurrent_args *args,
+                                      size_t *bytes);
 
 /* Arguments of lsc_gdn_prefill_conv.  T = total_tokens; sequence i owns tokens
  * cu_seqlens[i] .. cu_seqlens[i+1]-1 of x, q, k and v. */

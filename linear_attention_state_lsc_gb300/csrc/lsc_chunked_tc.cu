@@ -1,8 +1,9 @@
-// lsc_chunked_tc.cu -- the resumed-prefill GDN recurrence evaluated 64 tokens
-// at a time on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
-// Same token-ordered result as the token-by-token kernels (per token
-// S' = a S (I - b k k^T) + b v k^T, o = S' q), rearranged so that the work of
-// a chunk is a handful of matrix products plus a small triangular inverse.
+// lsc_chunked_tc.cu -- the state kernel of the chunked gated delta rule on the
+// 5th-generation tensor cores (tcgen05, TMEM accumulators): the resumed-prefill
+// recurrence run 64 tokens at a time from the restored state, with the
+// state-free quantities of every chunk (T', B, E, F, e_last; lsc_chunk.h) read
+// from the workspace records that the preparation kernel (lsc_chunk_prep.cu)
+// wrote before it on the same stream.
 //
 // Sources, cited by page title and section:
 //   [VA] "非连续 KV Cache" §6 (recurrent_gated_delta_rule, the token recurrence)
@@ -12,159 +13,74 @@
 // The pages give the token recurrence only; the chunked form is its algebraic
 // rearrangement, exact up to rounding.
 //
-// One chunk, tokens 0..C-1, from state S (dv x dk, rows r):
-//   Gam(j,t) = a_(j+1) ... a_t,  E_t = a_0 ... a_t,  F_j = Gam(j, C-1)
-//   P = S K^T, R = S Q^T (dv x C),  G_jt = k_j.k_t,  M_jt = k_j.q_t
-//   A_tj = b_t Gam(j,t) G_jt (j < t),  T = (I + A)^-1 (unit lower triangular)
-//   X_rt = b_t (v_t[r] - E_t P_rt),  D = X T^T    (d_t = x_t - sum_(j<t) A_tj d_j)
-//   B_tj = Gam(j,t) M_jt (j <= t),   O = E o R + D B^T   (o_t of every row)
-//   S' = E_(C-1) S + D (F o K)                     (the rank-C update)
-// Gam is formed from a per-chunk running sum of log2|a| (zeros and signs of a
-// tracked apart), so no product of gates under- or overflows on the way.
-//
-// Products on the tensor cores, in tf32 with an fp32 accumulator.  Every
-// operand x is split as x = hi + lo (hi = tf32(x), lo = tf32(x - hi)) and each
-// product is formed as hi.hi + hi.lo + lo.hi: about 22 significant bits per
-// operand, so the products carry fp32-level error (the dropped lo.lo term is
-// below 2^-21 of the product).  Per chunk and v head (M 128 = state rows):
-//   Gram    [K;Q] K^T           M 128 (k rows, q rows), N 64,  K 128 (smem)
-//   P | R   S [K;Q]^T           N 128, K 128   A = S from TMEM
-//   D       X T^T               N 64,  K 64    A = X from TMEM
-//   O       E o R + D B^T       N 64,  K 64    A = D from TMEM
-//   update  S += D (F o K)      N 128, K 64    A = D from TMEM
-// The state lives in TMEM as the update's accumulator and is decayed by
-// E_(C-1) in place each chunk.  The CUDA cores form A and B from the Gram
-// accumulator (one row per thread), invert I + A by 16 x 16 blocks (the
-// diagonal blocks by forward substitution, then three levels of block
-// products), and split the TMEM operands; one thread per state row.
+// Per chunk and v head (M 128 = state rows, thread r = row r = TMEM lane r):
+//   P'  = S (E o K)^T        N 64,  K 128   A = S from TMEM
+//   R'  = S (E o Q)^T        N 64,  K 128   A = S from TMEM
+//   D   = (V - P') T'^T      N 64,  K 64    A = X = V - P' from TMEM
+//   O   = R' + D B^T         N 64,  K 64    A = D from TMEM  (o_t of every row)
+//   S   = e_last S + D (F o K)   N 128, K 64    A = D from TMEM
+// Products in tf32 with an fp32 accumulator.  Every operand x is split as
+// x = hi + lo and each product formed as hi.hi + hi.lo + lo.hi: about 22
+// significant bits per operand, so the products carry fp32-level error (the
+// dropped lo.lo term is below 2^-21 of the product).  The tensor cores read a
+// 32-bit operand as tf32 by truncation (its low 13 bits ignored), so the state
+// in TMEM serves as its own hi part and only lo = tf32(S - trunc(S)) is
+// written; the other operands use hi = tf32 rounded to nearest.
 //
 // CTA = one (sequence, v head), 256 threads, one CTA per SM (TMEM: all 512
-// columns; shared memory: ~224 KB):
-//   warps 0-3   row warps: thread r owns state row r (TMEM lane r) and row r
-//               of A (r < 64) or of B (r >= 64); warp 0 allocates the TMEM
-//               and thread 0 issues the MMAs and commits once the operands
-//               they read are in place, thread 32 the state update beside
-//               thread 0's O product (two warps per SM sub-partition leave
-//               each thread up to 255 registers);
-//   warps 4-7   producers: load the next chunk's k and q from global memory
-//               into registers while the current chunk runs, split them and
-//               store them as tf32 operands (token-major [K; Q] once the
-//               current chunk's products that overlay that tile are done,
-//               channel-major F o K once its update is done), and form the
-//               next chunk's gate scan.
-// Hand-offs go through mbarriers: producer -> MMA (operands in shared
-// memory), row warps -> MMA (TMEM operands written, TMEM results read), MMA
-// -> row warps / producers (tcgen05.commit).  Every wait is bounded: on
-// expiry the thread records LSC_ERR_DEV_TIMEOUT, the CTA stops issuing work,
-// waits (bounded) for the MMAs it issued and frees its TMEM.  The per-chunk
-// code runs as rolled loops with small bodies: each chunk executes it once,
-// and straight-line code of that size would be fetched from L2 every chunk.
+// columns; shared memory ~201 KB):
+//   warps 0-3   row warps: thread r owns state row r; thread 0 issues P', R',
+//               D and O, thread 32 the state update (beside O), each once the
+//               operands it reads are in place;
+//   warps 4-7   producers: store the chunk's tf32 operand tiles into shared
+//               memory as the products that read the previous contents finish
+//               (E o K over the k half of the token-major tile, then T'; E o Q
+//               over the q half, then B; channel-major F o K), loading k, q
+//               and the records from global memory ahead of time.
+// Hand-offs go through mbarriers: producers -> MMA (tiles in shared memory),
+// row warps -> MMA (TMEM operands written, TMEM results read), MMA -> row
+// warps / producers (tcgen05.commit).  Every wait is bounded: on expiry the
+// thread records LSC_ERR_DEV_TIMEOUT, the CTA stops issuing work, waits
+// (bounded) for the MMAs it issued and frees its TMEM.
 //
-// Shared-memory operands (no swizzle, 8 x 16-byte core matrices):
-//   [K; Q] token-major: element (row i, channel c) at (i/8)*4112 + (c/4)*128 +
-//   (i%8)*16 + (c%4)*4 -- K-major with LBO 128, SBO 4112 (rows 0-63 k, 64-127 q);
-//   F o K channel-major: element (channel c, token j) at (c/8)*2304 +
-//   (j/4)*144 + (c%8)*16 + (j%4)*4 -- K-major with LBO 144, SBO 2304;
-//   T and B (64 x 64, row t, column j) at (t/8)*2304 + (j/4)*144 + (t%8)*16 +
-//   (j%4)*4: T over the k rows and B over the q rows of the [K; Q] tiles once
-//   P | R has read them.
-// The 16 bytes beyond each 4096 (resp. 128) spread the threads' stores over
-// all banks.
+// TMEM columns (lanes = state rows):
+//   0-127    S (fp32; the hi part of its own split)
+//   128-255  lo of S; after D: D hi (128-191), D lo (192-255)
+//   256-319  P'; after X is formed: D
+//   320-447  X hi (320-383), X lo (384-447)
+//   448-511  R', then O = R' + D B^T
+// Shared-memory tiles (no swizzle, lsc_chunk.h): the token-major [E o K; E o Q]
+// tile (hi, lo), T' over its k half once P' has read it, B over its q half
+// once R' has; F o K channel-major (hi, lo).
+#include "lsc_chunk.h"
 #include "lsc_gdn_common.cuh"
 #include "lsc_tc.h"
 
 namespace lsc {
 namespace {
 
-constexpr int kC = 64;        // tokens per chunk
-constexpr int kDK = 128;      // head_k_dim of this kernel
+using namespace chunk;
+
 constexpr int kThreads = 256;
 constexpr int kRowThreads = 128;
-constexpr int kProd0 = 128;   // first producer thread
+constexpr int kProd0 = 128;  // first producer thread
 constexpr uint32_t kTmemCols = 512;
 
-// TMEM columns (lane = state row for every accumulator and A operand)
-constexpr uint32_t T_S = 0;      // state, fp32 (128)
-constexpr uint32_t T_SHI = 128;  // tf32 hi of S (128)      -> X hi (64), X lo (64)
-constexpr uint32_t T_SLO = 256;  // tf32 lo of S (128)      -> D (64), D hi (64)
-constexpr uint32_t T_P = 384;    // P (64)                  -> x, then D lo (64)
-constexpr uint32_t T_R = 448;    // Gram (64), then R -> E o R -> O (64)
-constexpr uint32_t T_XHI = 128, T_XLO = 192;
-constexpr uint32_t T_D = 256, T_DHI = 320, T_DLO = 384;
-
-// shared-memory layout (bytes)
-constexpr uint32_t kKqRg = 4096 + 16;      // one 8-row group of the token-major tile
-constexpr uint32_t kKqBytes = 16 * kKqRg;  // 128 rows
-constexpr uint32_t kQRow0 = 8 * kKqRg;     // q rows start at row 64
-constexpr uint32_t kLbo = 128 + 16;        // one 4-column core-matrix column of a 64-column tile
-constexpr uint32_t kRg64 = 16 * kLbo;      // one 8-row group of a 64-column tile
-constexpr uint32_t kKtBytes = 16 * kRg64;  // channel-major K: 128 channel rows
-constexpr uint32_t kSqBytes = 8 * kRg64;   // T or B: 64 rows
-
-// Packed triangles (fp32), every row a multiple of 4 floats, 16-byte aligned:
-// A by rows (row t: columns j in [0, 4 ceil(t/4)), zero for j >= t), T by
-// rows including the diagonal (row t: columns j in [0, 4 floor(t/4) + 4),
-// zero for j > t).
-__host__ __device__ constexpr int a1_of(int t) { return 4 * ((t + 3) / 4); }
-__host__ __device__ constexpr int b1_of(int t) { return 4 * ((t + 4) / 4); }
-// sum over m = 1..n of floor(m / 4)
-__host__ __device__ constexpr int quarter_sum(int n) {
-  return n <= 0 ? 0 : 2 * (n / 4) * (n / 4 - 1) + (n / 4) * (n % 4 + 1);
-}
-__host__ __device__ constexpr int a_row(int t) { return 4 * quarter_sum(t + 2); }      // sum of a1_of(i), i < t
-__host__ __device__ constexpr int t_row(int t) { return 4 * t + 4 * quarter_sum(t - 1); }  // sum of b1_of(i), i < t
-static_assert(a_row(1) == 0 && a_row(2) == 4 && a_row(5) == 16 && t_row(1) == 4 && t_row(5) == 4 * 4 + 8, "packing");
-constexpr int kAFloats = a_row(kC);
-constexpr int kTFloats = t_row(kC);
-constexpr int kYFloats = 3 * 16 * 16;  // block-product scratch of the inverse
-
-// per-chunk gate quantities, formed by the producers (double-buffered)
-struct ChunkGates {
-  float beta[kC];
-  float cum[kC];   // running sum of log2|a_t| over the chunk (0 where a_t = 0)
-  float E[kC];     // a_0 ... a_t
-  float F[kC];     // Gam(t, C-1)
-  int32_t seg[kC];   // last t' <= t with a_t' = 0, or -1
-  int32_t nneg[kC];  // number of negative a_t' for t' <= t
-  float e_last;
-  int32_t pad[3];
-};
+constexpr uint32_t T_S = 0;
+constexpr uint32_t T_SLO = 128;
+constexpr uint32_t T_DHI = 128, T_DLO = 192;
+constexpr uint32_t T_P = 256, T_D = 256;
+constexpr uint32_t T_XHI = 320, T_XLO = 384;
+constexpr uint32_t T_R = 448;
 
 constexpr uint32_t OFF_KQHI = 0;
-constexpr uint32_t OFF_KQLO = OFF_KQHI + kKqBytes;
-constexpr uint32_t OFF_KTHI = OFF_KQLO + kKqBytes;
+constexpr uint32_t OFF_KQLO = kKqBytes;
+constexpr uint32_t OFF_KTHI = 2 * kKqBytes;
 constexpr uint32_t OFF_KTLO = OFF_KTHI + kKtBytes;
-constexpr uint32_t OFF_A = OFF_KTLO + kKtBytes;
-constexpr uint32_t OFF_TP = OFF_A + 4 * kAFloats;
-constexpr uint32_t OFF_Y = OFF_TP + 4 * kTFloats;
-constexpr uint32_t OFF_GATES = OFF_Y + 4 * kYFloats;
-constexpr uint32_t kSmemBytes = OFF_GATES + 2 * sizeof(ChunkGates);
-// T and B operands (hi, lo) over the [K; Q] tiles, written once P | R is done
-constexpr uint32_t OFF_THI = OFF_KQHI, OFF_TLO = OFF_KQLO;
-constexpr uint32_t OFF_BHI = OFF_KQHI + kQRow0, OFF_BLO = OFF_KQLO + kQRow0;
-static_assert(kSqBytes <= kQRow0 && kQRow0 + kSqBytes <= kKqBytes, "T over the k rows, B over the q rows");
-static_assert(OFF_A % 16 == 0 && OFF_TP % 16 == 0 && OFF_Y % 16 == 0 && OFF_GATES % 16 == 0, "alignment");
+constexpr uint32_t kSmemBytes = OFF_KTLO + kKtBytes;
+constexpr uint32_t OFF_THI = OFF_KQHI, OFF_TLO = OFF_KQLO;                    // T' over the k half
+constexpr uint32_t OFF_BHI = OFF_KQHI + kQRow0, OFF_BLO = OFF_KQLO + kQRow0;  // B over the q half
 static_assert(kSmemBytes <= 226 * 1024, "shared memory budget (one CTA per SM)");
-
-// byte offset of (row, col) in a 64-column operand tile
-__host__ __device__ constexpr uint32_t sq_off(int row, int col) {
-  return (uint32_t)(row / 8) * kRg64 + (uint32_t)(col / 4) * kLbo + (uint32_t)(row % 8) * 16 + (uint32_t)(col % 4) * 4;
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));  // results below 2^-126 flush to 0
-  return y;
-}
-
-// Gam(j, t) for j <= t (j = -1: E_t)
-__device__ __forceinline__ float gam(const ChunkGates &G, int j, int t) {
-  if (G.seg[t] > j) return 0.f;
-  const float c0 = j >= 0 ? G.cum[j] : 0.f;
-  const int n0 = j >= 0 ? G.nneg[j] : 0;
-  const float m = ex2(G.cum[t] - c0);
-  return ((G.nneg[t] - n0) & 1) ? -m : m;
-}
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, uint64_t limit, int32_t *status,
                                               volatile int *abort_flag) {
@@ -196,8 +112,9 @@ __device__ __forceinline__ bool named_any_rows(bool v) {
 }
 
 struct Bars {
-  uint64_t kq, kt, gates, split, ab, xt, dd;  // arrivals
-  uint64_t g, pr, d, o, u;                    // MMA commits
+  uint64_t kqk, kqq, tk, tq, kt;  // producers: E o K, E o Q, T', B, F o K stored
+  uint64_t split, xt, dd;         // row warps: lo of S, X, D hi / lo (and the decayed S) written
+  uint64_t p, r, d, o, u;         // MMA commits
 };
 
 // 64 TMEM columns of this thread's lane as floats, one wait
@@ -227,92 +144,27 @@ __device__ __forceinline__ void sts_split4(uint8_t *sm, uint32_t off_hi, uint32_
   *reinterpret_cast<uint4 *>(sm + off_lo) = make_uint4(l0, l1, l2, l3);
 }
 
-// T = (I + A)^-1 by 16 x 16 blocks, on the 128 row threads (rows and the
-// diagonal of T packed by rows at Tp; A packed by rows at Ap; Y is scratch).
-//   diagonal blocks:  T_bb = (I + A_bb)^-1 by forward substitution, thread
-//                     16 b + jj forming column jj of T_bb;
-//   level L = 1..3:   Y_ab = sum_(b<=m<a) A_am T_mb, then T_ab = -T_aa Y_ab,
-//                     for a = b + L; one work item = (block, row, 4 columns).
-// Row offsets inside a 16-row block: the rows 16 m + i of a packed triangle
-// start at row(16 m) + 16 m i + row(i) (each row of the block is 16 m longer
-// than row i of the first block), so only row(16 m) is formed at run time.
-__device__ __forceinline__ float4 mask_above(float4 v, int col0, int row) {  // zero the entries with col > row
-  if (col0 > row) v.x = 0.f;
-  if (col0 + 1 > row) v.y = 0.f;
-  if (col0 + 2 > row) v.z = 0.f;
-  if (col0 + 3 > row) v.w = 0.f;
-  return v;
+__device__ __forceinline__ float4 scale4(float4 v, float s) { return make_float4(v.x * s, v.y * s, v.z * s, v.w * s); }
+
+// lo part of x when the tensor cores read x itself as its hi part (truncation)
+__device__ __forceinline__ uint32_t lo_of_truncated(float x) {
+  return tc::to_tf32(x - __uint_as_float(__float_as_uint(x) & 0xffffe000u));
 }
-__device__ __forceinline__ void fma4(float4 &acc, float s, const float4 &v) {
-  acc.x = fmaf(s, v.x, acc.x);
-  acc.y = fmaf(s, v.y, acc.y);
-  acc.z = fmaf(s, v.z, acc.z);
-  acc.w = fmaf(s, v.w, acc.w);
-}
-__device__ __forceinline__ void invert_unit_lower(const float *Ap, float *Tp, float *Y, int r) {
-  if (r < kC) {
-    const int b = r / 16, jj = r % 16, b16 = 16 * b;
-    const float *ab = Ap + a_row(b16) + b16;  // + 16 b tt + a_row(tt) + n gives A(16 b + tt, 16 b + n)
-    float acc[16];
+
+// ---- MMA issue (one thread; three tf32 passes per product, unrolled) --------
+// A from TMEM (hi at a_hi, lo at a_lo; a k step of 8 columns), B from a
+// K-major shared-memory tile (hi / lo descriptors; a k step advances the start
+// address by kstep16 16-byte units).
+template <int KSTEPS>
+__device__ __forceinline__ void issue3(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t b_hi, uint64_t b_lo,
+                                       uint32_t kstep16, uint32_t idesc, bool acc) {
 #pragma unroll
-    for (int tt = 0; tt < 16; ++tt) acc[tt] = tt == jj ? 1.f : 0.f;
+  for (int ps = 0; ps < 3; ++ps) {
+    const uint32_t a = ps == 2 ? a_lo : a_hi;
+    const uint64_t b = ps == 1 ? b_lo : b_hi;
 #pragma unroll
-    for (int n = 0; n < 15; ++n) {
-      const float tn = acc[n];
-#pragma unroll
-      for (int tt = n + 1; tt < 16; ++tt) acc[tt] = fmaf(-ab[b16 * tt + a_row(tt) + n], tn, acc[tt]);
-    }
-    float *tb = Tp + t_row(b16) + b16 + jj;  // + 16 b tt + t_row(tt) gives T(16 b + tt, 16 b + jj)
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt)
-      if (tt >= jj) tb[b16 * tt + t_row(tt)] = acc[tt];
-  }
-  named_sync_rows();
-  float4 *Y4 = reinterpret_cast<float4 *>(Y);
-#pragma unroll 1
-  for (int L = 1; L < 4; ++L) {
-    const int nitems = (4 - L) * 64;
-    // Y_ab(i, 4 q .. 4 q + 3) = sum over m in [b, a) and kk of A(16 a + i, 16 m + kk) T(16 m + kk, 16 b + 4 q ..)
-#pragma unroll 1
-    for (int e = r; e < nitems; e += kRowThreads) {
-      const int bb = e / 64, i = (e / 4) % 16, q = e % 4, a = bb + L, col = 16 * bb + 4 * q;
-      const float *arow = Ap + a_row(16 * a + i);
-      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-      for (int m = bb; m < a; ++m) {
-        const int m16 = 16 * m;
-        const float *tm = Tp + t_row(m16) + col;  // + 16 m kk + t_row(kk) gives T(16 m + kk, col)
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const float4 av = *reinterpret_cast<const float4 *>(arow + m16 + 4 * k4);
-          const float as[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int kk = 4 * k4 + e2;
-            const float4 tv = mask_above(*reinterpret_cast<const float4 *>(tm + m16 * kk + t_row(kk)), col, m16 + kk);
-            fma4(y, as[e2], tv);
-          }
-        }
-      }
-      Y4[e] = y;  // [block][row i][4-column group q]
-    }
-    named_sync_rows();
-    // T_ab(i, 4 q ..) = -sum over kk <= i of T(16 a + i, 16 a + kk) Y_ab(kk, 4 q ..)
-#pragma unroll 1
-    for (int e = r; e < nitems; e += kRowThreads) {
-      const int bb = e / 64, i = (e / 4) % 16, q = e % 4, a = bb + L;
-      float *trow = Tp + t_row(16 * a + i);
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 tv = mask_above(*reinterpret_cast<const float4 *>(trow + 16 * a + 4 * k4), 4 * k4, i);
-        const float ts[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) fma4(t, ts[e2], Y4[bb * 64 + (4 * k4 + e2) * 4 + q]);
-      }
-      *reinterpret_cast<float4 *>(trow + 16 * bb + 4 * q) = make_float4(-t.x, -t.y, -t.z, -t.w);
-    }
-    named_sync_rows();
+    for (int k = 0; k < KSTEPS; ++k)
+      tc::mma_ts(d, a + 8 * k, b + (uint64_t)(kstep16 * k), idesc, (acc || ps != 0 || k != 0) ? 1u : 0u);
   }
 }
 
@@ -348,19 +200,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
     return;
   }
   const int nch = (t1 - t0 + kC - 1) / kC;
-  ChunkGates *gates = reinterpret_cast<ChunkGates *>(sm + OFF_GATES);
+  // record of chunk c: recs + c * rec_stride
+  const float *recs = p.ws + (slot_base(t0, i) * p.Hv + h) * (int64_t)kRecFloats;
+  const int64_t rec_stride = (int64_t)p.Hv * kRecFloats;
   TS *Sg = reinterpret_cast<TS *>(p.layer + (int64_t)slot * p.page + p.ssm_off) + (int64_t)h * dv * kDK;
 
   if (tid == 0) {
-    mbar_init(&bars.kq, kThreads - kProd0);  // every producer thread
+    mbar_init(&bars.kqk, kThreads - kProd0);  // every producer thread
+    mbar_init(&bars.kqq, kThreads - kProd0);
+    mbar_init(&bars.tk, kThreads - kProd0);
+    mbar_init(&bars.tq, kThreads - kProd0);
     mbar_init(&bars.kt, kThreads - kProd0);
-    mbar_init(&bars.gates, 1);
     mbar_init(&bars.split, kRowThreads);
-    mbar_init(&bars.ab, kRowThreads);
     mbar_init(&bars.xt, kRowThreads);
     mbar_init(&bars.dd, kRowThreads);
-    mbar_init(&bars.g, 1);
-    mbar_init(&bars.pr, 1);
+    mbar_init(&bars.p, 1);
+    mbar_init(&bars.r, 1);
     mbar_init(&bars.d, 1);
     mbar_init(&bars.o, 1);
     mbar_init(&bars.u, 1);
@@ -382,70 +237,29 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
   if (warp < 4) {
     // ======================================================= row warps
     const int r = tid;
-    // MMA issue (thread 0): three tf32 passes (hi.hi, hi.lo, lo.hi) per
-    // product.  The issue loops stay rolled and advance the descriptors by
-    // constants (the start address sits in the descriptor's low bits): a k
-    // step of 8 tf32 columns is 256 bytes along a 128-column tile, 288 bytes
-    // along a 64-column tile, 8 columns of a TMEM operand.
-    const uint32_t kqhi = smem_u32(sm + OFF_KQHI), kqlo = smem_u32(sm + OFF_KQLO);
-    const uint32_t kthi = smem_u32(sm + OFF_KTHI), ktlo = smem_u32(sm + OFF_KTLO);
-    const uint32_t thi = smem_u32(sm + OFF_THI), tlo = smem_u32(sm + OFF_TLO);
-    const uint32_t bhi = smem_u32(sm + OFF_BHI), blo = smem_u32(sm + OFF_BLO);
+    const bool row_ok = r < dv;
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     constexpr uint32_t id64 = tc::idesc_tf32(128, 64, false);
     constexpr uint32_t id128 = tc::idesc_tf32(128, 128, false);
+    // B operand descriptors; a k step of 8 tf32 columns is 256 bytes along
+    // the token-major tile, 2 kLbo bytes along a 64-column tile
+    const uint64_t dk_hi = tc::smem_desc(smem_u32(sm + OFF_KQHI), 128, kKqRg);
+    const uint64_t dk_lo = tc::smem_desc(smem_u32(sm + OFF_KQLO), 128, kKqRg);
+    const uint64_t dq_hi = tc::smem_desc(smem_u32(sm + OFF_KQHI + kQRow0), 128, kKqRg);
+    const uint64_t dq_lo = tc::smem_desc(smem_u32(sm + OFF_KQLO + kQRow0), 128, kKqRg);
+    const uint64_t dt_hi = tc::smem_desc(smem_u32(sm + OFF_THI), kLbo, kRg64);
+    const uint64_t dt_lo = tc::smem_desc(smem_u32(sm + OFF_TLO), kLbo, kRg64);
+    const uint64_t db_hi = tc::smem_desc(smem_u32(sm + OFF_BHI), kLbo, kRg64);
+    const uint64_t db_lo = tc::smem_desc(smem_u32(sm + OFF_BLO), kLbo, kRg64);
+    const uint64_t dkt_hi = tc::smem_desc(smem_u32(sm + OFF_KTHI), kLbo, kRg64);
+    const uint64_t dkt_lo = tc::smem_desc(smem_u32(sm + OFF_KTLO), kLbo, kRg64);
+    constexpr uint32_t kq_step = 256 >> 4, sq_step = (2 * kLbo) >> 4;
     uint64_t *last = nullptr;  // the last commit's barrier and phase (threads 0 and 32)
     uint32_t last_par = 0;
     auto commit = [&](uint64_t *bar, uint32_t par) {
       tc::mma_commit(bar);
       last = bar, last_par = par;
     };
-    // [K;Q] (128 rows) x K (64 rows)^T -> T_R
-    auto issue_gram = [&]() {
-#pragma unroll 1
-      for (int ps = 0; ps < 3; ++ps) {
-        uint64_t ad = tc::smem_desc(ps == 2 ? kqlo : kqhi, 128, kKqRg);
-        uint64_t bd = tc::smem_desc(ps == 1 ? kqlo : kqhi, 128, kKqRg);
-#pragma unroll 1
-        for (int s = 0; s < kDK / 8; s += 4, ad += 4 * (256 >> 4), bd += 4 * (256 >> 4)) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            tc::mma_ss(tmem + T_R, ad + u * (256 >> 4), bd + u * (256 >> 4), id64, (ps | s | u) != 0);
-        }
-      }
-    };
-    // S x [K;Q]^T -> T_P (P) | T_R (R)
-    auto issue_pr = [&]() {
-#pragma unroll 1
-      for (int ps = 0; ps < 3; ++ps) {
-        uint32_t a = tmem + (ps == 2 ? T_SLO : T_SHI);
-        uint64_t bd = tc::smem_desc(ps == 1 ? kqlo : kqhi, 128, kKqRg);
-#pragma unroll 1
-        for (int s = 0; s < kDK / 8; s += 4, a += 32, bd += 4 * (256 >> 4)) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) tc::mma_ts(tmem + T_P, a + 8 * u, bd + u * (256 >> 4), id128, (ps | s | u) != 0);
-        }
-      }
-    };
-    // (a_hi, a_lo: TMEM, 64 columns) x (b_hi, b_lo: 64-column smem tiles, N rows)^T -> d
-    auto issue_t64 = [&](uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo, uint32_t idesc,
-                         bool acc) {
-#pragma unroll 1
-      for (int ps = 0; ps < 3; ++ps) {
-        uint32_t a = tmem + (ps == 2 ? a_lo : a_hi);
-        uint64_t bd = tc::smem_desc(ps == 1 ? b_lo : b_hi, kLbo, kRg64);
-#pragma unroll 1
-        for (int s = 0; s < kC / 8; s += 4, a += 32, bd += 4 * ((2 * kLbo) >> 4)) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            tc::mma_ts(tmem + d, a + 8 * u, bd + u * ((2 * kLbo) >> 4), idesc, acc || (ps | s | u) != 0);
-        }
-      }
-    };
-    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
-    const bool row_ok = r < dv;
-    float *Ap = reinterpret_cast<float *>(sm + OFF_A);
-    float *Tp = reinterpret_cast<float *>(sm + OFF_TP);
-    float *Yp = reinterpret_cast<float *>(sm + OFF_Y);
     // initial state -> TMEM (zero when cold; rows >= dv stay zero)
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
@@ -482,191 +296,129 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
     }
     tc::tmem_wait_st();
 
+#pragma unroll 1
     for (int c = 0; c < nch; ++c) {
-      const ChunkGates &G = gates[c & 1];
       const uint32_t par = c & 1;
       const int nt = min(kC, t1 - t0 - c * kC);
       const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
-      // ---- 0: (thread 0) the Gram product once the chunk's operands are stored
-      bool ok0 = true;
-      if (r == 0 && (ok0 = wait_or_abort(&bars.kq, par, lim, p.status, abort_flag))) {
-        tc::fence_after_sync();
-        issue_gram();
-        commit(&bars.g, par);
-      }
-      __syncwarp();
-      // ---- 1: split S into the tf32 A operands of P | R, decay S in place
-      bool ok = ok0 && (c == 0 || wait_or_abort(&bars.u, par ^ 1, lim, p.status, abort_flag)) &&
-                wait_or_abort(&bars.gates, par, lim, p.status, abort_flag);
-      if (named_any_rows(!ok)) break;
-      tc::fence_after_sync();
-      const float e_last = G.e_last;
-#pragma unroll 1
-      for (int q = 0; q < kDK / 16; ++q) {
-        uint32_t v[16], hi[16], lo[16];
-        tc::tmem_ld16(tl + T_S + 16 * q, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float s = __uint_as_float(v[e]);
-          tc::split_tf32(s, hi[e], lo[e]);
-          v[e] = __float_as_uint(s * e_last);
-        }
-        tc::tmem_st16(tl + T_SHI + 16 * q, hi);
-        tc::tmem_st16(tl + T_SLO + 16 * q, lo);
-        tc::tmem_st16(tl + T_S + 16 * q, v);
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      mbar_arrive(&bars.split);
-
-      // v_t[r] of this chunk, in flight while A and B are formed
+      const float *rec = recs + c * rec_stride;
+      // v_t[r] of this chunk, in flight during the first steps
       float x[kC];
 #pragma unroll
       for (int t = 0; t < kC; ++t)
         x[t] = (t < nt && row_ok) ? __ldg(p.v + ((tb + t) * p.Hv + h) * dv + r) : 0.f;
+      const float e_last = __ldg(rec + kRecMisc);
 
-      // ---- 2: row r of A (r < 64: A_rj = b_r Gam(j,r) G_rj, j < r, packed
-      // to smem) or of B (r >= 64: B_tj = Gam(j,t) M_jt, j <= t, t = r - 64,
-      // kept in registers until its operand tile is free), from the Gram
-      // accumulator's lane r (k_r.k_j for r < 64, q_t.k_j for r >= 64)
-      ok = ok0 && wait_or_abort(&bars.g, par, lim, p.status, abort_flag);
+      // ---- 1: lo of S (the update of the previous chunk is complete)
+      bool ok0 = true;
+      bool ok = c == 0 || wait_or_abort(&bars.u, par ^ 1, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
-      float brow[kC];
-      {
-        const int t = r < kC ? r : r - kC;
-        const float ct = G.cum[t], bt = G.beta[t];
-        const int st = G.seg[t], nt_neg = G.nneg[t];
-        ld64(tl + T_R, brow);  // the Gram row, weighted in place
-        tc::fence_before_sync();
-        mbar_arrive(&bars.ab);  // the Gram columns are read: free for R
+#pragma unroll 1
+      for (int q = 0; q < kDK / 32; ++q) {
+        uint32_t v[32];
+        tc::tmem_ld32(tl + T_S + 32 * q, v);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < kC; ++j) {
-          const float m = ex2(ct - G.cum[j]);
-          const float gm = st > j ? 0.f : (((nt_neg - G.nneg[j]) & 1) ? -m : m);  // Gam(j, t) for j <= t
-          brow[j] *= gm;
-        }
-        if (r < kC) {
-          float *arow = Ap + a_row(t);
-#pragma unroll
-          for (int j4 = 0; j4 < kC; j4 += 4)
-            if (j4 < a1_of(t))
-              *reinterpret_cast<float4 *>(arow + j4) =
-                  make_float4(j4 < t ? bt * brow[j4] : 0.f, j4 + 1 < t ? bt * brow[j4 + 1] : 0.f,
-                              j4 + 2 < t ? bt * brow[j4 + 2] : 0.f, j4 + 3 < t ? bt * brow[j4 + 3] : 0.f);
-        } else {
-#pragma unroll
-          for (int j = 0; j < kC; ++j)
-            if (j > t) brow[j] = 0.f;
-        }
+        for (int e = 0; e < 32; ++e) v[e] = lo_of_truncated(__uint_as_float(v[e]));
+        tc::tmem_st32(tl + T_SLO + 32 * q, v);
       }
-      named_sync_rows();  // A visible to every row thread
-      if (r == 0 && (ok0 = wait_or_abort(&bars.split, par, lim, p.status, abort_flag) &&
-                           wait_or_abort(&bars.ab, par, lim, p.status, abort_flag))) {
-        tc::fence_after_sync();
-        issue_pr();  // P | R = S [K;Q]^T
-        commit(&bars.pr, par);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(&bars.split);
+      if (r == 0) {
+        if ((ok0 = wait_or_abort(&bars.split, par, lim, p.status, abort_flag) &&
+                   wait_or_abort(&bars.kqk, par, lim, p.status, abort_flag))) {
+          tc::fence_after_sync();
+          issue3<kDK / 8>(tmem + T_P, tmem + T_S, tmem + T_SLO, dk_hi, dk_lo, kq_step, id64, false);  // P'
+          commit(&bars.p, par);
+        }
+        if (ok0 && (ok0 = wait_or_abort(&bars.kqq, par, lim, p.status, abort_flag))) {
+          tc::fence_after_sync();
+          issue3<kDK / 8>(tmem + T_R, tmem + T_S, tmem + T_SLO, dq_hi, dq_lo, kq_step, id64, false);  // R'
+          commit(&bars.r, par);
+        }
       }
       __syncwarp();
 
-      // ---- 3: T = (I + A)^-1 (fp32, packed), while P | R runs
-      invert_unit_lower(Ap, Tp, Yp, r);
-
-      // ---- 4: once P | R is done (the last reader of S hi / lo and of the
-      // [K;Q] tiles): X = b o (v - E o P) -> tf32 hi / lo, R <- E o R, T and
-      // B -> tf32 operand tiles
-      ok = ok0 && wait_or_abort(&bars.pr, par, lim, p.status, abort_flag);
+      // ---- 2: X = V - P' -> tf32 hi / lo
+      ok = ok0 && wait_or_abort(&bars.p, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
       {
         float pv[kC];
         ld64(tl + T_P, pv);
 #pragma unroll
-        for (int t = 0; t < kC; ++t) x[t] = G.beta[t] * (x[t] - G.E[t] * pv[t]);
-#pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) tc::split_tf32(x[16 * q + e], hi[e], lo[e]);
+          for (int e = 0; e < 16; ++e) tc::split_tf32(x[16 * q + e] - pv[16 * q + e], hi[e], lo[e]);
           tc::tmem_st16(tl + T_XHI + 16 * q, hi);
           tc::tmem_st16(tl + T_XLO + 16 * q, lo);
         }
       }
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[16];
-        tc::tmem_ld16(tl + T_R + 16 * q, w);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(G.E[16 * q + e] * __uint_as_float(w[e]));
-        tc::tmem_st16(tl + T_R + 16 * q, w);
-      }
-      // T operand: row r / 2, columns 32 (r % 2) .. + 31, from the packed rows
-      {
-        const int t = r >> 1, j0 = 32 * (r & 1);
-        const float *trow = Tp + t_row(t);
-#pragma unroll 1
-        for (int j4 = j0; j4 < j0 + 32; j4 += 4) {
-          // the packed row's slots above the diagonal are never written: zero them here
-          float4 v4 = j4 < b1_of(t) ? *reinterpret_cast<const float4 *>(trow + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j4 > t) v4.x = 0.f;
-          if (j4 + 1 > t) v4.y = 0.f;
-          if (j4 + 2 > t) v4.z = 0.f;
-          if (j4 + 3 > t) v4.w = 0.f;
-          sts_split4(sm, OFF_THI + sq_off(t, j4), OFF_TLO + sq_off(t, j4), v4);
-        }
-      }
-      if (r >= kC) {
-        const int t = r - kC;
-#pragma unroll
-        for (int j4 = 0; j4 < kC; j4 += 4)
-          sts_split4(sm, OFF_BHI + sq_off(t, j4), OFF_BLO + sq_off(t, j4),
-                     make_float4(brow[j4], brow[j4 + 1], brow[j4 + 2], brow[j4 + 3]));
-      }
       tc::tmem_wait_st();
-      fence_proxy_async_smem();  // T and B written by the generic proxy, read by the MMA
       tc::fence_before_sync();
       mbar_arrive(&bars.xt);
-      if (r == 0 && (ok0 = wait_or_abort(&bars.xt, par, lim, p.status, abort_flag))) {
+      if (r == 0 && ok0 &&
+          (ok0 = wait_or_abort(&bars.xt, par, lim, p.status, abort_flag) &&
+                 wait_or_abort(&bars.tk, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
-        issue_t64(T_D, T_XHI, T_XLO, thi, tlo, id64, false);  // D = X T^T
+        issue3<kC / 8>(tmem + T_D, tmem + T_XHI, tmem + T_XLO, dt_hi, dt_lo, sq_step, id64, false);  // D
         commit(&bars.d, par);
       }
       __syncwarp();
 
-      // ---- 5: D -> tf32 hi / lo (A of O and of the update)
-      ok = ok0 && wait_or_abort(&bars.d, par, lim, p.status, abort_flag);
+      // ---- 3: S <- e_last S once R' (the last product reading S) is done
+      ok = ok0 && wait_or_abort(&bars.r, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[16], hi[16], lo[16];
-        tc::tmem_ld16(tl + T_D + 16 * q, w);
+      for (int q = 0; q < kDK / 32; ++q) {
+        uint32_t v[32];
+        tc::tmem_ld32(tl + T_S + 32 * q, v);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) tc::split_tf32(__uint_as_float(w[e]), hi[e], lo[e]);
-        tc::tmem_st16(tl + T_DHI + 16 * q, hi);
-        tc::tmem_st16(tl + T_DLO + 16 * q, lo);
+        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * e_last);
+        tc::tmem_st32(tl + T_S + 32 * q, v);
+      }
+
+      // ---- 4: D -> tf32 hi / lo (A of O and of the update)
+      ok = ok0 && wait_or_abort(&bars.d, par, lim, p.status, abort_flag);
+      if (named_any_rows(!ok)) break;
+      tc::fence_after_sync();
+      {
+        float dvv[kC];
+        ld64(tl + T_D, dvv);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) tc::split_tf32(dvv[16 * q + e], hi[e], lo[e]);
+          tc::tmem_st16(tl + T_DHI + 16 * q, hi);
+          tc::tmem_st16(tl + T_DLO + 16 * q, lo);
+        }
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(&bars.dd);
-      // O (thread 0) and the update (thread 32) are independent products on
-      // the same A operand: two issuing threads keep the tensor core fed
-      if (r == 0 && (ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag))) {
+      // O (thread 0) and the update (thread 32) read the same A operand: two
+      // issuing threads keep the tensor core fed
+      if (r == 0 && ok0 &&
+          (ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag) &&
+                 wait_or_abort(&bars.tq, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
-        issue_t64(T_R, T_DHI, T_DLO, bhi, blo, id64, true);  // O = E o R + D B^T
+        issue3<kC / 8>(tmem + T_R, tmem + T_DHI, tmem + T_DLO, db_hi, db_lo, sq_step, id64, true);  // O
         commit(&bars.o, par);
       } else if (r == 32 && (ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag) &&
                                    wait_or_abort(&bars.kt, par, lim, p.status, abort_flag))) {
         tc::fence_after_sync();
-        issue_t64(T_S, T_DHI, T_DLO, kthi, ktlo, id128, true);  // S += D (F o K)
+        issue3<kC / 8>(tmem + T_S, tmem + T_DHI, tmem + T_DLO, dkt_hi, dkt_lo, sq_step, id128, true);  // update
         commit(&bars.u, par);
       }
       __syncwarp();
 
-      // ---- 6: outputs
+      // ---- 5: outputs
       ok = ok0 && wait_or_abort(&bars.o, par, lim, p.status, abort_flag);
       if (named_any_rows(!ok)) break;
       tc::fence_after_sync();
@@ -686,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
         }
       }
       tc::fence_before_sync();
-      named_sync_rows();  // every row has read O: the next Gram may overwrite it
+      named_sync_rows();  // every row has read O: the next R' may overwrite it
     }
     // ---- final state -> the slot
     const bool fin = nch == 0 || wait_or_abort(&bars.u, (nch - 1) & 1, lim, p.status, abort_flag);
@@ -730,26 +482,33 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
     // ======================================================= producers
     const int pt = tid - kProd0, pw = pt >> 5;
     const int al = lane & 7, bl = lane >> 3;
-    const float *qg = p.q, *kg = p.k;
-    // the next chunk's k and q: [token block half][channel block half][token in
+    // k and q of a chunk: [token block half][channel block half][token in
     // block]; this thread's 4 x 4 blocks are tokens 4a..4a+3, channels
-    // 4b..4b+3 with a = al + 8 ah, b = bl + 4 pw + 16 bh
+    // 4b..4b+3 with a = al + 8 ah, b = bl + 4 pw + 16 bh; E and F of its tokens
     float4 kr[2][2][4], qr[2][2][4];
-    auto load_rows = [&](const float *src, int c, float4 (&dst)[2][2][4]) {
+    float ev[2][4], fv[2][4];
+    auto load_kq = [&](int c) {
       const int nt = min(kC, t1 - t0 - c * kC);
       const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
+      const float *rec = recs + c * rec_stride;
 #pragma unroll
       for (int ah = 0; ah < 2; ++ah)
 #pragma unroll
-        for (int bh = 0; bh < 2; ++bh)
+        for (int u = 0; u < 4; ++u) {
+          const int tok = 4 * (al + 8 * ah) + u;
+          ev[ah][u] = __ldg(rec + kRecE + tok);
+          fv[ah][u] = __ldg(rec + kRecF + tok);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int tok = 4 * (al + 8 * ah) + u, b = bl + 4 * pw + 16 * bh;
-            dst[ah][bh][u] = tok < nt ? __ldg(reinterpret_cast<const float4 *>(src + ((tb + tok) * p.Hk + g) * kDK + 4 * b))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int bh = 0; bh < 2; ++bh) {
+            const int b = bl + 4 * pw + 16 * bh;
+            const int64_t off = ((tb + tok) * p.Hk + g) * kDK + 4 * b;
+            const bool in = tok < nt;
+            kr[ah][bh][u] = in ? __ldg(reinterpret_cast<const float4 *>(p.k + off)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            qr[ah][bh][u] = in ? __ldg(reinterpret_cast<const float4 *>(p.q + off)) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
+        }
     };
-    // token-major rows: k at row j, q at row 64 + j
+    // token-major E o K (rows 0-63) or E o Q (rows 64-127)
     auto store_rows = [&](const float4 (&src)[2][2][4], int row0) {
 #pragma unroll
       for (int ah = 0; ah < 2; ++ah)
@@ -757,17 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
         for (int bh = 0; bh < 2; ++bh)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int j = row0 + 4 * (al + 8 * ah) + u, b = bl + 4 * pw + 16 * bh;
-            const uint32_t o = (uint32_t)(j / 8) * kKqRg + (uint32_t)b * 128 + (uint32_t)(j % 8) * 16;
-            sts_split4(sm, OFF_KQHI + o, OFF_KQLO + o, src[ah][bh][u]);
+            const int j = 4 * (al + 8 * ah) + u, c4 = 4 * (bl + 4 * pw + 16 * bh);
+            sts_split4(sm, OFF_KQHI + kq_off(row0 + j, c4), OFF_KQLO + kq_off(row0 + j, c4),
+                       scale4(src[ah][bh][u], ev[ah][u]));
           }
     };
     // channel-major F o K: K[j][c] F_j at (channel c, token j)
-    auto store_kt = [&](const ChunkGates &G) {
+    auto store_kt = [&]() {
 #pragma unroll
       for (int ah = 0; ah < 2; ++ah) {
         const int a = al + 8 * ah;
-        const float f0 = G.F[4 * a], f1 = G.F[4 * a + 1], f2 = G.F[4 * a + 2], f3 = G.F[4 * a + 3];
+        const float f0 = fv[ah][0], f1 = fv[ah][1], f2 = fv[ah][2], f3 = fv[ah][3];
 #pragma unroll
         for (int bh = 0; bh < 2; ++bh) {
           const int b = bl + 4 * pw + 16 * bh;
@@ -779,106 +538,70 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int ch = 4 * b + e;
-            const uint32_t o = (uint32_t)(ch / 8) * kRg64 + (uint32_t)a * kLbo + (uint32_t)(ch % 8) * 16;
-            sts_split4(sm, OFF_KTHI + o, OFF_KTLO + o, make_float4(col[e][0], col[e][1], col[e][2], col[e][3]));
+            sts_split4(sm, OFF_KTHI + sq_off(ch, 4 * a), OFF_KTLO + sq_off(ch, 4 * a),
+                       make_float4(col[e][0], col[e][1], col[e][2], col[e][3]));
           }
         }
       }
     };
-    // gate scan of chunk c by producer warp 0: two tokens per lane
-    auto form_gates = [&](int c) {
-      ChunkGates &G = gates[c & 1];
-      const int nt = min(kC, t1 - t0 - c * kC);
-      const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
-      float la[2], bb[2];
-      int zi[2], ng[2];
+    // T' and B of a chunk: row pt / 2, columns 32 (pt % 2) .. + 31 (the
+    // 16-byte groups past the diagonal's are zero and not read)
+    const int trow = pt >> 1, tj0 = 32 * (pt & 1);
+    float4 tv[8], bv[8];
+    auto load_tb = [&](int c) {
+      const float *rec = recs + c * rec_stride;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = 2 * lane + e;
-        const float a = t < nt ? __ldg(p.alpha + (tb + t) * p.Hv + h) : 1.f;
-        bb[e] = t < nt ? __ldg(p.beta + (tb + t) * p.Hv + h) : 0.f;
-        la[e] = a != 0.f ? log2f(fabsf(a)) : 0.f;
-        zi[e] = a == 0.f ? t : -1;
-        ng[e] = a < 0.f ? 1 : 0;
+      for (int m = 0; m < 8; ++m) {
+        const int j4 = tj0 + 4 * m;
+        const bool in = j4 < 4 * row_groups(trow);
+        tv[m] = in ? __ldg(reinterpret_cast<const float4 *>(rec + kRecT + trow * kC + j4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        bv[m] = in ? __ldg(reinterpret_cast<const float4 *>(rec + kRecB + trow * kC + j4)) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      // inclusive scans over the 64 tokens (lane holds tokens 2 lane, 2 lane + 1)
-      float cs = la[0] + la[1];
-      int zs = max(zi[0], zi[1]), ns = ng[0] + ng[1];
+    };
+    auto store_sq = [&](const float4 (&src)[8], uint32_t off_hi, uint32_t off_lo) {
 #pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const float cu = __shfl_up_sync(0xffffffffu, cs, m);
-        const int zu = __shfl_up_sync(0xffffffffu, zs, m), nu = __shfl_up_sync(0xffffffffu, ns, m);
-        if (lane >= m) {
-          cs += cu;
-          zs = max(zs, zu);
-          ns += nu;
-        }
-      }
-      // exclusive prefix for this lane's first token
-      float cx = __shfl_up_sync(0xffffffffu, cs, 1);
-      int nx = __shfl_up_sync(0xffffffffu, ns, 1), zx = __shfl_up_sync(0xffffffffu, zs, 1);
-      if (lane == 0) {
-        cx = 0.f;
-        nx = 0;
-        zx = -1;
-      }
-      G.cum[2 * lane] = cx + la[0];
-      G.cum[2 * lane + 1] = cs;
-      G.seg[2 * lane] = max(zx, zi[0]);
-      G.seg[2 * lane + 1] = zs;
-      G.nneg[2 * lane] = nx + ng[0];
-      G.nneg[2 * lane + 1] = ns;
-      G.beta[2 * lane] = bb[0];
-      G.beta[2 * lane + 1] = bb[1];
-      __syncwarp();
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = 2 * lane + e;
-        G.E[t] = gam(G, -1, t);
-        G.F[t] = gam(G, t, kC - 1);
-      }
-      if (lane == 0) G.e_last = gam(G, -1, kC - 1);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.gates);
+      for (int m = 0; m < 8; ++m)
+        sts_split4(sm, off_hi + sq_off(trow, tj0 + 4 * m), off_lo + sq_off(trow, tj0 + 4 * m), src[m]);
+    };
+    auto publish = [&](uint64_t *bar) {
+      fence_proxy_async_smem();  // generic-proxy stores, read by the MMA
+      mbar_arrive(bar);
     };
 
-    // Chunk c + 1 is prepared during chunk c: its k and q are loaded first;
-    // after P | R (c) its gates are formed; after O (c) (the last reader of
-    // the tiles that T and B overlay) the [K; Q] tiles are stored; after the
-    // update of chunk c the channel-major F o K.  Every producer waits for
-    // the gates of chunk c + 1 before it stores the [K; Q] tiles, so the gate
-    // barrier is never two phases ahead of a waiting producer.
+    // Chunk c's tiles are stored as the products reading the previous
+    // contents finish: T' after P'(c), B after R'(c); then the next chunk's
+    // E o K after D(c), E o Q after O(c), F o K after the update of chunk c.
     if (nch > 0) {
-      load_rows(kg, 0, kr);
-      load_rows(qg, 0, qr);
-      if (pw == 0) form_gates(0);
-      if (wait_or_abort(&bars.gates, 0, lim, p.status, abort_flag)) {
-        store_rows(kr, 0);
-        store_rows(qr, kC);
-        fence_proxy_async_smem();
-        mbar_arrive(&bars.kq);
-        store_kt(gates[0]);
-        fence_proxy_async_smem();
-        mbar_arrive(&bars.kt);
-      }
-    }
-    for (int c = 0; c + 1 < nch && !*abort_flag; ++c) {
-      const uint32_t par = c & 1, npar = par ^ 1;
-      load_rows(kg, c + 1, kr);
-      load_rows(qg, c + 1, qr);
-      if (!wait_or_abort(&bars.pr, par, lim, p.status, abort_flag)) break;
-      if (pw == 0) form_gates(c + 1);
-      if (!wait_or_abort(&bars.gates, npar, lim, p.status, abort_flag) ||
-          !wait_or_abort(&bars.o, par, lim, p.status, abort_flag))
-        break;
+      load_kq(0);
       store_rows(kr, 0);
+      publish(&bars.kqk);
       store_rows(qr, kC);
-      fence_proxy_async_smem();
-      mbar_arrive(&bars.kq);
+      publish(&bars.kqq);
+      store_kt();
+      publish(&bars.kt);
+      load_tb(0);
+    }
+#pragma unroll 1
+    for (int c = 0; c < nch && !*abort_flag; ++c) {
+      const uint32_t par = c & 1;
+      if (!wait_or_abort(&bars.p, par, lim, p.status, abort_flag)) break;
+      store_sq(tv, OFF_THI, OFF_TLO);
+      publish(&bars.tk);
+      if (!wait_or_abort(&bars.r, par, lim, p.status, abort_flag)) break;
+      store_sq(bv, OFF_BHI, OFF_BLO);
+      publish(&bars.tq);
+      if (c + 1 == nch) break;
+      load_kq(c + 1);
+      if (!wait_or_abort(&bars.d, par, lim, p.status, abort_flag)) break;
+      store_rows(kr, 0);
+      publish(&bars.kqk);
+      if (!wait_or_abort(&bars.o, par, lim, p.status, abort_flag)) break;
+      store_rows(qr, kC);
+      publish(&bars.kqq);
       if (!wait_or_abort(&bars.u, par, lim, p.status, abort_flag)) break;
-      store_kt(gates[npar]);
-      fence_proxy_async_smem();
-      mbar_arrive(&bars.kt);
+      store_kt();
+      publish(&bars.kt);
+      load_tb(c + 1);
     }
   }
 

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "lsc.h"
+#include "lsc_chunk.h"
 #include "lsc_internal.h"
 
 #define LSC_STR2(x) #x
@@ -601,7 +602,11 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
   if (a->n_seq > 65535) return LSC_ERR_UNSUPPORTED;
   // AUTO takes the token kernel: on the CUDA cores it is the faster of the two
   const bool chunked = a->algorithm == LSC_RECURRENT_CHUNKED;
-  if (chunked && g.dk != 128) return LSC_ERR_UNSUPPORTED;
+  if (chunked && g.dk != lsc::chunk::kDK) return LSC_ERR_UNSUPPORTED;
+  if (chunked && a->workspace != nullptr &&
+      (((uintptr_t)a->workspace & 15) != 0 ||
+       a->workspace_bytes < (size_t)lsc::chunk::workspace_bytes(a->total_tokens, a->n_seq, g.Hv)))
+    return ((uintptr_t)a->workspace & 15) != 0 ? LSC_ERR_MISALIGNED : LSC_ERR_INVALID_ARG;
   rc = check_device(p);
   if (rc != LSC_OK) return rc;
   if (a->n_seq == 0) return LSC_OK;
@@ -628,8 +633,34 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
   r.status = g.status;
   r.wait_limit_ns = fault("timeout0") ? 0 : kWaitLimitNs;
   r.drain_limit_ns = kWaitLimitNs;
-  return chunked ? lsc::launch_recurrent_chunked_tc(r, g.dk, g.ssm_dtype, (cudaStream_t)stream)
-                 : lsc::launch_recurrent(r, g.dk, g.ssm_dtype, (cudaStream_t)stream);
+  if (!chunked) return lsc::launch_recurrent(r, g.dk, g.ssm_dtype, (cudaStream_t)stream);
+  // The chunked form: the preparation kernel writes every chunk's state-free
+  // record into the workspace, the state kernel reads them, in stream order.
+  const size_t need = (size_t)lsc::chunk::workspace_bytes(a->total_tokens, a->n_seq, g.Hv);
+  void *ws = a->workspace;
+  const bool own = ws == nullptr;
+  if (own) {
+    if (cudaMallocAsync(&ws, need, (cudaStream_t)stream) != cudaSuccess) {
+      cudaGetLastError();
+      return LSC_ERR_NO_MEMORY;
+    }
+  }
+  r.ws = static_cast<float *>(ws);
+  rc = lsc::launch_chunk_prep(r, p->num_sms, (cudaStream_t)stream);
+  if (rc == LSC_OK) rc = lsc::launch_recurrent_chunked_tc(r, g.dk, g.ssm_dtype, (cudaStream_t)stream);
+  if (own && cudaFreeAsync(ws, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    if (rc == LSC_OK) rc = LSC_ERR_CUDA;
+  }
+  return rc;
+}
+
+int lsc_gdn_recurrent_workspace_bytes(const lsc_pool *p, const lsc_gdn_recurrent_args *a, size_t *bytes) {
+  if (!p || !a || !bytes || a->n_seq < 0 || a->total_tokens < 0) return LSC_ERR_INVALID_ARG;
+  *bytes = a->algorithm == LSC_RECURRENT_CHUNKED
+               ? (size_t)lsc::chunk::workspace_bytes(a->total_tokens, a->n_seq, p->g.Hv)
+               : 0;
+  return LSC_OK;
 }
 
 }  // extern "C"

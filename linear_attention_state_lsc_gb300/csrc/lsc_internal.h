@@ -173,13 +173,18 @@ struct RecurrentParams {
   int32_t *status;
   uint64_t wait_limit_ns;   // bound of each mbarrier wait (tensor-core form; 0: give up at once)
   uint64_t drain_limit_ns;  // bound of the wait for issued MMAs after a timeout
+  float *ws;                // chunked form: workspace records (lsc_chunk.h)
 };
 int launch_recurrent(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
 // the token recurrence for head_k_dim 128 (lsc_rec128.cu)
 int launch_recurrent128(const RecurrentParams &p, int ssm_dtype, cudaStream_t stream);
 // the chunked evaluation (lsc_chunked.cu): head_k_dim 128, head_v_dim <= 128
 int launch_recurrent_chunked(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
-// the chunked evaluation on the tensor cores (lsc_chunked_tc.cu): head_k_dim 128, head_v_dim <= 128
+// the chunked evaluation on the tensor cores: head_k_dim 128, head_v_dim <= 128.
+// launch_chunk_prep (lsc_chunk_prep.cu) writes the state-free records of
+// every chunk to p.ws; launch_recurrent_chunked_tc (lsc_chunked_tc.cu), on
+// the same stream after it, runs the state through the chunks.
+int launch_chunk_prep(const RecurrentParams &p, int num_sms, cudaStream_t stream);
 int launch_recurrent_chunked_tc(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
 
 struct PrefillConvParams {

@@ -96,7 +96,8 @@ class lsc_gdn_recurrent_args(C.Structure):
     _fields_ = [("n_seq", C.c_int32), ("num_k_heads", C.c_int32), ("total_tokens", C.c_int32),
                 ("algorithm", C.c_int32), ("idx", C.c_void_p), ("has_init", C.c_void_p),
                 ("cu_seqlens", C.c_void_p), ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p),
-                ("alpha", C.c_void_p), ("beta", C.c_void_p), ("out", C.c_void_p)]
+                ("alpha", C.c_void_p), ("beta", C.c_void_p), ("out", C.c_void_p),
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
 
 
 class lsc_pc_row(C.Structure):
@@ -158,6 +159,8 @@ def load():
         "lsc_scatter": ([P, I32, P, I32, P, P, P], C.c_int),
         "lsc_gdn_decode": ([P, I32, C.POINTER(lsc_gdn_decode_args), P], C.c_int),
         "lsc_gdn_recurrent": ([P, I32, C.POINTER(lsc_gdn_recurrent_args), P], C.c_int),
+        "lsc_gdn_recurrent_workspace_bytes": ([P, C.POINTER(lsc_gdn_recurrent_args), C.POINTER(C.c_size_t)],
+                                              C.c_int),
         "lsc_gdn_prefill_conv": ([P, I32, C.POINTER(lsc_gdn_prefill_conv_args), P], C.c_int),
         "lsc_kv_pool_required_bytes": ([C.POINTER(lsc_kv_pool_desc), C.POINTER(C.c_size_t)], C.c_int),
         "lsc_kv_pool_create": ([C.POINTER(lsc_kv_pool_desc), P, C.c_size_t, C.POINTER(P)], C.c_int),
@@ -328,10 +331,16 @@ def lsc_gdn_decode(pool, layer, args, stream=None):
 
 
 def recurrent_args(n_seq, num_k_heads, total_tokens, idx, has_init, cu_seqlens, q, k, v, alpha,
-                   beta, out, algorithm=0):
+                   beta, out, algorithm=0, workspace=None, workspace_bytes=0):
     return lsc_gdn_recurrent_args(n_seq, num_k_heads, total_tokens, algorithm, ptr(idx), ptr(has_init),
                                   ptr(cu_seqlens), ptr(q), ptr(k), ptr(v), ptr(alpha), ptr(beta),
-                                  ptr(out))
+                                  ptr(out), ptr(workspace), workspace_bytes)
+
+
+def lsc_gdn_recurrent_workspace_bytes(pool, args):
+    n = C.c_size_t(0)
+    rc = load().lsc_gdn_recurrent_workspace_bytes(pool, C.byref(args), C.byref(n))
+    return rc, n.value
 
 
 def lsc_gdn_recurrent(pool, layer, args, stream=None):
