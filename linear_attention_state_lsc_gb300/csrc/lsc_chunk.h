@@ -26,9 +26,11 @@ constexpr int kC = 64;    // tokens per chunk
 constexpr int kDK = 128;  // head_k_dim of the chunked form
 
 // ---- workspace record of one (chunk slot, v head), fp32 --------------------
-// T'[t][j] and B[t][j] row-major, 64 x 64; only the 16-byte groups with
-// j < 4 floor(t/4) + 4 are written (the entries with j > t inside the last
-// group are zero); the rest of each row is never read.
+// T'[t][j] and B[t][j], 64 x 64, by 16-byte column groups: the four entries
+// (t, 4 g .. 4 g + 3) at float offset rec_off(t, 4 g) = (64 g + t) * 4, so a
+// warp reaching 32 consecutive rows of one group touches 512 contiguous bytes.
+// Only the groups with 4 g < 4 floor(t/4) + 4 are written (the entries with
+// j > t inside the last one are zero); the others are never read.
 constexpr int kRecT = 0;
 constexpr int kRecB = kC * kC;
 constexpr int kRecE = 2 * kC * kC;     // E_t
@@ -40,6 +42,8 @@ static_assert(kRecBytes % 16 == 0, "records keep 16-byte alignment");
 
 // Number of 16-byte groups of row t that carry T' or B entries.
 __host__ __device__ constexpr int row_groups(int t) { return t / 4 + 1; }
+// Float offset of entries (t, j4 .. j4 + 3), j4 a multiple of 4.
+__host__ __device__ constexpr int rec_off(int t, int j4) { return (kC * (j4 / 4) + t) * 4; }
 
 // Chunk slots: chunk c of sequence i (tokens cu[i] + 64 c ..) has slot
 // floor(cu[i] / 64) + i + c.  For cu non-decreasing in [0, T] the slots of

@@ -26,10 +26,12 @@
 //   8-11        item: thread r reads row r of the Gram accumulator (k_r.k_j for
 //               r < 64, q_(r-64).k_j above), the group scans the head's gates,
 //               forms row r of A (packed in shared memory) or of B (straight
-//               to the record), inverts I + A by 16 x 16 blocks and writes the
-//               rows of T' = T diag(b), then E, F and e_last.
-// Gam is formed from a per-chunk running sum of log2|a| (zeros and signs of a
-// tracked apart), so no product of gates under- or overflows on the way.
+//               to the record), inverts I + A (one column per thread of two of
+//               its warps, on different SM sub-partitions) and writes the rows
+//               of T' = T diag(b), then E, F and e_last.
+// Products of gates are formed in token order (running products along a row,
+// product scans for E and F), as the token recurrence applies them: a zero
+// gate zeroes what follows, tiny ones fade to zero without a division.
 // Every wait is bounded: on expiry the thread records LSC_ERR_DEV_TIMEOUT and
 // the CTA stops; the state kernel then reads undefined records, and the call's
 // results are unspecified (as its status word says).
@@ -49,32 +51,18 @@ constexpr int kGroupThreads = 128;
 constexpr uint32_t kTmemCols = 128;  // two Gram buffers of 64 columns
 constexpr int kStagedSeqs = 4096;    // cu_seqlens kept in shared memory up to this many sequences
 
-// Packed triangles (fp32), every row a multiple of 4 floats, 16-byte aligned:
-// A by rows (row t: columns j in [0, 4 ceil(t/4)), zero for j >= t), T by
-// rows including the diagonal (row t: columns j in [0, 4 floor(t/4) + 4),
-// zero for j > t).
-__host__ __device__ constexpr int a1_of(int t) { return 4 * ((t + 3) / 4); }
-__host__ __device__ constexpr int b1_of(int t) { return 4 * ((t + 4) / 4); }
-// sum over m = 1..n of floor(m / 4)
-__host__ __device__ constexpr int quarter_sum(int n) {
-  return n <= 0 ? 0 : 2 * (n / 4) * (n / 4 - 1) + (n / 4) * (n % 4 + 1);
-}
-__host__ __device__ constexpr int a_row(int t) { return 4 * quarter_sum(t + 2); }          // sum of a1_of(i), i < t
-__host__ __device__ constexpr int t_row(int t) { return 4 * t + 4 * quarter_sum(t - 1); }  // sum of b1_of(i), i < t
-static_assert(a_row(1) == 0 && a_row(2) == 4 && a_row(5) == 16 && t_row(1) == 4 && t_row(5) == 4 * 4 + 8, "packing");
-static_assert(b1_of(63) == 4 * row_groups(63), "the T' rows written are the packed rows");
-constexpr int kAFloats = a_row(kC);
-constexpr int kTFloats = t_row(kC);
-constexpr int kYFloats = 3 * 16 * 16;  // block-product scratch of the inverse
+// A and T of one (chunk, v head) in shared memory, fp32, 64 x 64 each: A
+// transposed (At[j][t] = A_tj, so the 16 rows of a block column are
+// contiguous), T by rows (Tm[t][j]).  Only the entries below the diagonal of
+// A and on or below it of T are written or read.
+constexpr int kTileFloats = kC * kC;
 
 // gate quantities of one (chunk, v head)
 struct Gates {
-  float beta[kC];
-  float cum[kC];     // running sum of log2|a_t| over the chunk (0 where a_t = 0)
-  float E[kC];       // a_0 ... a_t
-  float F[kC];       // Gam(t, C-1)
-  int32_t seg[kC];   // last t' <= t with a_t' = 0, or -1
-  int32_t nneg[kC];  // number of negative a_t' for t' <= t
+  float a[kC];     // a_t (1 past the chunk's tokens)
+  float beta[kC];  // b_t (0 past the chunk's tokens)
+  float E[kC];     // a_0 ... a_t
+  float F[kC];     // Gam(t, C-1) = a_(t+1) ... a_(C-1)
   float e_last;
   int32_t pad[3];
 };
@@ -83,29 +71,13 @@ constexpr uint32_t OFF_KQHI = 0;
 constexpr uint32_t OFF_KQLO = kKqBytes;
 constexpr uint32_t OFF_GRP = 2 * kKqBytes;
 constexpr uint32_t G_A = 0;
-constexpr uint32_t G_T = G_A + 4 * kAFloats;
-constexpr uint32_t G_Y = G_T + 4 * kTFloats;
-constexpr uint32_t G_GATES = G_Y + 4 * kYFloats;
+constexpr uint32_t G_T = G_A + 4 * kTileFloats;
+constexpr uint32_t G_GATES = G_T + 4 * kTileFloats;
 constexpr uint32_t kGrpBytes = G_GATES + sizeof(Gates);
 constexpr uint32_t OFF_CU = OFF_GRP + kGroups * kGrpBytes;
 constexpr uint32_t kSmemBytes = OFF_CU + 4 * (kStagedSeqs + 4);
-static_assert(G_T % 16 == 0 && G_Y % 16 == 0 && G_GATES % 16 == 0 && kGrpBytes % 16 == 0, "alignment");
+static_assert(G_T % 16 == 0 && G_GATES % 16 == 0 && kGrpBytes % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget (one CTA per SM)");
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));  // results below 2^-126 flush to 0
-  return y;
-}
-
-// Gam(j, t) for j <= t (j = -1: E_t)
-__device__ __forceinline__ float gam(const Gates &G, int j, int t) {
-  if (G.seg[t] > j) return 0.f;
-  const float c0 = j >= 0 ? G.cum[j] : 0.f;
-  const int n0 = j >= 0 ? G.nneg[j] : 0;
-  const float m = ex2(G.cum[t] - c0);
-  return ((G.nneg[t] - n0) & 1) ? -m : m;
-}
 
 // A solver group (128 threads) synchronises on its own named barrier (1 + its
 // index) and leaves with the warp reconverged for the .sync.aligned TMEM
@@ -157,87 +129,56 @@ __device__ __forceinline__ float4 mask_above(float4 v, int col0, int row) {  // 
   if (col0 + 3 > row) v.w = 0.f;
   return v;
 }
-__device__ __forceinline__ void fma4(float4 &acc, float s, const float4 &v) {
-  acc.x = fmaf(s, v.x, acc.x);
-  acc.y = fmaf(s, v.y, acc.y);
-  acc.z = fmaf(s, v.z, acc.z);
-  acc.w = fmaf(s, v.w, acc.w);
-}
 
-// T = (I + A)^-1 by 16 x 16 blocks, on one solver group's 128 threads (A
-// packed by rows at Ap; rows and the diagonal of T packed by rows at Tp; Y is
-// scratch):
-//   diagonal blocks:  T_bb = (I + A_bb)^-1 by forward substitution, thread
-//                     16 b + jj forming column jj of T_bb;
-//   level L = 1..3:   Y_ab = sum_(b<=m<a) A_am T_mb, then T_ab = -T_aa Y_ab,
-//                     for a = b + L; one work item = (block, row, 4 columns).
-// Row offsets inside a 16-row block: the rows 16 m + i of a packed triangle
-// start at row(16 m) + 16 m i + row(i) (each row of the block is 16 m longer
-// than row i of the first block), so only row(16 m) is formed at run time.
-__device__ __forceinline__ void invert_unit_lower(const float *Ap, float *Tp, float *Y, int r, int bar_id) {
-  if (r < kC) {
-    const int b = r / 16, jj = r % 16, b16 = 16 * b;
-    const float *ab = Ap + a_row(b16) + b16;  // + 16 b tt + a_row(tt) + n gives A(16 b + tt, 16 b + n)
-    float acc[16];
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt) acc[tt] = tt == jj ? 1.f : 0.f;
-#pragma unroll
-    for (int n = 0; n < 15; ++n) {
-      const float tn = acc[n];
-#pragma unroll
-      for (int tt = n + 1; tt < 16; ++tt) acc[tt] = fmaf(-ab[b16 * tt + a_row(tt) + n], tn, acc[tt]);
-    }
-    float *tb = Tp + t_row(b16) + b16 + jj;  // + 16 b tt + t_row(tt) gives T(16 b + tt, 16 b + jj)
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt)
-      if (tt >= jj) tb[b16 * tt + t_row(tt)] = acc[tt];
-  }
-  group_sync(bar_id);
-  float4 *Y4 = reinterpret_cast<float4 *>(Y);
+// T = (I + A)^-1, one column per thread: thread j forms column j of T by
+// 16-row blocks, top to bottom, each as
+//   y = e_j - sum_(m < a) A[a][m] T[m][:, j]     (block products, 16-wide)
+//   y_i -= sum_(i' < i) A[a][a]_(i i') y_i'       (forward substitution)
+// with block a's rows of A read as broadcast 16-byte columns of At, and
+// writes y to rows 16 a .. 16 a + 15 of column j of Tm.  Columns are
+// independent, so no barrier is needed inside.  The blocks start at
+// a0 (a multiple of 16 not above j, the same for the whole warp): rows above
+// j's block come out zero.
+__device__ __forceinline__ void invert_unit_lower(const float *At, float *Tm, int j, int a0) {
 #pragma unroll 1
-  for (int L = 1; L < 4; ++L) {
-    const int nitems = (4 - L) * 64;
-    // Y_ab(i, 4 q .. 4 q + 3) = sum over m in [b, a) and kk of A(16 a + i, 16 m + kk) T(16 m + kk, 16 b + 4 q ..)
-#pragma unroll 1
-    for (int e = r; e < nitems; e += kGroupThreads) {
-      const int bb = e / 64, i = (e / 4) % 16, q = e % 4, a = bb + L, col = 16 * bb + 4 * q;
-      const float *arow = Ap + a_row(16 * a + i);
-      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-      for (int m = bb; m < a; ++m) {
-        const int m16 = 16 * m;
-        const float *tm = Tp + t_row(m16) + col;  // + 16 m kk + t_row(kk) gives T(16 m + kk, col)
+  for (int a = a0; a < kC / 16; ++a) {
+    float y[16];
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const float4 av = *reinterpret_cast<const float4 *>(arow + m16 + 4 * k4);
-          const float as[4] = {av.x, av.y, av.z, av.w};
+    for (int i = 0; i < 16; ++i) y[i] = 16 * a + i == j ? 1.f : 0.f;
+#pragma unroll 1
+    for (int m = a0; m < a; ++m) {
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int kk = 4 * k4 + e2;
-            const float4 tv = mask_above(*reinterpret_cast<const float4 *>(tm + m16 * kk + t_row(kk)), col, m16 + kk);
-            fma4(y, as[e2], tv);
-          }
-        }
+      for (int kk = 0; kk < 16; ++kk) {
+        const int c = 16 * m + kk;
+        const float tv = Tm[c * kC + j];
+        const float4 *col = reinterpret_cast<const float4 *>(At + c * kC + 16 * a);
+        const float4 c0 = col[0], c1 = col[1], c2 = col[2], c3 = col[3];
+        y[0] = fmaf(-c0.x, tv, y[0]);
+        y[1] = fmaf(-c0.y, tv, y[1]);
+        y[2] = fmaf(-c0.z, tv, y[2]);
+        y[3] = fmaf(-c0.w, tv, y[3]);
+        y[4] = fmaf(-c1.x, tv, y[4]);
+        y[5] = fmaf(-c1.y, tv, y[5]);
+        y[6] = fmaf(-c1.z, tv, y[6]);
+        y[7] = fmaf(-c1.w, tv, y[7]);
+        y[8] = fmaf(-c2.x, tv, y[8]);
+        y[9] = fmaf(-c2.y, tv, y[9]);
+        y[10] = fmaf(-c2.z, tv, y[10]);
+        y[11] = fmaf(-c2.w, tv, y[11]);
+        y[12] = fmaf(-c3.x, tv, y[12]);
+        y[13] = fmaf(-c3.y, tv, y[13]);
+        y[14] = fmaf(-c3.z, tv, y[14]);
+        y[15] = fmaf(-c3.w, tv, y[15]);
       }
-      Y4[e] = y;  // [block][row i][4-column group q]
     }
-    group_sync(bar_id);
-    // T_ab(i, 4 q ..) = -sum over kk <= i of T(16 a + i, 16 a + kk) Y_ab(kk, 4 q ..)
-#pragma unroll 1
-    for (int e = r; e < nitems; e += kGroupThreads) {
-      const int bb = e / 64, i = (e / 4) % 16, q = e % 4, a = bb + L;
-      float *trow = Tp + t_row(16 * a + i);
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 tv = mask_above(*reinterpret_cast<const float4 *>(trow + 16 * a + 4 * k4), 4 * k4, i);
-        const float ts[4] = {tv.x, tv.y, tv.z, tv.w};
+    for (int ip = 0; ip < 15; ++ip) {
+      const float *col = At + (16 * a + ip) * kC + 16 * a;
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) fma4(t, ts[e2], Y4[bb * 64 + (4 * k4 + e2) * 4 + q]);
-      }
-      *reinterpret_cast<float4 *>(trow + 16 * bb + 4 * q) = make_float4(-t.x, -t.y, -t.z, -t.w);
+      for (int i = ip + 1; i < 16; ++i) y[i] = fmaf(-col[i], y[ip], y[i]);
     }
-    group_sync(bar_id);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Tm[(16 * a + i) * kC + j] = y[i];
   }
 }
 
@@ -270,56 +211,57 @@ __device__ __forceinline__ bool locate(const int32_t *cu, int n_seq, int total, 
   return true;
 }
 
-// Gate scan of one (chunk, v head) by one warp: two tokens per lane.
-__device__ __forceinline__ void form_gates(Gates &G, const RecurrentParams &p, int h, const Located &L, int lane) {
-  float la[2], bb[2];
-  int zi[2], ng[2];
+// The gates of one (chunk, v head), two tokens per lane (alpha 1 and beta 0
+// past the chunk's tokens).
+struct GateIn {
+  float a[2], b[2];
+};
+__device__ __forceinline__ GateIn load_gates(const RecurrentParams &p, int h, const Located &L, int lane) {
+  GateIn in;
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int t = 2 * lane + e;
-    const float a = t < L.nt ? __ldg(p.alpha + (int64_t)(L.t0 + t) * p.Hv + h) : 1.f;
-    bb[e] = t < L.nt ? __ldg(p.beta + (int64_t)(L.t0 + t) * p.Hv + h) : 0.f;
-    la[e] = a != 0.f ? log2f(fabsf(a)) : 0.f;
-    zi[e] = a == 0.f ? t : -1;
-    ng[e] = a < 0.f ? 1 : 0;
+    in.a[e] = t < L.nt ? __ldg(p.alpha + (int64_t)(L.t0 + t) * p.Hv + h) : 1.f;
+    in.b[e] = t < L.nt ? __ldg(p.beta + (int64_t)(L.t0 + t) * p.Hv + h) : 0.f;
   }
-  // inclusive scans over the 64 tokens (lane holds tokens 2 lane, 2 lane + 1)
-  float cs = la[0] + la[1];
-  int zs = max(zi[0], zi[1]), ns = ng[0] + ng[1];
+  return in;
+}
+
+// Gate products of one (chunk, v head) by one warp, two tokens per lane:
+// E_t = a_0 ... a_t (an inclusive product scan) and F_t = a_(t+1) ... a_(C-1)
+// (= E_(C-1) / E_t, formed as a product so that no zero or underflowed E
+// divides).  Products run in token order; a zero gate zeroes what follows it,
+// a negative one flips signs, and tiny ones fade to zero, as in the token
+// recurrence.
+__device__ __forceinline__ void form_gates(Gates &G, const GateIn &in, int lane) {
+  // inclusive product over this lane's pair, then over the lanes below
+  const float p0 = in.a[0], p01 = in.a[0] * in.a[1];
+  float inc = p01;
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
-    const float cu = __shfl_up_sync(0xffffffffu, cs, m);
-    const int zu = __shfl_up_sync(0xffffffffu, zs, m), nu = __shfl_up_sync(0xffffffffu, ns, m);
-    if (lane >= m) {
-      cs += cu;
-      zs = max(zs, zu);
-      ns += nu;
-    }
+    const float up = __shfl_up_sync(0xffffffffu, inc, m);
+    if (lane >= m) inc = up * inc;
   }
-  // exclusive prefix for this lane's first token
-  float cx = __shfl_up_sync(0xffffffffu, cs, 1);
-  int nx = __shfl_up_sync(0xffffffffu, ns, 1), zx = __shfl_up_sync(0xffffffffu, zs, 1);
-  if (lane == 0) {
-    cx = 0.f;
-    nx = 0;
-    zx = -1;
-  }
-  G.cum[2 * lane] = cx + la[0];
-  G.cum[2 * lane + 1] = cs;
-  G.seg[2 * lane] = max(zx, zi[0]);
-  G.seg[2 * lane + 1] = zs;
-  G.nneg[2 * lane] = nx + ng[0];
-  G.nneg[2 * lane + 1] = ns;
-  G.beta[2 * lane] = bb[0];
-  G.beta[2 * lane + 1] = bb[1];
-  __syncwarp();
+  float exc = __shfl_up_sync(0xffffffffu, inc, 1);  // product of the lanes below
+  if (lane == 0) exc = 1.f;
+  // suffix products: the lanes above, then within the pair
+  float suf = p01;
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int t = 2 * lane + e;
-    G.E[t] = gam(G, -1, t);
-    G.F[t] = gam(G, t, kC - 1);
+  for (int m = 1; m < 32; m <<= 1) {
+    const float dn = __shfl_down_sync(0xffffffffu, suf, m);
+    if (lane + m < 32) suf = suf * dn;
   }
-  if (lane == 0) G.e_last = gam(G, -1, kC - 1);
+  float above = __shfl_down_sync(0xffffffffu, suf, 1);  // product of the lanes above
+  if (lane == 31) above = 1.f;
+  G.a[2 * lane] = in.a[0];
+  G.a[2 * lane + 1] = in.a[1];
+  G.beta[2 * lane] = in.b[0];
+  G.beta[2 * lane + 1] = in.b[1];
+  G.E[2 * lane] = exc * p0;
+  G.E[2 * lane + 1] = exc * p01;
+  G.F[2 * lane] = in.a[1] * above;
+  G.F[2 * lane + 1] = above;
+  if (lane == 31) G.e_last = exc * p01;
   __syncwarp();
 }
 
@@ -439,7 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
     uint8_t *gsm = sm + OFF_GRP + grp * kGrpBytes;
     float *Ap = reinterpret_cast<float *>(gsm + G_A);
     float *Tp = reinterpret_cast<float *>(gsm + G_T);
-    float *Yp = reinterpret_cast<float *>(gsm + G_Y);
     Gates &G = *reinterpret_cast<Gates *>(gsm + G_GATES);
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's TMEM lanes
     const int t = r < kC ? r : r - kC;  // A row (r < 64) or B row
@@ -449,6 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
       const int g = (int)(it % p.Hk);
       Located L;
       if (!locate(cu, p.n_seq, p.total_tokens, s, p.idx, p.num_slots, L)) continue;
+      // the first head's gates in flight while the Gram product is awaited
+      GateIn gin;
+      if (r < 32 && grp < p.group) gin = load_gates(p, g * p.group + grp, L, lane);
       if (!wait_or_abort(&bars.gfull[n & 1], (n >> 1) & 1, lim, p.status, abort_flag)) break;
       tc::fence_after_sync();
       float graw[kC];
@@ -459,46 +403,50 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
       for (int u = grp; u < p.group; u += kGroups) {
         const int h = g * p.group + u;
         float *rec = p.ws + (s * p.Hv + h) * (int64_t)kRecFloats;
-        if (r < 32) form_gates(G, p, h, L, lane);
+        if (r < 32) {
+          if (u != grp) gin = load_gates(p, h, L, lane);
+          form_gates(G, gin, lane);
+        }
         group_sync(bar_id);
         {
-          // row t of Gam(j, t) o Gram (j <= t), four columns at a time
-          const float ct = G.cum[t], bt = G.beta[t];
-          const int st = G.seg[t], nt_neg = G.nneg[t];
-          float *arow = Ap + a_row(t), *brow = rec + kRecB + t * kC;
+          // row t of Gam(j, t) o Gram (j <= t): Gam(j, t) = a_(j+1) ... a_t as
+          // a running product from j = t down to 0
+          const float bt = G.beta[t];
+          float *brec = rec + kRecB;
+          float w[kC];
+          float gm = 1.f;
 #pragma unroll
-          for (int j4 = 0; j4 < kC; j4 += 4) {
-            float w[4];
+          for (int j = kC - 1; j >= 0; --j) {
+            if (j < t) gm *= G.a[j + 1];
+            w[j] = j <= t ? graw[j] * gm : 0.f;
+          }
+          if (r < kC) {  // A_tj = b_t Gam(j,t) k_t.k_j, j < t, transposed
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = j4 + e;
-              const float m = ex2(ct - G.cum[j]);
-              const float gm = (st > j || j > t) ? 0.f : (((nt_neg - G.nneg[j]) & 1) ? -m : m);
-              w[e] = graw[j] * gm;
-            }
-            if (r < kC) {  // A_tj = b_t Gam(j,t) k_t.k_j, j < t, packed
-              if (j4 < a1_of(t))
-                *reinterpret_cast<float4 *>(arow + j4) =
-                    make_float4(j4 < t ? bt * w[0] : 0.f, j4 + 1 < t ? bt * w[1] : 0.f, j4 + 2 < t ? bt * w[2] : 0.f,
-                                j4 + 3 < t ? bt * w[3] : 0.f);
-            } else if (j4 < 4 * row_groups(t)) {  // B_tj = Gam(j,t) q_t.k_j, j <= t, to the record
-              *reinterpret_cast<float4 *>(brow + j4) = make_float4(w[0], w[1], w[2], w[3]);
-            }
+            for (int j = 0; j < kC - 1; ++j)
+              if (j < t) Ap[j * kC + t] = bt * w[j];
+          } else {  // B_tj = Gam(j,t) q_t.k_j, j <= t, to the record
+#pragma unroll
+            for (int j4 = 0; j4 < kC; j4 += 4)
+              if (j4 < 4 * row_groups(t))
+                *reinterpret_cast<float4 *>(brec + rec_off(t, j4)) = make_float4(w[j4], w[j4 + 1], w[j4 + 2], w[j4 + 3]);
           }
         }
         group_sync(bar_id);
-        invert_unit_lower(Ap, Tp, Yp, r, bar_id);
+        // two of the group's warps invert, one per SM sub-partition pair
+        // (group 0: its warps 0 and 2, group 1: its warps 1 and 3)
+        if (((warp ^ grp) & 1) == 0) invert_unit_lower(Ap, Tp, 32 * ((warp & 3) >> 1) + lane, 2 * ((warp & 3) >> 1));
+        group_sync(bar_id);
         {
           // T' = T diag(b): row r / 2, columns 32 (r % 2) .. + 31
           const int tt = r >> 1, j0 = 32 * (r & 1);
-          const float *trow = Tp + t_row(tt);
-          float *dst = rec + kRecT + tt * kC;
+          const float *trow = Tp + tt * kC;
+          float *dst = rec + kRecT;
 #pragma unroll 1
           for (int j4 = j0; j4 < j0 + 32; j4 += 4) {
-            if (j4 >= b1_of(tt)) break;
+            if (j4 >= 4 * row_groups(tt)) break;
             // the packed row's slots above the diagonal are never written: mask them
             const float4 v4 = mask_above(*reinterpret_cast<const float4 *>(trow + j4), j4, tt);
-            *reinterpret_cast<float4 *>(dst + j4) =
+            *reinterpret_cast<float4 *>(dst + rec_off(tt, j4)) =
                 make_float4(v4.x * G.beta[j4], v4.y * G.beta[j4 + 1], v4.z * G.beta[j4 + 2], v4.w * G.beta[j4 + 3]);
           }
         }

@@ -13,12 +13,11 @@
 // The pages give the token recurrence only; the chunked form is its algebraic
 // rearrangement, exact up to rounding.
 //
-// Per chunk and v head (M 128 = state rows, thread r = row r = TMEM lane r):
-//   P'  = S (E o K)^T        N 64,  K 128   A = S from TMEM
-//   R'  = S (E o Q)^T        N 64,  K 128   A = S from TMEM
-//   D   = (V - P') T'^T      N 64,  K 64    A = X = V - P' from TMEM
-//   O   = R' + D B^T         N 64,  K 64    A = D from TMEM  (o_t of every row)
-//   S   = e_last S + D (F o K)   N 128, K 64    A = D from TMEM
+// Per chunk and v head (M 128 = state rows = TMEM lanes):
+//   [P' | R'] = S [E o K; E o Q]^T    N 128, K 128   A = S from TMEM
+//   D  = (V - P') T'^T                N 64,  K 64    A = X = V - P' from TMEM
+//   S  = e_last S + D (F o K)         N 128, K 64    A = D from TMEM
+//   O  = R' + D B^T                   N 64,  K 64    A = D from TMEM (o_t of every row)
 // Products in tf32 with an fp32 accumulator.  Every operand x is split as
 // x = hi + lo and each product formed as hi.hi + hi.lo + lo.hi: about 22
 // significant bits per operand, so the products carry fp32-level error (the
@@ -28,30 +27,34 @@
 // written; the other operands use hi = tf32 rounded to nearest.
 //
 // CTA = one (sequence, v head), 256 threads, one CTA per SM (TMEM: all 512
-// columns; shared memory ~201 KB):
-//   warps 0-3   row warps: thread r owns state row r; thread 0 issues P', R',
-//               D and O, thread 32 the state update (beside O), each once the
-//               operands it reads are in place;
-//   warps 4-7   producers: store the chunk's tf32 operand tiles into shared
-//               memory as the products that read the previous contents finish
-//               (E o K over the k half of the token-major tile, then T'; E o Q
-//               over the q half, then B; channel-major F o K), loading k, q
-//               and the records from global memory ahead of time.
-// Hand-offs go through mbarriers: producers -> MMA (tiles in shared memory),
-// row warps -> MMA (TMEM operands written, TMEM results read), MMA -> row
-// warps / producers (tcgen05.commit).  Every wait is bounded: on expiry the
-// thread records LSC_ERR_DEV_TIMEOUT, the CTA stops issuing work, waits
-// (bounded) for the MMAs it issued and frees its TMEM.
+// columns; shared memory ~201 KB).  Every warp runs the same code: warp w
+// reaches TMEM lanes 32 (w % 4) .. + 31, so thread (w, lane) owns state row
+// r = 32 (w % 4) + lane and the column half w / 4 of each row-wise pass (lo of
+// S, X, the decay, the split of D, the outputs), and a share of every operand
+// tile stored to shared memory.  Warp 0 waits until the operands of a product
+// are in place and one elected lane issues its MMAs and commits them (from
+// converged code, so the operands stay warp-uniform).  Per chunk c:
+//   [P' | R'](c) on the tensor core, meanwhile F o K (c) stored -> X formed,
+//   T' and B (c) stored over the [E o K; E o Q] tile -> D(c), meanwhile S
+//   decayed -> D split -> O(c), then update(c), meanwhile E o K (c+1) stored
+//   over T', E o Q (c+1) over B -> lo of S (c+1); the outputs of chunk c are
+//   written while [P' | R'](c+1) runs.
+// The loads of chunk c+1 (k, q, v, records) are issued during chunk c.
+// Hand-offs go through mbarriers: threads -> MMA (operands written), MMA ->
+// threads (tcgen05.commit).  Every wait is bounded: on expiry the thread
+// records LSC_ERR_DEV_TIMEOUT, the CTA stops issuing work, waits (bounded)
+// for the MMAs it issued and frees its TMEM.
 //
 // TMEM columns (lanes = state rows):
 //   0-127    S (fp32; the hi part of its own split)
-//   128-255  lo of S; after D: D hi (128-191), D lo (192-255)
-//   256-319  P'; after X is formed: D
-//   320-447  X hi (320-383), X lo (384-447)
-//   448-511  R', then O = R' + D B^T
+//   128-255  lo of S; after [P' | R']: X hi (128-191), X lo (192-255); after
+//            D: D hi (128-191), D lo (192-255)
+//   256-383  [P' | R'] of even chunks: P' (256-319), then D; R' (320-383), then O
+//   384-511  the same for odd chunks, so that a chunk's outputs are written
+//            while the next chunk's [P' | R'] runs
 // Shared-memory tiles (no swizzle, lsc_chunk.h): the token-major [E o K; E o Q]
-// tile (hi, lo), T' over its k half once P' has read it, B over its q half
-// once R' has; F o K channel-major (hi, lo).
+// tile (hi, lo), T' over its k half and B over its q half once [P' | R'] has
+// read it; F o K channel-major (hi, lo).
 #include "lsc_chunk.h"
 #include "lsc_gdn_common.cuh"
 #include "lsc_tc.h"
@@ -62,16 +65,11 @@ namespace {
 using namespace chunk;
 
 constexpr int kThreads = 256;
-constexpr int kRowThreads = 128;
-constexpr int kProd0 = 128;  // first producer thread
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t T_S = 0;
-constexpr uint32_t T_SLO = 128;
-constexpr uint32_t T_DHI = 128, T_DLO = 192;
-constexpr uint32_t T_P = 256, T_D = 256;
-constexpr uint32_t T_XHI = 320, T_XLO = 384;
-constexpr uint32_t T_R = 448;
+constexpr uint32_t T_LO = 128;   // lo of S; X hi / lo; D hi / lo
+constexpr uint32_t T_PR = 256;   // [P' | R'] of even chunks (P', then D; R', then O); odd chunks at + 128
 
 constexpr uint32_t OFF_KQHI = 0;
 constexpr uint32_t OFF_KQLO = kKqBytes;
@@ -90,49 +88,19 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, ui
   return false;
 }
 
-// Row warps (warps 0-3) synchronise among themselves on named barrier 1, in
-// the non-aligned forms (thread 0 may arrive apart from its warp), and leave
-// with the warp reconverged for the warp-wide .sync.aligned TMEM loads and
-// stores that follow.
-__device__ __forceinline__ void named_sync_rows() {
-  asm volatile("barrier.sync 1, 128;" ::: "memory");
+// true on every thread of the CTA when v is true on any of them; leaves every
+// warp reconverged for the warp-wide .sync.aligned TMEM loads and stores
+__device__ __forceinline__ bool cta_any(bool v) {
+  const bool r = __syncthreads_or(v) != 0;
   __syncwarp();
-}
-// true on every row thread when v is true on any of them
-__device__ __forceinline__ bool named_any_rows(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-      "barrier.red.or.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  __syncwarp();
-  return r != 0;
+  return r;
 }
 
 struct Bars {
-  uint64_t kqk, kqq, tk, tq, kt;  // producers: E o K, E o Q, T', B, F o K stored
-  uint64_t split, xt, dd;         // row warps: lo of S, X, D hi / lo (and the decayed S) written
-  uint64_t p, r, d, o, u;         // MMA commits
+  uint64_t kqk, kqq, kt;   // E o K, E o Q, F o K stored (every thread)
+  uint64_t split, xt, dd;  // lo of S; X, T' and B; D hi / lo and the decayed S written (every thread)
+  uint64_t pr, d, u, o;    // MMA commits
 };
-
-// 64 TMEM columns of this thread's lane as floats, one wait
-__device__ __forceinline__ void ld64(uint32_t taddr, float (&x)[kC]) {
-  uint32_t a[16], b[16], c[16], d[16];
-  tc::tmem_ld16(taddr, a);
-  tc::tmem_ld16(taddr + 16, b);
-  tc::tmem_ld16(taddr + 32, c);
-  tc::tmem_ld16(taddr + 48, d);
-  tc::tmem_wait_ld();
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    x[e] = __uint_as_float(a[e]);
-    x[16 + e] = __uint_as_float(b[e]);
-    x[32 + e] = __uint_as_float(c[e]);
-    x[48 + e] = __uint_as_float(d[e]);
-  }
-}
 
 __device__ __forceinline__ void sts_split4(uint8_t *sm, uint32_t off_hi, uint32_t off_lo, float4 f) {
   uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
@@ -144,14 +112,34 @@ __device__ __forceinline__ void sts_split4(uint8_t *sm, uint32_t off_hi, uint32_
   *reinterpret_cast<uint4 *>(sm + off_lo) = make_uint4(l0, l1, l2, l3);
 }
 
+__device__ __forceinline__ float4 ldg4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+
 __device__ __forceinline__ float4 scale4(float4 v, float s) { return make_float4(v.x * s, v.y * s, v.z * s, v.w * s); }
+
+// 4 x 4 transpose inside each aligned group of four lanes: lane k of the
+// group holds a[c] = element (k, c) and ends with a[r] = element (r, k).  Two
+// exchange steps (lanes k ^ 1, then k ^ 2), two shuffles each.
+__device__ __forceinline__ void transpose4(float (&a)[4], int lane) {
+  const bool odd = lane & 1, high = lane & 2;
+  float x0 = odd ? a[0] : a[1], x1 = odd ? a[2] : a[3];
+  float y0 = __shfl_xor_sync(0xffffffffu, x0, 1), y1 = __shfl_xor_sync(0xffffffffu, x1, 1);
+  const float t0 = odd ? y0 : a[0], t1 = odd ? a[1] : y0, t2 = odd ? y1 : a[2], t3 = odd ? a[3] : y1;
+  x0 = high ? t0 : t2;
+  x1 = high ? t1 : t3;
+  y0 = __shfl_xor_sync(0xffffffffu, x0, 2);
+  y1 = __shfl_xor_sync(0xffffffffu, x1, 2);
+  a[0] = high ? y0 : t0;
+  a[1] = high ? y1 : t1;
+  a[2] = high ? t2 : y0;
+  a[3] = high ? t3 : y1;
+}
 
 // lo part of x when the tensor cores read x itself as its hi part (truncation)
 __device__ __forceinline__ uint32_t lo_of_truncated(float x) {
   return tc::to_tf32(x - __uint_as_float(__float_as_uint(x) & 0xffffe000u));
 }
 
-// ---- MMA issue (one thread; three tf32 passes per product, unrolled) --------
+// ---- MMA issue (one thread; three tf32 passes per product) --------------------
 // A from TMEM (hi at a_hi, lo at a_lo; a k step of 8 columns), B from a
 // K-major shared-memory tile (hi / lo descriptors; a k step advances the start
 // address by kstep16 16-byte units).
@@ -206,19 +194,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
   TS *Sg = reinterpret_cast<TS *>(p.layer + (int64_t)slot * p.page + p.ssm_off) + (int64_t)h * dv * kDK;
 
   if (tid == 0) {
-    mbar_init(&bars.kqk, kThreads - kProd0);  // every producer thread
-    mbar_init(&bars.kqq, kThreads - kProd0);
-    mbar_init(&bars.tk, kThreads - kProd0);
-    mbar_init(&bars.tq, kThreads - kProd0);
-    mbar_init(&bars.kt, kThreads - kProd0);
-    mbar_init(&bars.split, kRowThreads);
-    mbar_init(&bars.xt, kRowThreads);
-    mbar_init(&bars.dd, kRowThreads);
-    mbar_init(&bars.p, 1);
-    mbar_init(&bars.r, 1);
+    mbar_init(&bars.kqk, kThreads);
+    mbar_init(&bars.kqq, kThreads);
+    mbar_init(&bars.kt, kThreads);
+    mbar_init(&bars.split, kThreads);
+    mbar_init(&bars.xt, kThreads);
+    mbar_init(&bars.dd, kThreads);
+    mbar_init(&bars.pr, 1);
     mbar_init(&bars.d, 1);
-    mbar_init(&bars.o, 1);
     mbar_init(&bars.u, 1);
+    mbar_init(&bars.o, 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -234,377 +219,398 @@ __global__ void __launch_bounds__(kThreads, 1) chunked_tc_kernel(const __grid_co
   volatile int *abort_flag = &s_abort;
   const uint64_t lim = p.wait_limit_ns;
 
-  if (warp < 4) {
-    // ======================================================= row warps
-    const int r = tid;
-    const bool row_ok = r < dv;
-    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
-    constexpr uint32_t id64 = tc::idesc_tf32(128, 64, false);
-    constexpr uint32_t id128 = tc::idesc_tf32(128, 128, false);
-    // B operand descriptors; a k step of 8 tf32 columns is 256 bytes along
-    // the token-major tile, 2 kLbo bytes along a 64-column tile
-    const uint64_t dk_hi = tc::smem_desc(smem_u32(sm + OFF_KQHI), 128, kKqRg);
-    const uint64_t dk_lo = tc::smem_desc(smem_u32(sm + OFF_KQLO), 128, kKqRg);
-    const uint64_t dq_hi = tc::smem_desc(smem_u32(sm + OFF_KQHI + kQRow0), 128, kKqRg);
-    const uint64_t dq_lo = tc::smem_desc(smem_u32(sm + OFF_KQLO + kQRow0), 128, kKqRg);
-    const uint64_t dt_hi = tc::smem_desc(smem_u32(sm + OFF_THI), kLbo, kRg64);
-    const uint64_t dt_lo = tc::smem_desc(smem_u32(sm + OFF_TLO), kLbo, kRg64);
-    const uint64_t db_hi = tc::smem_desc(smem_u32(sm + OFF_BHI), kLbo, kRg64);
-    const uint64_t db_lo = tc::smem_desc(smem_u32(sm + OFF_BLO), kLbo, kRg64);
-    const uint64_t dkt_hi = tc::smem_desc(smem_u32(sm + OFF_KTHI), kLbo, kRg64);
-    const uint64_t dkt_lo = tc::smem_desc(smem_u32(sm + OFF_KTLO), kLbo, kRg64);
-    constexpr uint32_t kq_step = 256 >> 4, sq_step = (2 * kLbo) >> 4;
-    uint64_t *last = nullptr;  // the last commit's barrier and phase (threads 0 and 32)
-    uint32_t last_par = 0;
-    auto commit = [&](uint64_t *bar, uint32_t par) {
-      tc::mma_commit(bar);
-      last = bar, last_par = par;
-    };
-    // initial state -> TMEM (zero when cold; rows >= dv stay zero)
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      uint32_t v[32];
+  // this thread's state row, column half and TMEM lanes
+  const int r0 = 32 * (warp & 3), r = r0 + lane, hf = warp >> 2;
+  // v and out move as 16-byte pieces (four rows of a token) when their rows
+  // allow it; lane 4 q + k then reaches rows r0 + 4 q .. + 3 of token 4 i + k
+  const bool vec = dv % 4 == 0 && (((uintptr_t)p.v | (uintptr_t)p.out) & 15) == 0;
+  const int rq = r0 + 4 * (lane >> 2), kq = lane & 3;
+  const bool row_ok = r < dv;
+  const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  // operand tiles: k / q blocks (tokens 4a..4a+3, a = al + 8 ah; channels
+  // 4 cg..4 cg+3) and T' / B pieces (row trow, columns 16 q4 + 4 m)
+  const int al = lane & 7, cg = (lane >> 3) + 4 * warp;
+  const int trow = tid & 63, q4 = tid >> 6;
+
+  constexpr uint32_t id64 = tc::idesc_tf32(128, 64, false);
+  constexpr uint32_t id128 = tc::idesc_tf32(128, 128, false);
+  // B operand descriptors; a k step of 8 tf32 columns is 256 bytes along the
+  // token-major tile, 2 kLbo bytes along a 64-column tile
+  const uint64_t dkq_hi = tc::smem_desc(smem_u32(sm + OFF_KQHI), 128, kKqRg);
+  const uint64_t dkq_lo = tc::smem_desc(smem_u32(sm + OFF_KQLO), 128, kKqRg);
+  const uint64_t dt_hi = tc::smem_desc(smem_u32(sm + OFF_THI), kLbo, kRg64);
+  const uint64_t dt_lo = tc::smem_desc(smem_u32(sm + OFF_TLO), kLbo, kRg64);
+  const uint64_t db_hi = tc::smem_desc(smem_u32(sm + OFF_BHI), kLbo, kRg64);
+  const uint64_t db_lo = tc::smem_desc(smem_u32(sm + OFF_BLO), kLbo, kRg64);
+  const uint64_t dkt_hi = tc::smem_desc(smem_u32(sm + OFF_KTHI), kLbo, kRg64);
+  const uint64_t dkt_lo = tc::smem_desc(smem_u32(sm + OFF_KTLO), kLbo, kRg64);
+  constexpr uint32_t kq_step = 256 >> 4, sq_step = (2 * kLbo) >> 4;
+  uint64_t *last = nullptr;  // warp 0: the last commit's barrier and phase
+  uint32_t last_par = 0;
+
+  // ---- per-chunk operands held in registers ----------------------------------
+  float4 kr[2][4], qr[2][4];  // k, q of this thread's blocks
+  float ev[2][4], fv[2][4];   // E, F of its tokens
+  float4 tv[4], bv[4];        // T', B pieces
+  float x[32];                // v of its row at tokens 32 hf .. 32 hf + 31 (vec: before transposing)
+  float e_last = 1.f;
+  auto load_kq = [&](int c) {
+    const int nt = min(kC, t1 - t0 - c * kC);
+    const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
+    const float *rec = recs + c * rec_stride;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = 0u;
-      if (warm && row_ok) {
-        if constexpr (sizeof(TS) == 4) {
-          const float4 *src = reinterpret_cast<const float4 *>(Sg + (int64_t)r * kDK + 32 * q);
+    for (int ah = 0; ah < 2; ++ah) {
+      const float4 e4 = ldg4(rec + kRecE + 4 * (al + 8 * ah)), f4 = ldg4(rec + kRecF + 4 * (al + 8 * ah));
+      ev[ah][0] = e4.x, ev[ah][1] = e4.y, ev[ah][2] = e4.z, ev[ah][3] = e4.w;
+      fv[ah][0] = f4.x, fv[ah][1] = f4.y, fv[ah][2] = f4.z, fv[ah][3] = f4.w;
+    }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 f = __ldg(src + e);
-            v[4 * e] = __float_as_uint(f.x);
-            v[4 * e + 1] = __float_as_uint(f.y);
-            v[4 * e + 2] = __float_as_uint(f.z);
-            v[4 * e + 3] = __float_as_uint(f.w);
-          }
-        } else {
-          const uint4 *src = reinterpret_cast<const uint4 *>(Sg + (int64_t)r * kDK + 32 * q);
+    for (int ah = 0; ah < 2; ++ah)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint4 b = __ldg(src + e);
-            const uint32_t w4[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              v[8 * e + 2 * k] = w4[k] << 16;
-              v[8 * e + 2 * k + 1] = w4[k] & 0xffff0000u;
-            }
-          }
-        }
+      for (int u = 0; u < 4; ++u) {
+        const int tok = 4 * (al + 8 * ah) + u;
+        const int64_t off = ((tb + tok) * p.Hk + g) * kDK + 4 * cg;
+        const bool in = tok < nt;
+        kr[ah][u] = in ? ldg4(p.k + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qr[ah][u] = in ? ldg4(p.q + off) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      __syncwarp();
-      tc::tmem_st32(tl + T_S + 32 * q, v);
+  };
+  auto load_rest = [&](int c) {  // v, T', B and e_last of chunk c
+    const int nt = min(kC, t1 - t0 - c * kC);
+    const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
+    const float *rec = recs + c * rec_stride;
+    if (vec) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int t = 32 * hf + 4 * i + kq;
+        const float4 f =
+            (t < nt && rq < dv) ? ldg4(p.v + ((tb + t) * p.Hv + h) * dv + rq) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[4 * i] = f.x, x[4 * i + 1] = f.y, x[4 * i + 2] = f.z, x[4 * i + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int t = 32 * hf + e;
+        x[e] = (t < nt && row_ok) ? __ldg(p.v + ((tb + t) * p.Hv + h) * dv + r) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int j4 = 16 * q4 + 4 * m;
+      const bool in = j4 < 4 * row_groups(trow);
+      tv[m] = in ? ldg4(rec + kRecT + rec_off(trow, j4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      bv[m] = in ? ldg4(rec + kRecB + rec_off(trow, j4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    e_last = __ldg(rec + kRecMisc);
+  };
+  // token-major E o K (rows 0-63) or E o Q (rows 64-127)
+  auto store_rows = [&](const float4 (&src)[2][4], int row0) {
+#pragma unroll
+    for (int ah = 0; ah < 2; ++ah)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = row0 + 4 * (al + 8 * ah) + u;
+        sts_split4(sm, OFF_KQHI + kq_off(j, 4 * cg), OFF_KQLO + kq_off(j, 4 * cg), scale4(src[ah][u], ev[ah][u]));
+      }
+  };
+  // channel-major F o K: K[j][c] F_j at (channel c, token j)
+  auto store_kt = [&]() {
+#pragma unroll
+    for (int ah = 0; ah < 2; ++ah) {
+      const int a = al + 8 * ah;
+      const float4 *k4 = kr[ah];
+      const float f0 = fv[ah][0], f1 = fv[ah][1], f2 = fv[ah][2], f3 = fv[ah][3];
+      const float col[4][4] = {{k4[0].x * f0, k4[1].x * f1, k4[2].x * f2, k4[3].x * f3},
+                               {k4[0].y * f0, k4[1].y * f1, k4[2].y * f2, k4[3].y * f3},
+                               {k4[0].z * f0, k4[1].z * f1, k4[2].z * f2, k4[3].z * f3},
+                               {k4[0].w * f0, k4[1].w * f1, k4[2].w * f2, k4[3].w * f3}};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int ch = 4 * cg + e;
+        sts_split4(sm, OFF_KTHI + sq_off(ch, 4 * a), OFF_KTLO + sq_off(ch, 4 * a),
+                   make_float4(col[e][0], col[e][1], col[e][2], col[e][3]));
+      }
+    }
+  };
+  auto publish = [&](uint64_t *bar) {
+    fence_proxy_async_smem();  // generic-proxy stores, read by the MMA
+    mbar_arrive(bar);
+  };
+  // lo of S (this thread's 64 columns) -> TMEM, then arrive on `split`
+  auto split_state = [&]() {
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      uint32_t v[32];
+      tc::tmem_ld32(tl + T_S + 64 * hf + 32 * q, v);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = lo_of_truncated(__uint_as_float(v[e]));
+      tc::tmem_st32(tl + T_LO + 64 * hf + 32 * q, v);
     }
     tc::tmem_wait_st();
-
-#pragma unroll 1
-    for (int c = 0; c < nch; ++c) {
-      const uint32_t par = c & 1;
-      const int nt = min(kC, t1 - t0 - c * kC);
-      const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
-      const float *rec = recs + c * rec_stride;
-      // v_t[r] of this chunk, in flight during the first steps
-      float x[kC];
-#pragma unroll
-      for (int t = 0; t < kC; ++t)
-        x[t] = (t < nt && row_ok) ? __ldg(p.v + ((tb + t) * p.Hv + h) * dv + r) : 0.f;
-      const float e_last = __ldg(rec + kRecMisc);
-
-      // ---- 1: lo of S (the update of the previous chunk is complete)
-      bool ok0 = true;
-      bool ok = c == 0 || wait_or_abort(&bars.u, par ^ 1, lim, p.status, abort_flag);
-      if (named_any_rows(!ok)) break;
-      tc::fence_after_sync();
-#pragma unroll 1
-      for (int q = 0; q < kDK / 32; ++q) {
-        uint32_t v[32];
-        tc::tmem_ld32(tl + T_S + 32 * q, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = lo_of_truncated(__uint_as_float(v[e]));
-        tc::tmem_st32(tl + T_SLO + 32 * q, v);
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      mbar_arrive(&bars.split);
-      if (r == 0) {
-        if ((ok0 = wait_or_abort(&bars.split, par, lim, p.status, abort_flag) &&
-                   wait_or_abort(&bars.kqk, par, lim, p.status, abort_flag))) {
-          tc::fence_after_sync();
-          issue3<kDK / 8>(tmem + T_P, tmem + T_S, tmem + T_SLO, dk_hi, dk_lo, kq_step, id64, false);  // P'
-          commit(&bars.p, par);
-        }
-        if (ok0 && (ok0 = wait_or_abort(&bars.kqq, par, lim, p.status, abort_flag))) {
-          tc::fence_after_sync();
-          issue3<kDK / 8>(tmem + T_R, tmem + T_S, tmem + T_SLO, dq_hi, dq_lo, kq_step, id64, false);  // R'
-          commit(&bars.r, par);
-        }
-      }
-      __syncwarp();
-
-      // ---- 2: X = V - P' -> tf32 hi / lo
-      ok = ok0 && wait_or_abort(&bars.p, par, lim, p.status, abort_flag);
-      if (named_any_rows(!ok)) break;
-      tc::fence_after_sync();
-      {
-        float pv[kC];
-        ld64(tl + T_P, pv);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) tc::split_tf32(x[16 * q + e] - pv[16 * q + e], hi[e], lo[e]);
-          tc::tmem_st16(tl + T_XHI + 16 * q, hi);
-          tc::tmem_st16(tl + T_XLO + 16 * q, lo);
-        }
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      mbar_arrive(&bars.xt);
-      if (r == 0 && ok0 &&
-          (ok0 = wait_or_abort(&bars.xt, par, lim, p.status, abort_flag) &&
-                 wait_or_abort(&bars.tk, par, lim, p.status, abort_flag))) {
-        tc::fence_after_sync();
-        issue3<kC / 8>(tmem + T_D, tmem + T_XHI, tmem + T_XLO, dt_hi, dt_lo, sq_step, id64, false);  // D
-        commit(&bars.d, par);
-      }
-      __syncwarp();
-
-      // ---- 3: S <- e_last S once R' (the last product reading S) is done
-      ok = ok0 && wait_or_abort(&bars.r, par, lim, p.status, abort_flag);
-      if (named_any_rows(!ok)) break;
-      tc::fence_after_sync();
-#pragma unroll 1
-      for (int q = 0; q < kDK / 32; ++q) {
-        uint32_t v[32];
-        tc::tmem_ld32(tl + T_S + 32 * q, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * e_last);
-        tc::tmem_st32(tl + T_S + 32 * q, v);
-      }
-
-      // ---- 4: D -> tf32 hi / lo (A of O and of the update)
-      ok = ok0 && wait_or_abort(&bars.d, par, lim, p.status, abort_flag);
-      if (named_any_rows(!ok)) break;
-      tc::fence_after_sync();
-      {
-        float dvv[kC];
-        ld64(tl + T_D, dvv);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) tc::split_tf32(dvv[16 * q + e], hi[e], lo[e]);
-          tc::tmem_st16(tl + T_DHI + 16 * q, hi);
-          tc::tmem_st16(tl + T_DLO + 16 * q, lo);
-        }
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      mbar_arrive(&bars.dd);
-      // O (thread 0) and the update (thread 32) read the same A operand: two
-      // issuing threads keep the tensor core fed
-      if (r == 0 && ok0 &&
-          (ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag) &&
-                 wait_or_abort(&bars.tq, par, lim, p.status, abort_flag))) {
-        tc::fence_after_sync();
-        issue3<kC / 8>(tmem + T_R, tmem + T_DHI, tmem + T_DLO, db_hi, db_lo, sq_step, id64, true);  // O
-        commit(&bars.o, par);
-      } else if (r == 32 && (ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag) &&
-                                   wait_or_abort(&bars.kt, par, lim, p.status, abort_flag))) {
-        tc::fence_after_sync();
-        issue3<kC / 8>(tmem + T_S, tmem + T_DHI, tmem + T_DLO, dkt_hi, dkt_lo, sq_step, id128, true);  // update
-        commit(&bars.u, par);
-      }
-      __syncwarp();
-
-      // ---- 5: outputs
-      ok = ok0 && wait_or_abort(&bars.o, par, lim, p.status, abort_flag);
-      if (named_any_rows(!ok)) break;
-      tc::fence_after_sync();
-      {
-        float *o = p.out + (tb * p.Hv + h) * dv + r;
-        const int64_t ostride = (int64_t)p.Hv * dv;
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[16];
-          tc::tmem_ld16(tl + T_R + 16 * q, w);
-          tc::tmem_wait_ld();
-          if (row_ok) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              if (16 * q + e < nt) o[(16 * q + e) * ostride] = __uint_as_float(w[e]);
-          }
-        }
-      }
-      tc::fence_before_sync();
-      named_sync_rows();  // every row has read O: the next R' may overwrite it
-    }
-    // ---- final state -> the slot
-    const bool fin = nch == 0 || wait_or_abort(&bars.u, (nch - 1) & 1, lim, p.status, abort_flag);
-    if (!named_any_rows(!fin || *abort_flag)) {
-      tc::fence_after_sync();
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t v[32];
-        __syncwarp();
-        tc::tmem_ld32(tl + T_S + 32 * q, v);
-        tc::tmem_wait_ld();
-        if (row_ok) {
-          if constexpr (sizeof(TS) == 4) {
-            float4 *dst = reinterpret_cast<float4 *>(Sg + (int64_t)r * kDK + 32 * q);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-          } else {
-            uint4 *dst = reinterpret_cast<uint4 *>(Sg + (int64_t)r * kDK + 32 * q);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint32_t w4[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * e + 2 * k]),
-                                                          __uint_as_float(v[8 * e + 2 * k + 1]));
-                w4[k] = *reinterpret_cast<uint32_t *>(&b2);
-              }
-              dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-          }
-        }
-      }
-    }
-    // every MMA issued must be complete before the TMEM is freed (threads 0
-    // and 32 each wait for their own last commit)
-    if ((r == 0 || r == 32) && last) mbar_wait_bounded(last, last_par, p.drain_limit_ns);
     tc::fence_before_sync();
-  } else {
-    // ======================================================= producers
-    const int pt = tid - kProd0, pw = pt >> 5;
-    const int al = lane & 7, bl = lane >> 3;
-    // k and q of a chunk: [token block half][channel block half][token in
-    // block]; this thread's 4 x 4 blocks are tokens 4a..4a+3, channels
-    // 4b..4b+3 with a = al + 8 ah, b = bl + 4 pw + 16 bh; E and F of its tokens
-    float4 kr[2][2][4], qr[2][2][4];
-    float ev[2][4], fv[2][4];
-    auto load_kq = [&](int c) {
-      const int nt = min(kC, t1 - t0 - c * kC);
-      const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
-      const float *rec = recs + c * rec_stride;
+    mbar_arrive(&bars.split);
+  };
+  // outputs of chunk c: O columns 32 hf .. + 31 of this row (buffer c % 2)
+  auto write_out = [&](int c) {
+    const int nt = min(kC, t1 - t0 - c * kC);
+    const int64_t tb = (int64_t)t0 + (int64_t)c * kC;
+    uint32_t w[32];
+    tc::tmem_ld32(tl + T_PR + 128 * (c & 1) + 64 + 32 * hf, w);
+    tc::tmem_wait_ld();
+    if (vec) {
 #pragma unroll
-      for (int ah = 0; ah < 2; ++ah)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int tok = 4 * (al + 8 * ah) + u;
-          ev[ah][u] = __ldg(rec + kRecE + tok);
-          fv[ah][u] = __ldg(rec + kRecF + tok);
-#pragma unroll
-          for (int bh = 0; bh < 2; ++bh) {
-            const int b = bl + 4 * pw + 16 * bh;
-            const int64_t off = ((tb + tok) * p.Hk + g) * kDK + 4 * b;
-            const bool in = tok < nt;
-            kr[ah][bh][u] = in ? __ldg(reinterpret_cast<const float4 *>(p.k + off)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            qr[ah][bh][u] = in ? __ldg(reinterpret_cast<const float4 *>(p.q + off)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-    };
-    // token-major E o K (rows 0-63) or E o Q (rows 64-127)
-    auto store_rows = [&](const float4 (&src)[2][2][4], int row0) {
-#pragma unroll
-      for (int ah = 0; ah < 2; ++ah)
-#pragma unroll
-        for (int bh = 0; bh < 2; ++bh)
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = 4 * (al + 8 * ah) + u, c4 = 4 * (bl + 4 * pw + 16 * bh);
-            sts_split4(sm, OFF_KQHI + kq_off(row0 + j, c4), OFF_KQLO + kq_off(row0 + j, c4),
-                       scale4(src[ah][bh][u], ev[ah][u]));
-          }
-    };
-    // channel-major F o K: K[j][c] F_j at (channel c, token j)
-    auto store_kt = [&]() {
-#pragma unroll
-      for (int ah = 0; ah < 2; ++ah) {
-        const int a = al + 8 * ah;
-        const float f0 = fv[ah][0], f1 = fv[ah][1], f2 = fv[ah][2], f3 = fv[ah][3];
-#pragma unroll
-        for (int bh = 0; bh < 2; ++bh) {
-          const int b = bl + 4 * pw + 16 * bh;
-          const float4 *k4 = kr[ah][bh];
-          const float col[4][4] = {{k4[0].x * f0, k4[1].x * f1, k4[2].x * f2, k4[3].x * f3},
-                                   {k4[0].y * f0, k4[1].y * f1, k4[2].y * f2, k4[3].y * f3},
-                                   {k4[0].z * f0, k4[1].z * f1, k4[2].z * f2, k4[3].z * f3},
-                                   {k4[0].w * f0, k4[1].w * f1, k4[2].w * f2, k4[3].w * f3}};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int ch = 4 * b + e;
-            sts_split4(sm, OFF_KTHI + sq_off(ch, 4 * a), OFF_KTLO + sq_off(ch, 4 * a),
-                       make_float4(col[e][0], col[e][1], col[e][2], col[e][3]));
-          }
-        }
+      for (int i = 0; i < 8; ++i) {
+        float a[4] = {__uint_as_float(w[4 * i]), __uint_as_float(w[4 * i + 1]), __uint_as_float(w[4 * i + 2]),
+                      __uint_as_float(w[4 * i + 3])};
+        transpose4(a, lane);  // lane 4 q + k: rows rq .. rq + 3 of token 4 i + k
+        const int t = 32 * hf + 4 * i + kq;
+        if (t < nt && rq < dv)
+          *reinterpret_cast<float4 *>(p.out + ((tb + t) * p.Hv + h) * dv + rq) = make_float4(a[0], a[1], a[2], a[3]);
       }
-    };
-    // T' and B of a chunk: row pt / 2, columns 32 (pt % 2) .. + 31 (the
-    // 16-byte groups past the diagonal's are zero and not read)
-    const int trow = pt >> 1, tj0 = 32 * (pt & 1);
-    float4 tv[8], bv[8];
-    auto load_tb = [&](int c) {
-      const float *rec = recs + c * rec_stride;
+    } else if (row_ok) {
+      float *o = p.out + ((tb + 32 * hf) * p.Hv + h) * dv + r;
+      const int64_t ostride = (int64_t)p.Hv * dv;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int j4 = tj0 + 4 * m;
-        const bool in = j4 < 4 * row_groups(trow);
-        tv[m] = in ? __ldg(reinterpret_cast<const float4 *>(rec + kRecT + trow * kC + j4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        bv[m] = in ? __ldg(reinterpret_cast<const float4 *>(rec + kRecB + trow * kC + j4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    };
-    auto store_sq = [&](const float4 (&src)[8], uint32_t off_hi, uint32_t off_lo) {
-#pragma unroll
-      for (int m = 0; m < 8; ++m)
-        sts_split4(sm, off_hi + sq_off(trow, tj0 + 4 * m), off_lo + sq_off(trow, tj0 + 4 * m), src[m]);
-    };
-    auto publish = [&](uint64_t *bar) {
-      fence_proxy_async_smem();  // generic-proxy stores, read by the MMA
-      mbar_arrive(bar);
-    };
+      for (int e = 0; e < 32; ++e)
+        if (32 * hf + e < nt) o[e * ostride] = __uint_as_float(w[e]);
+    }
+  };
 
-    // Chunk c's tiles are stored as the products reading the previous
-    // contents finish: T' after P'(c), B after R'(c); then the next chunk's
-    // E o K after D(c), E o Q after O(c), F o K after the update of chunk c.
-    if (nch > 0) {
-      load_kq(0);
-      store_rows(kr, 0);
-      publish(&bars.kqk);
-      store_rows(qr, kC);
-      publish(&bars.kqq);
-      store_kt();
-      publish(&bars.kt);
-      load_tb(0);
-    }
+  // ---- initial state -> TMEM (zero when cold; rows >= dv stay zero)
 #pragma unroll 1
-    for (int c = 0; c < nch && !*abort_flag; ++c) {
-      const uint32_t par = c & 1;
-      if (!wait_or_abort(&bars.p, par, lim, p.status, abort_flag)) break;
-      store_sq(tv, OFF_THI, OFF_TLO);
-      publish(&bars.tk);
-      if (!wait_or_abort(&bars.r, par, lim, p.status, abort_flag)) break;
-      store_sq(bv, OFF_BHI, OFF_BLO);
-      publish(&bars.tq);
-      if (c + 1 == nch) break;
-      load_kq(c + 1);
-      if (!wait_or_abort(&bars.d, par, lim, p.status, abort_flag)) break;
-      store_rows(kr, 0);
-      publish(&bars.kqk);
-      if (!wait_or_abort(&bars.o, par, lim, p.status, abort_flag)) break;
-      store_rows(qr, kC);
-      publish(&bars.kqq);
-      if (!wait_or_abort(&bars.u, par, lim, p.status, abort_flag)) break;
-      store_kt();
-      publish(&bars.kt);
-      load_tb(c + 1);
+  for (int q = 0; q < 2; ++q) {
+    uint32_t v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = 0u;
+    const int col0 = 64 * hf + 32 * q;
+    if (warm && row_ok) {
+      if constexpr (sizeof(TS) == 4) {
+        const float4 *src = reinterpret_cast<const float4 *>(Sg + (int64_t)r * kDK + col0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 f = __ldg(src + e);
+          v[4 * e] = __float_as_uint(f.x);
+          v[4 * e + 1] = __float_as_uint(f.y);
+          v[4 * e + 2] = __float_as_uint(f.z);
+          v[4 * e + 3] = __float_as_uint(f.w);
+        }
+      } else {
+        const uint4 *src = reinterpret_cast<const uint4 *>(Sg + (int64_t)r * kDK + col0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint4 b = __ldg(src + e);
+          const uint32_t w4[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[8 * e + 2 * k] = w4[k] << 16;
+            v[8 * e + 2 * k + 1] = w4[k] & 0xffff0000u;
+          }
+        }
+      }
     }
+    __syncwarp();
+    tc::tmem_st32(tl + T_S + col0, v);
+  }
+  tc::tmem_wait_st();
+
+  // ---- chunk 0's operands
+  if (nch > 0) {
+    load_kq(0);
+    load_rest(0);
+    split_state();
+    store_rows(kr, 0);
+    publish(&bars.kqk);
+    store_rows(qr, kC);
+    publish(&bars.kqq);
+    store_kt();
+    publish(&bars.kt);
   }
 
+  bool ok = true;
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    const uint32_t par = c & 1;
+    const uint32_t pr = T_PR + 128 * par;  // this chunk's [P' | R'] buffer
+    const bool more = c + 1 < nch;
+    bool ok0 = true;  // warp 0: its waits succeeded
+    // ---- [P' | R'] once lo of S and the [E o K; E o Q] tile are in place
+    if (warp == 0) {
+      // every lane observes the operands' barriers (the elected lane issues)
+      ok0 = wait_or_abort(&bars.split, par, lim, p.status, abort_flag) &&
+            wait_or_abort(&bars.kqk, par, lim, p.status, abort_flag) &&
+            wait_or_abort(&bars.kqq, par, lim, p.status, abort_flag);
+      ok0 = __all_sync(0xffffffffu, ok0);
+      if (ok0) {
+        tc::fence_after_sync();
+        if (tc::elect_one()) {
+          issue3<kDK / 8>(tmem + pr, tmem + T_S, tmem + T_LO, dkq_hi, dkq_lo, kq_step, id128, false);
+          tc::mma_commit(&bars.pr);
+        }
+        __syncwarp();
+        last = &bars.pr, last_par = par;
+      }
+    }
+    // ---- meanwhile: F o K of this chunk (the previous update has read the
+    // tile), then the next chunk's k and q in flight
+    if (c > 0) {
+      store_kt();
+      publish(&bars.kt);
+      write_out(c - 1);  // the previous chunk's O, in the other buffer
+    }
+    if (more) load_kq(c + 1);
+
+    // ---- X = V - P' -> tf32 hi / lo; T' and B over the [E o K; E o Q] tile
+    ok = ok0 && wait_or_abort(&bars.pr, par, lim, p.status, abort_flag);
+    if (cta_any(!ok)) break;
+    tc::fence_after_sync();
+    if (vec) {  // v arrived as 16-byte pieces of four rows: to this thread's row
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float a[4] = {x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]};
+        transpose4(a, lane);
+        x[4 * i] = a[0], x[4 * i + 1] = a[1], x[4 * i + 2] = a[2], x[4 * i + 3] = a[3];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {  // unrolled: x is indexed by q
+      uint32_t w[16], hi[16], lo[16];
+      tc::tmem_ld16(tl + pr + 32 * hf + 16 * q, w);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) tc::split_tf32(x[16 * q + e] - __uint_as_float(w[e]), hi[e], lo[e]);
+      tc::tmem_st16(tl + T_LO + 32 * hf + 16 * q, hi);
+      tc::tmem_st16(tl + T_LO + 64 + 32 * hf + 16 * q, lo);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int j4 = 16 * q4 + 4 * m;
+      sts_split4(sm, OFF_THI + sq_off(trow, j4), OFF_TLO + sq_off(trow, j4), tv[m]);
+      sts_split4(sm, OFF_BHI + sq_off(trow, j4), OFF_BLO + sq_off(trow, j4), bv[m]);
+    }
+    tc::tmem_wait_st();
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    mbar_arrive(&bars.xt);
+    if (warp == 0 && ok0) {
+      ok0 = __all_sync(0xffffffffu, wait_or_abort(&bars.xt, par, lim, p.status, abort_flag));
+      if (ok0) {
+        tc::fence_after_sync();
+        if (tc::elect_one()) {
+          issue3<kC / 8>(tmem + pr, tmem + T_LO, tmem + T_LO + 64, dt_hi, dt_lo, sq_step, id64, false);  // D
+          tc::mma_commit(&bars.d);
+        }
+        __syncwarp();
+        last = &bars.d, last_par = par;
+      }
+    }
+    // ---- meanwhile: the next chunk's v, T', B and e_last in flight
+    const float e_cur = e_last;
+    if (more) load_rest(c + 1);
+
+    // ---- S <- e_last S ([P' | R'], the last product reading S, is done)
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      uint32_t v[32];
+      tc::tmem_ld32(tl + T_S + 64 * hf + 32 * q, v);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * e_cur);
+      tc::tmem_st32(tl + T_S + 64 * hf + 32 * q, v);
+    }
+
+    // ---- D -> tf32 hi / lo (A of O and of the update)
+    ok = ok0 && wait_or_abort(&bars.d, par, lim, p.status, abort_flag);
+    if (cta_any(!ok)) break;
+    tc::fence_after_sync();
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      uint32_t w[16], hi[16], lo[16];
+      tc::tmem_ld16(tl + pr + 32 * hf + 16 * q, w);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) tc::split_tf32(__uint_as_float(w[e]), hi[e], lo[e]);
+      tc::tmem_st16(tl + T_LO + 32 * hf + 16 * q, hi);
+      tc::tmem_st16(tl + T_LO + 64 + 32 * hf + 16 * q, lo);
+    }
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+    mbar_arrive(&bars.dd);
+    if (warp == 0 && ok0) {
+      ok0 = wait_or_abort(&bars.dd, par, lim, p.status, abort_flag) &&
+            wait_or_abort(&bars.kt, par, lim, p.status, abort_flag);
+      ok0 = __all_sync(0xffffffffu, ok0);
+      if (ok0) {
+        tc::fence_after_sync();
+        if (tc::elect_one()) {
+          issue3<kC / 8>(tmem + pr + 64, tmem + T_LO, tmem + T_LO + 64, db_hi, db_lo, sq_step, id64, true);  // O
+          tc::mma_commit(&bars.o);
+          issue3<kC / 8>(tmem + T_S, tmem + T_LO, tmem + T_LO + 64, dkt_hi, dkt_lo, sq_step, id128, true);  // update
+          tc::mma_commit(&bars.u);
+        }
+        __syncwarp();
+        last = &bars.u, last_par = par;
+      }
+    }
+
+    // ---- meanwhile: the next chunk's E o K over T' (D has read it)
+    if (more) {
+      store_rows(kr, 0);
+      publish(&bars.kqk);
+    }
+    // ---- O done: the next chunk's E o Q over B, this chunk's outputs
+    ok = ok0 && wait_or_abort(&bars.o, par, lim, p.status, abort_flag);
+    if (cta_any(!ok)) break;
+    tc::fence_after_sync();
+    if (more) {
+      store_rows(qr, kC);
+      publish(&bars.kqq);
+    }
+    // ---- update done: lo of the next chunk's S
+    ok = ok0 && wait_or_abort(&bars.u, par, lim, p.status, abort_flag);
+    if (cta_any(!ok)) break;
+    tc::fence_after_sync();
+    if (more) split_state();
+  }
+
+  if (ok && nch > 0 && !*abort_flag) write_out(nch - 1);  // (uniform: ok and the flag are CTA-wide after the votes)
+
+  // ---- final state -> the slot (every thread takes part in the vote)
+  const bool fin = !cta_any(!ok || *abort_flag);
+  if (fin) {
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      uint32_t v[32];
+      const int col0 = 64 * hf + 32 * q;
+      tc::tmem_ld32(tl + T_S + col0, v);
+      tc::tmem_wait_ld();
+      if (row_ok) {
+        if constexpr (sizeof(TS) == 4) {
+          float4 *dst = reinterpret_cast<float4 *>(Sg + (int64_t)r * kDK + col0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                 __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(Sg + (int64_t)r * kDK + col0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * e + 2 * k]),
+                                                        __uint_as_float(v[8 * e + 2 * k + 1]));
+              w4[k] = *reinterpret_cast<uint32_t *>(&b2);
+            }
+            dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+    }
+  }
+  // every MMA issued must be complete before the TMEM is freed
+  if (tid == 0 && last) mbar_wait_bounded(last, last_par, p.drain_limit_ns);  // (warp 0 issued them)
+  tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) {
     tc::fence_after_sync();

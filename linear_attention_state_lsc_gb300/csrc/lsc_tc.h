@@ -73,6 +73,18 @@ __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence
 
 // ---- MMA (issued by one thread) ------------------------------------------------
 
+// True on one lane of the calling (converged) warp.  Issuing MMAs under it
+// from code that every lane of the warp runs keeps their operands
+// warp-uniform, so they stay in uniform registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t is = 0;
+  asm volatile(
+      "{\n\t.reg .b32 lid;\n\t.reg .pred p;\n\telect.sync lid|p, %1;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(is)
+      : "r"(0xffffffffu));
+  return is != 0;
+}
+
 // D[tmem] (+)= A[smem] x B[smem]^T  (A: M x K, B: N x K as seen by the descriptors)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
