@@ -52,6 +52,16 @@ def peaks():
     return FALLBACK_HBM, "fallback"
 
 
+def measured(key, default):
+    """One figure of MEASURED_PEAKS.json, or `default` when the file is absent."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        if key in d:
+            return float(d[key])
+    return default
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
@@ -605,25 +615,47 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     flops = 6.0 * T * w.num_v_heads * w.head_v_dim * w.head_k_dim * nl
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     fp32_peak = sms * 128 * 2 * 2070e6
+    # the chunked order's caller workspace, allocated once outside the timing
+    ra0 = L.recurrent_args(64, w.num_k_heads, T, idx, has, *dev, out, algorithm=L.LSC_RECURRENT_AUTO)
+    _, ws_bytes = L.lsc_gdn_recurrent_workspace_bytes(pool, ra0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     rec = {}
-    for algo in (L.LSC_RECURRENT_TOKEN, L.LSC_RECURRENT_CHUNKED):
-        ra = L.recurrent_args(64, w.num_k_heads, T, idx, has, *dev, out, algorithm=algo)
+    for algo in (L.LSC_RECURRENT_AUTO, L.LSC_RECURRENT_TOKEN):
+        ra = L.recurrent_args(64, w.num_k_heads, T, idx, has, *dev, out, algorithm=algo,
+                              workspace=ws if algo == L.LSC_RECURRENT_AUTO else None,
+                              workspace_bytes=ws_bytes if algo == L.LSC_RECURRENT_AUTO else 0)
         rec[algo] = timed(lambda: rec_all(ra), 2)
-    t, t_ch = rec[L.LSC_RECURRENT_TOKEN], rec[L.LSC_RECURRENT_CHUNKED]
+    t, t_tok = rec[L.LSC_RECURRENT_AUTO], rec[L.LSC_RECURRENT_TOKEN]
+    # tensor-core work of the chunked order, tf32 x 3 passes: per (chunk, v head)
+    # [P'|R'] 2*128*128*128, D and O 2*128*64*64 each, the update 2*128*128*64;
+    # per (chunk, qk head) the Gram product 2*128*64*128
+    n_chunks = sum((int(n) + 63) // 64 for n in lengths)
+    tc_flops = 3.0 * nl * (n_chunks * w.num_v_heads * (2.0 * 128 ** 3 + 2 * 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
+                           + n_chunks * w.num_k_heads * 2.0 * 128 * 64 * 128)
+    tf32_peak = measured("bf16_tflops", 1900.0) * 1e12 * 1.1 / 2.25
     parts["recurrent_c4"] = {"workload": f"c4: 64 sequences, {T} tokens, 36 layers, state [32,128,128] f32",
-                             "kernel": "recurrent128_kernel<f32> (token order, two tokens per pass over the state; the default)",
+                             "kernel": "chunk_prep_kernel + chunked_tc_kernel<f32> (64-token chunks on the tensor "
+                                       "cores, tf32 x 3; the default at head_k_dim 128)",
                              "ms_per_36_layers": round(t * 1e3, 3),
                              "token_layers_per_s": round(T * nl / t, 1),
                              "TFLOP/s": round(flops / t / 1e12, 2),
                              "roofline": {"bound": "alu", "peak_TFLOP/s": round(fp32_peak / 1e12, 1),
                                           "frac": round(flops / t / fp32_peak, 4),
-                                          "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 flop x 2070 MHz"},
-                             "flops_basis": "6 dk dv per (token, head): S k, the rank-1 update, S q; "
-                                            "frac_7dkdv counts 7 dk dv (with the decay of S)",
-                             "frac_7dkdv": round(flops * 7 / 6 / t / fp32_peak, 4),
-                             "chunked": {"kernel": "recurrent_chunked_kernel<f32> (16-token chunks)",
-                                         "ms_per_36_layers": round(t_ch * 1e3, 3),
-                                         "frac": round(flops / t_ch / fp32_peak, 4)}}
+                                          "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 flop x 2070 MHz: the token "
+                                                        "recurrence's own bound, kept for comparison"},
+                             "flops_basis": "algorithmic: 6 dk dv per (token, v head) -- S k, the rank-1 update, "
+                                            "S q -- whichever order computes it",
+                             "tensor": {"TFLOP/s_issued": round(tc_flops / t / 1e12, 1),
+                                        "tf32_peak_TFLOP/s": round(tf32_peak / 1e12, 1),
+                                        "frac": round(tc_flops / t / tf32_peak, 4),
+                                        "peak_basis": "measured bf16 burst x 1.1/2.25 (tf32 vs bf16 nominal)",
+                                        "work_basis": "tf32 x 3 products of both kernels"},
+                             "workspace_bytes_per_layer": int(ws_bytes),
+                             "token": {"kernel": "recurrent128_kernel<f32> (token order, two tokens per pass)",
+                                       "ms_per_36_layers": round(t_tok * 1e3, 3),
+                                       "frac": round(flops / t_tok / fp32_peak, 4)},
+                             "speedup_vs_token": round(t_tok / t, 3)}
+    del ws
     L.lsc_pool_destroy(pool)
     del buf, out, dev
     torch.cuda.empty_cache()
@@ -926,7 +958,7 @@ NCU_CASES = {
     "restore": ("c1", 64, "restore"),        # 64 hits x 2 layers, 549 MB per launch
     "restore_c3": ("c3", 512, "restore"),    # the c3 storm on 2 of its 36 layers (4.4 GB pool, 1.76 GB algorithmic)
     "recurrent": ("c4", 16, "recurrent"),    # 16 sequences of 64..512 tokens, one layer (token order)
-    "recurrent_chunked": ("c4", 16, "recurrent_chunked"),  # the same, 16-token chunks
+    "recurrent_chunked": ("c4", 16, "recurrent_chunked"),  # the same, 64-token chunks (preparation + state kernels)
     "prefill": ("c4", 32, "prefill"),        # prefill conv: 32 sequences of 64..2048 tokens, one layer
     "copy_prefix": ("c1", 4, "copy_prefix"), # K/V copy: 12 layers x 512 blocks of 64 KiB, 4 prefixes of 32 blocks
 }

@@ -286,17 +286,19 @@ typedef struct {
   const float *alpha;        /* device [T, Hv] */
   const float *beta;         /* device [T, Hv] */
   float *out;                /* device [T, Hv, dv] */
-  void *workspace;           /* CHUNKED only: device scratch of at least workspace_bytes
-                                (lsc_gdn_recurrent_workspace_bytes), 16-byte aligned, free
-                                until the call's work on the stream completes; NULL = the
-                                library takes it from the device's stream-ordered pool
-                                (cudaMallocAsync / cudaFreeAsync on the call's stream) */
+  void *workspace;           /* chunked order only: device scratch of at least
+                                workspace_bytes (lsc_gdn_recurrent_workspace_bytes),
+                                16-byte aligned, untouched by others until the call's work
+                                on the stream completes; NULL = the library takes it from
+                                the device's stream-ordered pool (cudaMallocAsync /
+                                cudaFreeAsync on the call's stream) */
   size_t workspace_bytes;
 } lsc_gdn_recurrent_args;
 
 /* Evaluation order of lsc_gdn_recurrent (both give the token recurrence's
  * result up to fp32 rounding). */
-#define LSC_RECURRENT_AUTO 0    /* the library's choice (currently TOKEN, the faster one) */
+#define LSC_RECURRENT_AUTO 0    /* the library's choice: CHUNKED for head_k_dim 128 (the faster
+                                   one there), TOKEN otherwise */
 #define LSC_RECURRENT_TOKEN 1   /* one token at a time */
 #define LSC_RECURRENT_CHUNKED 2 /* 64 tokens at a time on the tensor cores: the token recurrence
                                    rearranged into per-chunk products (head_k_dim 128 only);
@@ -314,6 +316,13 @@ typedef struct {
  * aligned (MISALIGNED).  algorithm selects the evaluation order (any other
  * value: INVALID_ARG).  Supported: head_k_dim in {16, 32, 64, 128} (CHUNKED:
  * 128 only), head_v_dim <= 128, ssm dtype f32 or bf16; else UNSUPPORTED.
+ * The chunked order runs two kernels on the stream: the first writes the
+ * state-free records of every chunk into the workspace, the second reads them.
+ * A caller workspace that is too small gives INVALID_ARG, one not 16-byte
+ * aligned MISALIGNED; a failed stream-ordered allocation NO_MEMORY.  With
+ * cu_seqlens not non-decreasing, chunk records of different sequences may
+ * share workspace slots, and the results of every sequence of the call are
+ * then unspecified (the offending sequence is reported as above).
  */
 int lsc_gdn_recurrent(lsc_pool *pool, int32_t layer, const lsc_gdn_recurrent_args *args,
                       void *stream);
@@ -321,7 +330,8 @@ int lsc_gdn_recurrent(lsc_pool *pool, int32_t layer, const lsc_gdn_recurrent_arg
 /*
  * Device scratch that lsc_gdn_recurrent needs for `args` (its n_seq,
  * total_tokens and algorithm; the pool gives num_v_heads and head_k_dim): 0
- * for TOKEN; for CHUNKED one 33 344-byte record per (64-token chunk slot,
+ * when the call runs the token order; for the chunked order (CHUNKED, or AUTO
+ * with head_k_dim 128) one 33 344-byte record per (64-token chunk slot,
  * v head), with (total_tokens + 63) / 64 + n_seq chunk slots -- the records of
  * the state-free quantities of every chunk (lsc_chunk.h), written by the
  * call's first kernel and read by its second.  Host only, no device work.

@@ -600,8 +600,10 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
   if (!all_aligned({a->idx, a->cu_seqlens, a->v, a->alpha, a->beta, a->out}, 4)) return LSC_ERR_MISALIGNED;
   if (g.ssm_dtype == LSC_F16) return LSC_ERR_UNSUPPORTED;
   if (a->n_seq > 65535) return LSC_ERR_UNSUPPORTED;
-  // AUTO takes the token kernel: on the CUDA cores it is the faster of the two
-  const bool chunked = a->algorithm == LSC_RECURRENT_CHUNKED;
+  // AUTO takes the chunked form on the tensor cores where it applies (head_k_dim
+  // 128), the faster of the two there; the token kernels elsewhere
+  const bool chunked = a->algorithm == LSC_RECURRENT_CHUNKED ||
+                       (a->algorithm == LSC_RECURRENT_AUTO && g.dk == lsc::chunk::kDK);
   if (chunked && g.dk != lsc::chunk::kDK) return LSC_ERR_UNSUPPORTED;
   if (chunked && a->workspace != nullptr &&
       (((uintptr_t)a->workspace & 15) != 0 ||
@@ -657,9 +659,9 @@ int lsc_gdn_recurrent(lsc_pool *p, int32_t layer, const lsc_gdn_recurrent_args *
 
 int lsc_gdn_recurrent_workspace_bytes(const lsc_pool *p, const lsc_gdn_recurrent_args *a, size_t *bytes) {
   if (!p || !a || !bytes || a->n_seq < 0 || a->total_tokens < 0) return LSC_ERR_INVALID_ARG;
-  *bytes = a->algorithm == LSC_RECURRENT_CHUNKED
-               ? (size_t)lsc::chunk::workspace_bytes(a->total_tokens, a->n_seq, p->g.Hv)
-               : 0;
+  const bool chunked = a->algorithm == LSC_RECURRENT_CHUNKED ||
+                       (a->algorithm == LSC_RECURRENT_AUTO && p->g.dk == lsc::chunk::kDK);
+  *bytes = chunked ? (size_t)lsc::chunk::workspace_bytes(a->total_tokens, a->n_seq, p->g.Hv) : 0;
   return LSC_OK;
 }
 
