@@ -340,6 +340,28 @@ int lsc_gdn_recurrent(lsc_pool *pool, int32_t layer, const lsc_gdn_recurrent_arg
 int lsc_gdn_recurrent_workspace_bytes(const lsc_pool *pool, const lsc_gdn_recurrent_args *args,
                                       size_t *bytes);
 
+/*
+ * lsc_gdn_recurrent's chunked order without any device allocation, for callers
+ * that may not allocate at call time (a serving loop with a fixed device
+ * footprint, a host whose own allocator owns the GPU's memory, a path that
+ * cannot afford an allocation's synchronisation).  The pages describe no such
+ * call; it is a convenience of this library.
+ *
+ * Same arguments and results as lsc_gdn_recurrent with algorithm CHUNKED
+ * (args->algorithm must be AUTO or CHUNKED, args->workspace NULL and
+ * args->workspace_bytes 0, else INVALID_ARG; head_k_dim must be 128, else
+ * UNSUPPORTED).  The per-chunk records go to a scratch array of 64 MiB that the
+ * library keeps in each device's memory for the life of the process; a call
+ * whose records need more (lsc_gdn_recurrent_workspace_bytes with CHUNKED)
+ * returns NO_MEMORY before any work.  The first call on a device, with that
+ * device current, looks up the array's device address (a runtime query, no
+ * allocation); make that first call before any stream capture.  All calls
+ * share the array: calls whose work may overlap on the GPU race and must be
+ * ordered by the caller.
+ */
+int lsc_gdn_recurrent_noalloc(lsc_pool *pool, int32_t layer, const lsc_gdn_recurrent_args *args,
+                              void *stream);
+
 /* Arguments of lsc_gdn_prefill_conv.  T = total_tokens; sequence i owns tokens
  * cu_seqlens[i] .. cu_seqlens[i+1]-1 of x, q, k and v. */
 typedef struct {

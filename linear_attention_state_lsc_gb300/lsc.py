@@ -161,6 +161,7 @@ def load():
         "lsc_gdn_recurrent": ([P, I32, C.POINTER(lsc_gdn_recurrent_args), P], C.c_int),
         "lsc_gdn_recurrent_workspace_bytes": ([P, C.POINTER(lsc_gdn_recurrent_args), C.POINTER(C.c_size_t)],
                                               C.c_int),
+        "lsc_gdn_recurrent_noalloc": ([P, I32, C.POINTER(lsc_gdn_recurrent_args), P], C.c_int),
         "lsc_gdn_prefill_conv": ([P, I32, C.POINTER(lsc_gdn_prefill_conv_args), P], C.c_int),
         "lsc_kv_pool_required_bytes": ([C.POINTER(lsc_kv_pool_desc), C.POINTER(C.c_size_t)], C.c_int),
         "lsc_kv_pool_create": ([C.POINTER(lsc_kv_pool_desc), P, C.c_size_t, C.POINTER(P)], C.c_int),
@@ -335,6 +336,10 @@ def recurrent_args(n_seq, num_k_heads, total_tokens, idx, has_init, cu_seqlens, 
     return lsc_gdn_recurrent_args(n_seq, num_k_heads, total_tokens, algorithm, ptr(idx), ptr(has_init),
                                   ptr(cu_seqlens), ptr(q), ptr(k), ptr(v), ptr(alpha), ptr(beta),
                                   ptr(out), ptr(workspace), workspace_bytes)
+
+
+def lsc_gdn_recurrent_noalloc(pool, layer, args, stream=None):
+    return load().lsc_gdn_recurrent_noalloc(pool, layer, C.byref(args), _stream(stream))
 
 
 def lsc_gdn_recurrent_workspace_bytes(pool, args):
