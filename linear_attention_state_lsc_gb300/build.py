@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblsc.so")
-SOURCES = ["lsc_host.cu", "lsc_copy.cu", "lsc_gdn.cu", "lsc_rec128.cu", "lsc_chunked.cu", "lsc_chunked_tc.cu", "lsc_chunk_prep.cu", "lsc_noalloc.cu", "lsc_decode_f32.cu", "lsc_decode_bf16.cu",
+SOURCES = ["lsc_host.cu", "lsc_copy.cu", "lsc_gdn.cu", "lsc_rec128.cu", "lsc_chunked_tc.cu", "lsc_chunk_prep.cu", "lsc_noalloc.cu", "lsc_decode_f32.cu", "lsc_decode_bf16.cu",
            "lsc_prefill.cu", "lsc_kv.cu", "lsc_prefix_cache.cpp", "lsc_store.cpp"]
 HEADERS = [os.path.join(CSRC, h) for h in ("lsc_internal.h", "lsc_ptx.h", "lsc_tc.h", "lsc_chunk.h", "lsc_gdn_common.cuh", "lsc_decode.cuh")] + \
     [os.path.join(INCLUDE, h) for h in ("lsc.h", "lsc_prefix_cache.h", "lsc_kv.h", "lsc_store.h")]

@@ -178,8 +178,6 @@ struct RecurrentParams {
 int launch_recurrent(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
 // the token recurrence for head_k_dim 128 (lsc_rec128.cu)
 int launch_recurrent128(const RecurrentParams &p, int ssm_dtype, cudaStream_t stream);
-// the chunked evaluation (lsc_chunked.cu): head_k_dim 128, head_v_dim <= 128
-int launch_recurrent_chunked(const RecurrentParams &p, int dk, int ssm_dtype, cudaStream_t stream);
 // the chunked evaluation on the tensor cores: head_k_dim 128, head_v_dim <= 128.
 // launch_chunk_prep (lsc_chunk_prep.cu) writes the state-free records of
 // every chunk to p.ws; launch_recurrent_chunked_tc (lsc_chunked_tc.cu), on
