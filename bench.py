@@ -961,6 +961,8 @@ NCU_CASES = {
     "recurrent_chunked": ("c4", 16, "recurrent_chunked"),  # the same, 64-token chunks (preparation + state kernels)
     "prefill": ("c4", 32, "prefill"),        # prefill conv: 32 sequences of 64..2048 tokens, one layer
     "copy_prefix": ("c1", 4, "copy_prefix"), # K/V copy: 12 layers x 512 blocks of 64 KiB, 4 prefixes of 32 blocks
+    "gather": ("c2", 256, "gather"),         # c2 pool, 256 rows -> dense conv + ssm (281 MB per launch)
+    "scatter": ("c2", 256, "scatter"),       # the same, dense -> slots
 }
 
 
@@ -997,6 +999,18 @@ def run_ncu_case(args):
         def launch(i):
             rc, _ = L.lsc_restore(pool, ops, rows.nkv, rows.block_size, rows.initialized, hs, fwd, None)
             assert rc == L.LSC_OK
+    elif kind in ("gather", "scatter"):
+        idx = torch.from_numpy(rng.permutation(w.num_slots)[:n].astype(np.int32)).cuda()
+        v = views[w.gdn_layers[0]]
+        conv_d = torch.zeros((n, v.conv_bytes), dtype=torch.uint8, device="cuda")
+        ssm_d = torch.zeros((n, v.ssm_bytes), dtype=torch.uint8, device="cuda")
+
+        def launch(i):
+            l = w.gdn_layers[i % 2]
+            if kind == "gather":
+                assert L.lsc_gather(pool, l, idx, None, n, conv_d, ssm_d, fwd) == L.LSC_OK
+            else:
+                assert L.lsc_scatter(pool, l, idx, n, conv_d, ssm_d, fwd) == L.LSC_OK
     elif kind == "decode":
         idx = torch.from_numpy(rng.permutation(w.num_slots)[:n].astype(np.int32)).cuda()
         has = torch.ones(n, dtype=torch.uint8, device="cuda")
