@@ -323,9 +323,9 @@ def run_lsc(args):
     value = whole_job_rate(world, step_bytes * args.steps, elapsed) / 1e9
     rows_per_s = whole_job_rate(world, n * args.steps, elapsed)
 
-    roof_restore = {"bound": "hbm", "kernel": "restore_kernel", "achieved": round(restore_gbs, 1),
+    roof_restore = {"bound": "hbm", "kernel": "restore_bulk_kernel", "achieved": round(restore_gbs, 1),
                     "peak": hbm_peak, "unit": "GB/s", "frac": round(restore_gbs / hbm_peak, 4),
-                    "traffic": kernel_traffic("restore_kernel"), "bytes_per_launch": rb,
+                    "traffic": kernel_traffic("restore_bulk_kernel"), "bytes_per_launch": rb,
                     "launch_ms": round(t_restore * 1e3, 4), "peak_source": peak_src}
     roof_decode = {"bound": "hbm", "kernel": "decode_kernel<128,f32>", "achieved": round(decode_gbs, 1),
                    "peak": hbm_peak, "unit": "GB/s", "frac": round(decode_gbs / hbm_peak, 4),
@@ -494,6 +494,24 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
         "kind": "context (the pages' mechanism), not a target", "launch_ms": round(t_loop * 1e3, 3),
         "GB/s": round(nb / t_loop / 1e9, 1), "frac": round(nb / t_loop / 1e9 / hbm_peak, 4),
         "restore_kernel_ms": round(t_lsc * 1e3, 3), "speedup_of_restore_kernel": round(t_loop / t_lsc, 2)}
+    # the restore's two copy forms on the same pool and rows: 1-D TMA bulk
+    # copies through shared memory (the default here) and 16-byte vectors
+    # through registers (LSC_RESTORE_COPY=vector)
+    t_bulk = timed_on(prep, lsc_call, 10)
+    os.environ["LSC_RESTORE_COPY"] = "vector"
+    try:
+        t_vec = timed_on(prep, lsc_call, 10)
+    finally:
+        del os.environ["LSC_RESTORE_COPY"]
+    parts["restore_c1_copy_forms"] = {
+        "workload": f"c1: {len(hits)} hit rows x {len(w.gdn_layers)} GDN layers (9.89 GB), the serving step's restore",
+        "bulk": {"kernel": "restore_bulk_kernel (the default: cp.async.bulk global -> shared -> global, "
+                           "3 x 32 KiB stages, 2 CTAs per SM)",
+                 "launch_ms": round(t_bulk * 1e3, 4), "GB/s": round(nb / t_bulk / 1e9, 1),
+                 "frac": round(nb / t_bulk / 1e9 / hbm_peak, 4)},
+        "vector": {"kernel": "restore_kernel (16-byte vectors, LSC_RESTORE_COPY=vector)",
+                   "launch_ms": round(t_vec * 1e3, 4), "GB/s": round(nb / t_vec / 1e9, 1),
+                   "frac": round(nb / t_vec / 1e9 / hbm_peak, 4)}}
     L.lsc_pool_destroy(pool)
     del buf, tviews, hs
     torch.cuda.empty_cache()
@@ -580,9 +598,9 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     v = views[w.gdn_layers[0]]
     bytes_ = restore_bytes(v, r.n_hit, len(w.gdn_layers), r.n_hit + r.n_miss)
     parts["restore_c3"] = {"workload": "c3: 512 rows over 1024 slots, 205 hit / 154 miss / 153 no-op, hot source",
-                           "kernel": "restore_kernel", "launch_ms": round(t * 1e3, 4), "bytes_per_launch": bytes_,
+                           "kernel": "restore_bulk_kernel", "launch_ms": round(t * 1e3, 4), "bytes_per_launch": bytes_,
                            "GB/s": round(bytes_ / t / 1e9, 1), "frac": round(bytes_ / t / 1e9 / hbm_peak, 4),
-                           "rows_per_s": round(512 / t, 1), "traffic": kernel_traffic("restore_kernel c3")}
+                           "rows_per_s": round(512 / t, 1), "traffic": kernel_traffic("restore_bulk_kernel c3")}
     tr = parts["restore_c3"]["traffic"]
     parts["restore_c3"]["frac_basis"] = ("algorithmic: every hit's read counted, though the hot source's re-reads "
                                          "hit L2, so frac can exceed 1")
@@ -961,6 +979,7 @@ NCU_CASES = {
     "recurrent_chunked": ("c4", 16, "recurrent_chunked"),  # the same, 64-token chunks (preparation + state kernels)
     "prefill": ("c4", 32, "prefill"),        # prefill conv: 32 sequences of 64..2048 tokens, one layer
     "copy_prefix": ("c1", 4, "copy_prefix"), # K/V copy: 12 layers x 512 blocks of 64 KiB, 4 prefixes of 32 blocks
+    "restore_vector": ("c1", 64, "restore_vector"),  # the restore case as 16-byte vectors (LSC_RESTORE_COPY=vector)
     "gather": ("c2", 256, "gather"),         # c2 pool, 256 rows -> dense conv + ssm (281 MB per launch)
     "scatter": ("c2", 256, "scatter"),       # the same, dense -> slots
 }
@@ -991,7 +1010,9 @@ def run_ncu_case(args):
 
         def launch(i):
             assert L.lsc_copy_prefix(kpool, kops, fwd)[0] == L.LSC_OK
-    elif kind == "restore":
+    elif kind in ("restore", "restore_vector"):
+        if kind == "restore_vector":
+            os.environ["LSC_RESTORE_COPY"] = "vector"
         rows = W.restore_rows(name)
         ops = L.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
         hs = torch.from_numpy(rows.hs_prefill.copy()).cuda()

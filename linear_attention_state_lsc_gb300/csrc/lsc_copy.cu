@@ -7,12 +7,15 @@
 //   [VA] "非连续 KV Cache" §3 (page stride, padding skipped by stride), §4-§5
 //        (gather_ssm_states / scatter_ssm_states_)
 //
-// All three kernels are HBM-bound copies.  They move 16-byte vectors with
-// coalesced loads and streaming stores, never touch bytes outside the conv and
-// ssm views of a page, and run as persistent grids sized from the SM count.
+// All are HBM-bound copies.  They move whole 32 KiB chunks with 1-D TMA bulk
+// copies (the restore, when the ranges allow) or 16-byte vectors with
+// coalesced loads and streaming stores, never touch bytes outside the conv
+// and ssm views of a page, and run as persistent grids sized from the SM
+// count.
 #include <cuda_runtime.h>
 
 #include "lsc_internal.h"
+#include "lsc_ptx.h"
 
 namespace lsc {
 namespace {
@@ -95,6 +98,79 @@ __global__ void __launch_bounds__(kThreads) restore_kernel(const __grid_constant
     const int2 hs = p.hit[h];
     copy_span(layer + (int64_t)hs.x * p.page + off, layer + (int64_t)hs.y * p.page + off, len);
   }
+}
+
+// The same restore through shared memory with 1-D TMA bulk copies, the
+// default when every copied range is 16-byte aligned in offset and length:
+// one warp per CTA, two CTAs per SM, a ring of kBulkStages 32 KiB stages.  Its
+// thread 0 keeps kBulkStages - 1 loads in flight: unit k is stored from its
+// stage once its load has landed, and the load of unit k + kBulkStages - 1
+// reuses the stage of unit k - 1 once that unit's store has read it.  Needs
+// every copied range 16-byte aligned in offset and length (the host checks).
+constexpr int kBulkStages = 3;
+constexpr uint32_t kBulkChunk = 32 << 10;
+constexpr uint64_t kBulkWaitNs = 1000000000ull;
+
+__global__ void __launch_bounds__(32) restore_bulk_kernel(const __grid_constant__ RestorePlan p) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kBulkStages];
+  const int gthreads = gridDim.x * blockDim.x;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < p.n_hs; j += gthreads) {
+    const int32_t e = p.hs_ops[j];
+    p.hs[e >> 1] = (uint8_t)(e & 1);
+  }
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < kBulkStages; ++s) mbar_init(&full[s], 1);
+  fence_mbar_init();
+  const uint64_t pol = l2_evict_first_policy();
+  const int64_t per_hit = (int64_t)p.num_gdn * p.chunks_per_slot;
+  const int64_t total = (int64_t)p.n_hits * per_hit;
+  const int64_t n = total > blockIdx.x ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  // unit k of this CTA -> (dst, src, len)
+  auto unit = [&](int64_t k, uint8_t *&dst, const uint8_t *&src, uint32_t &len) {
+    const int64_t u = blockIdx.x + k * gridDim.x;
+    const int h = (int)(u / per_hit);
+    const int64_t rem = u - (int64_t)h * per_hit;
+    const int g = (int)(rem / p.chunks_per_slot);
+    int c = (int)(rem - (int64_t)g * p.chunks_per_slot);
+    const int s = c >= p.seg_chunks[0] ? 1 : 0;
+    if (s) c -= p.seg_chunks[0];
+    const int64_t off = p.seg_off[s] + (int64_t)c * p.chunk_bytes;
+    const int64_t left = p.seg_len[s] - (int64_t)c * p.chunk_bytes;
+    len = (uint32_t)(left < p.chunk_bytes ? left : p.chunk_bytes);
+    uint8_t *layer = p.base + (int64_t)g * p.region_bytes;
+    const int2 hs = p.hit[h];
+    dst = layer + (int64_t)hs.x * p.page + off;
+    src = layer + (int64_t)hs.y * p.page + off;
+  };
+  auto load = [&](int64_t k) {
+    uint8_t *dst;
+    const uint8_t *src;
+    uint32_t len;
+    unit(k, dst, src, len);
+    const int st = (int)(k % kBulkStages);
+    mbar_arrive_expect_tx(&full[st], len);
+    bulk_g2s(ring + (size_t)st * kBulkChunk, src, len, &full[st], pol);
+  };
+  for (int64_t k = 0; k < kBulkStages - 1 && k < n; ++k) load(k);
+  for (int64_t k = 0; k < n; ++k) {
+    const int st = (int)(k % kBulkStages);
+    if (!mbar_wait_bounded(&full[st], (uint32_t)((k / kBulkStages) & 1), kBulkWaitNs)) {
+      report(p.status, LSC_ERR_DEV_TIMEOUT);
+      break;
+    }
+    uint8_t *dst;
+    const uint8_t *src;
+    uint32_t len;
+    unit(k, dst, src, len);
+    bulk_s2g(dst, ring + (size_t)st * kBulkChunk, len, pol);
+    bulk_commit();
+    if (k + kBulkStages - 1 < n) {
+      bulk_wait_read_one();  // unit k - 1's store has read its stage
+      load(k + kBulkStages - 1);
+    }
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // every store complete before exit
 }
 
 // copy_prefix: unit = (op, attention layer, lane, chunk of the op's rows);
@@ -207,9 +283,19 @@ int grid_for(const void *kernel, int num_sms, int64_t units) {
 }  // namespace
 
 int restore_grid(int num_sms) { return grid_for((const void *)restore_kernel, num_sms, 1LL << 40); }
+int restore_bulk_grid(int num_sms) { return 2 * num_sms; }
+
+SmemLimit g_bulk_smem;
 
 cudaError_t launch_restore(const RestorePlan &plan, int grid, cudaStream_t stream) {
-  restore_kernel<<<grid, kThreads, 0, stream>>>(plan);
+  if (plan.bulk) {
+    const int smem = kBulkStages * (int)kBulkChunk;
+    cudaError_t e = g_bulk_smem.ensure((const void *)restore_bulk_kernel, smem);
+    if (e != cudaSuccess) return e;
+    restore_bulk_kernel<<<grid, 32, smem, stream>>>(plan);
+  } else {
+    restore_kernel<<<grid, kThreads, 0, stream>>>(plan);
+  }
   return cudaGetLastError();
 }
 

@@ -384,8 +384,16 @@ int lsc_restore(lsc_pool *p, const LinearStateCacheOp *ops, int32_t n_rows, cons
   for (int s = 0; s < 2; ++s) P.seg_chunks[s] = (int32_t)((P.seg_len[s] + P.chunk_bytes - 1) / P.chunk_bytes);
   P.chunks_per_slot = P.seg_chunks[0] + P.seg_chunks[1];
   P.num_gdn = g.num_gdn;
+  P.status = g.status;
+  // The copy goes through shared memory with 1-D TMA bulk copies when every
+  // copied range is 16-byte aligned in offset and length (the bulk copy's
+  // rule), else as 16-byte (or narrower) vectors through registers;
+  // LSC_RESTORE_COPY=vector selects the vector copy, for measurement.
+  const char *mode = getenv("LSC_RESTORE_COPY");
+  const bool vector_only = mode && strcmp(mode, "vector") == 0;
+  P.bulk = !vector_only && ((P.seg_off[0] | P.seg_len[0] | P.seg_off[1] | P.seg_len[1]) & 15) == 0;
 
-  const int grid = lsc::restore_grid(p->num_sms);
+  const int grid = P.bulk ? lsc::restore_bulk_grid(p->num_sms) : lsc::restore_grid(p->num_sms);
   int launches = 0;
   int32_t i = 0;
   while (i < n_rows) {

@@ -116,6 +116,8 @@ struct RestorePlan {
   int32_t num_gdn;
   int32_t n_hits;
   int32_t n_hs;
+  int32_t bulk;            // 1: copy through shared memory with 1-D TMA bulk copies
+  int32_t *status;         // device error word (bulk copies: a bounded wait gave up)
   int2 hit[kPlanMaxHits];  // (dst slot, src slot)
   int32_t hs_ops[kPlanMaxHs];  // (row << 1) | value
 };
@@ -123,6 +125,7 @@ static_assert(sizeof(RestorePlan) <= 32000, "restore plan exceeds the kernel par
 
 cudaError_t launch_restore(const RestorePlan &plan, int grid, cudaStream_t stream);
 int restore_grid(int num_sms);
+int restore_bulk_grid(int num_sms);
 
 // ---- gather / scatter ------------------------------------------------------
 struct AccessParams {
