@@ -26,9 +26,9 @@
 //   8-11        item: thread r reads row r of the Gram accumulator (k_r.k_j for
 //               r < 64, q_(r-64).k_j above), the group scans the head's gates,
 //               forms row r of A (packed in shared memory) or of B (straight
-//               to the record), inverts I + A (one column per thread of two of
-//               its warps, on different SM sub-partitions) and writes the rows
-//               of T' = T diag(b), then E, F and e_last.
+//               to the record), inverts I + A (by 2 x 2 blocks, all four
+//               warps) and writes the rows of T' = T diag(b), then E, F and
+//               e_last.
 // Products of gates are formed in token order (running products along a row,
 // product scans for E and F), as the token recurrence applies them: a zero
 // gate zeroes what follows, tiny ones fade to zero without a division.
@@ -53,9 +53,11 @@ constexpr int kStagedSeqs = 4096;    // cu_seqlens kept in shared memory up to t
 
 // A and T of one (chunk, v head) in shared memory, fp32, 64 x 64 each: A
 // transposed (At[j][t] = A_tj, so the 16 rows of a block column are
-// contiguous), T by rows (Tm[t][j]).  Only the entries below the diagonal of
-// A and on or below it of T are written or read.
+// contiguous; row stride kC), T by rows (Tm[t][j]; row stride kTs, which puts
+// consecutive rows 4 banks apart, so that 16-byte reads of 8 consecutive rows
+// at one column meet no bank twice).
 constexpr int kTileFloats = kC * kC;
+constexpr int kTs = kC + 4;
 
 // gate quantities of one (chunk, v head)
 struct Gates {
@@ -72,10 +74,11 @@ constexpr uint32_t OFF_KQLO = kKqBytes;
 constexpr uint32_t OFF_GRP = 2 * kKqBytes;
 constexpr uint32_t G_A = 0;
 constexpr uint32_t G_T = G_A + 4 * kTileFloats;
-constexpr uint32_t G_GATES = G_T + 4 * kTileFloats;
+constexpr uint32_t G_GATES = G_T + 4 * kC * kTs;
 constexpr uint32_t kGrpBytes = G_GATES + sizeof(Gates);
 constexpr uint32_t OFF_CU = OFF_GRP + kGroups * kGrpBytes;
-constexpr uint32_t kSmemBytes = OFF_CU + 4 * (kStagedSeqs + 4);
+constexpr uint32_t OFF_SEQOK = OFF_CU + 4 * (kStagedSeqs + 4);
+constexpr uint32_t kSmemBytes = OFF_SEQOK + kStagedSeqs;
 static_assert(G_T % 16 == 0 && G_GATES % 16 == 0 && kGrpBytes % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget (one CTA per SM)");
 
@@ -130,55 +133,147 @@ __device__ __forceinline__ float4 mask_above(float4 v, int col0, int row) {  // 
   return v;
 }
 
-// T = (I + A)^-1, one column per thread: thread j forms column j of T by
-// 16-row blocks, top to bottom, each as
-//   y = e_j - sum_(m < a) A[a][m] T[m][:, j]     (block products, 16-wide)
-//   y_i -= sum_(i' < i) A[a][a]_(i i') y_i'       (forward substitution)
-// with block a's rows of A read as broadcast 16-byte columns of At, and
-// writes y to rows 16 a .. 16 a + 15 of column j of Tm.  Columns are
-// independent, so no barrier is needed inside.  The blocks start at
-// a0 (a multiple of 16 not above j, the same for the whole warp): rows above
-// j's block come out zero.
-__device__ __forceinline__ void invert_unit_lower(const float *At, float *Tm, int j, int a0) {
-#pragma unroll 1
-  for (int a = a0; a < kC / 16; ++a) {
+// T = (I + A)^-1 by the solver group's 128 threads (r = thread index in the
+// group), by the 2 x 2 block rule for lower triangular matrices,
+//   [P 0; R Q]^-1 = [P^-1 0; -Q^-1 R P^-1  Q^-1],
+// applied to 16 x 16 blocks and then to 32 x 32 blocks:
+//   (1) the four 16 x 16 diagonal blocks by forward substitution (warp w takes
+//       block w, lane l column l mod 16) -- their entries above the diagonal,
+//       and the two 16 x 16 blocks above the diagonal inside each 32 x 32
+//       half, are written zero, so that the products below run over whole
+//       blocks;
+//   (2) inside each half: X = A_10 T_00, then T_10 = -T_11 X;
+//   (3) the 32 x 32 block: X = A_10 T_00, then T_10 = -T_11 X.
+// At holds A transposed (At[j][t] = A_tj, t > j; row stride kC), Tm holds T by
+// rows (row stride kTs).  The products X are kept in the 32 x 32 block of Tm
+// above the diagonal (rows 0..31, columns 32..63), which is never part of T.
+// Step (3) reads the lower half's T_11 by columns: (2) copies it, transposed,
+// into the top-left 32 x 32 block of At, whose A entries step (3) no longer
+// needs.  Each product is an outer-product loop over its inner index with
+// 8-byte shared loads (4 or 8 distinct words per warp: one wavefront each).
+__device__ __forceinline__ void invert_unit_lower(float *At, float *Tm, int r, int bar_id) {
+  const int w = r >> 5, lane = r & 31;
+  {
+    const int o = 16 * w, jj = lane & 15;
     float y[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = 16 * a + i == j ? 1.f : 0.f;
-#pragma unroll 1
-    for (int m = a0; m < a; ++m) {
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk) {
-        const int c = 16 * m + kk;
-        const float tv = Tm[c * kC + j];
-        const float4 *col = reinterpret_cast<const float4 *>(At + c * kC + 16 * a);
-        const float4 c0 = col[0], c1 = col[1], c2 = col[2], c3 = col[3];
-        y[0] = fmaf(-c0.x, tv, y[0]);
-        y[1] = fmaf(-c0.y, tv, y[1]);
-        y[2] = fmaf(-c0.z, tv, y[2]);
-        y[3] = fmaf(-c0.w, tv, y[3]);
-        y[4] = fmaf(-c1.x, tv, y[4]);
-        y[5] = fmaf(-c1.y, tv, y[5]);
-        y[6] = fmaf(-c1.z, tv, y[6]);
-        y[7] = fmaf(-c1.w, tv, y[7]);
-        y[8] = fmaf(-c2.x, tv, y[8]);
-        y[9] = fmaf(-c2.y, tv, y[9]);
-        y[10] = fmaf(-c2.z, tv, y[10]);
-        y[11] = fmaf(-c2.w, tv, y[11]);
-        y[12] = fmaf(-c3.x, tv, y[12]);
-        y[13] = fmaf(-c3.y, tv, y[13]);
-        y[14] = fmaf(-c3.z, tv, y[14]);
-        y[15] = fmaf(-c3.w, tv, y[15]);
-      }
-    }
+    for (int i = 0; i < 16; ++i) y[i] = i == jj ? 1.f : 0.f;
 #pragma unroll
     for (int ip = 0; ip < 15; ++ip) {
-      const float *col = At + (16 * a + ip) * kC + 16 * a;
+      const float *col = At + (o + ip) * kC + o;  // col[i] = A[o + i][o + ip]
 #pragma unroll
       for (int i = ip + 1; i < 16; ++i) y[i] = fmaf(-col[i], y[ip], y[i]);
     }
+    if (lane < 16) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Tm[(16 * a + i) * kC + j] = y[i];
+      for (int i = 0; i < 16; ++i) Tm[(o + i) * kTs + o + jj] = y[i];
+    } else {  // zero blocks: rows 32 q .. + 15, columns 32 q + 16 .. + 15
+      const int z = 16 * w + lane - 16, q = z >> 5, row = (z & 31) >> 1;
+      float4 *dst = reinterpret_cast<float4 *>(Tm + (32 * q + row) * kTs + 32 * q + 16 + 8 * (z & 1));
+      dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  group_sync(bar_id);
+  {  // (2) X of half p (rows o + 16 .., columns o ..) to rows 0..15, columns 32 + 16 p ..
+    const int p = r >> 6, i = (r & 63) >> 2, j4 = 4 * (r & 3), o = 32 * p;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float a = At[(o + m) * kC + o + 16 + i];
+      const float4 t = *reinterpret_cast<const float4 *>(Tm + (o + m) * kTs + o + j4);
+      x.x = fmaf(a, t.x, x.x);
+      x.y = fmaf(a, t.y, x.y);
+      x.z = fmaf(a, t.z, x.z);
+      x.w = fmaf(a, t.w, x.w);
+    }
+    *reinterpret_cast<float4 *>(Tm + i * kTs + 32 + 16 * p + j4) = x;
+  }
+  group_sync(bar_id);
+  {  // (2) T of half p: rows o + 16 + i0 .. + 3, column o + lane mod 16
+    const int p = w >> 1, o = 32 * p, j = lane & 15, i0 = 8 * (w & 1) + 4 * (lane >> 4);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m4 = 0; m4 < 16; m4 += 4) {
+      float xs[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) xs[u] = Tm[(m4 + u) * kTs + 32 + 16 * p + j];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 s = *reinterpret_cast<const float4 *>(Tm + (o + 16 + i0 + e) * kTs + o + 16 + m4);
+        acc[e] = fmaf(s.x, xs[0], acc[e]);
+        acc[e] = fmaf(s.y, xs[1], acc[e]);
+        acc[e] = fmaf(s.z, xs[2], acc[e]);
+        acc[e] = fmaf(s.w, xs[3], acc[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      Tm[(o + 16 + i0 + e) * kTs + o + j] = -acc[e];
+      // the lower half's T_11 by columns: T[48 + i][32 + j] to At[j][16 + i]
+      if (p == 1) At[j * kC + 16 + i0 + e] = -acc[e];
+    }
+    // ... and its two diagonal blocks: T[32 + 16 b + i][32 + 16 b + m] to At[16 b + m][16 b + i]
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = 4 * r + u, b = e >> 8, i = (e >> 4) & 15, m = e & 15;
+      At[(16 * b + m) * kC + 16 * b + i] = Tm[(32 + 16 * b + i) * kTs + 32 + 16 * b + m];
+    }
+  }
+  group_sync(bar_id);
+  // (3): thread rows ri, ri + 1 of the 32 x 32 block, columns 2 jg, + 1 and
+  // 16 + 2 jg, + 1
+  const int ri = 8 * w + 2 * (lane >> 3), jc = 2 * (lane & 7);
+  {  // X = A_10 T_00 to rows 0..31, columns 32..63; T_00 is zero in columns
+     // 16..31 of rows 0..15
+    float x[2][4] = {};
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      const float2 a = *reinterpret_cast<const float2 *>(At + m * kC + 32 + ri);
+      const float2 t0 = *reinterpret_cast<const float2 *>(Tm + m * kTs + jc);
+      x[0][0] = fmaf(a.x, t0.x, x[0][0]);
+      x[0][1] = fmaf(a.x, t0.y, x[0][1]);
+      x[1][0] = fmaf(a.y, t0.x, x[1][0]);
+      x[1][1] = fmaf(a.y, t0.y, x[1][1]);
+      if (m >= 16) {
+        const float2 t1 = *reinterpret_cast<const float2 *>(Tm + m * kTs + 16 + jc);
+        x[0][2] = fmaf(a.x, t1.x, x[0][2]);
+        x[0][3] = fmaf(a.x, t1.y, x[0][3]);
+        x[1][2] = fmaf(a.y, t1.x, x[1][2]);
+        x[1][3] = fmaf(a.y, t1.y, x[1][3]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      *reinterpret_cast<float2 *>(Tm + (ri + e) * kTs + 32 + jc) = make_float2(x[e][0], x[e][1]);
+      *reinterpret_cast<float2 *>(Tm + (ri + e) * kTs + 48 + jc) = make_float2(x[e][2], x[e][3]);
+    }
+  }
+  group_sync(bar_id);
+  {  // T_10 = -T_11 X to rows 32.., columns 0..31; T_11 (read by columns from
+     // At) is zero right of its diagonal, so rows 0..15 of the block stop at
+     // inner index 15
+    float x[2][4] = {};
+    const int mend = w < 2 ? 16 : 32;
+#pragma unroll 4
+    for (int m = 0; m < mend; ++m) {
+      const float2 a = *reinterpret_cast<const float2 *>(At + m * kC + ri);
+      const float2 t0 = *reinterpret_cast<const float2 *>(Tm + m * kTs + 32 + jc);
+      const float2 t1 = *reinterpret_cast<const float2 *>(Tm + m * kTs + 48 + jc);
+      x[0][0] = fmaf(a.x, t0.x, x[0][0]);
+      x[0][1] = fmaf(a.x, t0.y, x[0][1]);
+      x[0][2] = fmaf(a.x, t1.x, x[0][2]);
+      x[0][3] = fmaf(a.x, t1.y, x[0][3]);
+      x[1][0] = fmaf(a.y, t0.x, x[1][0]);
+      x[1][1] = fmaf(a.y, t0.y, x[1][1]);
+      x[1][2] = fmaf(a.y, t1.x, x[1][2]);
+      x[1][3] = fmaf(a.y, t1.y, x[1][3]);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      *reinterpret_cast<float2 *>(Tm + (32 + ri + e) * kTs + jc) = make_float2(-x[e][0], -x[e][1]);
+      *reinterpret_cast<float2 *>(Tm + (32 + ri + e) * kTs + 16 + jc) = make_float2(-x[e][2], -x[e][3]);
+    }
   }
 }
 
@@ -190,8 +285,8 @@ __device__ __forceinline__ void invert_unit_lower(const float *At, float *Tm, in
 struct Located {
   int i, t0, nt;
 };
-__device__ __forceinline__ bool locate(const int32_t *cu, int n_seq, int total, int64_t s, const int32_t *idx,
-                                       int num_slots, Located &L) {
+__device__ __forceinline__ bool locate(const int32_t *cu, const uint8_t *seq_ok, int n_seq, int total, int64_t s,
+                                       const int32_t *idx, int num_slots, Located &L) {
   if (n_seq <= 0 || slot_base(cu[0], 0) > s) return false;
   int lo = 0, hi = n_seq - 1;
   while (lo < hi) {
@@ -203,8 +298,12 @@ __device__ __forceinline__ bool locate(const int32_t *cu, int n_seq, int total, 
   if (t0 < 0 || t1 < t0 || t1 > total) return false;
   const int64_t c = s - slot_base(t0, lo);
   if (c * kC >= (int64_t)(t1 - t0)) return false;
-  const int32_t slot = idx[lo];
-  if (slot < 0 || slot >= num_slots) return false;
+  if (seq_ok) {
+    if (!seq_ok[lo]) return false;
+  } else {
+    const int32_t slot = idx[lo];
+    if (slot < 0 || slot >= num_slots) return false;
+  }
   L.i = lo;
   L.t0 = t0 + (int)c * kC;
   L.nt = min(kC, t1 - L.t0);
@@ -278,11 +377,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // cu_seqlens and whether each sequence's slot is in range, staged once
   const int32_t *cu = p.cu;
+  const uint8_t *seq_ok = nullptr;
   if (p.n_seq <= kStagedSeqs) {
     int32_t *cu_s = reinterpret_cast<int32_t *>(sm + OFF_CU);
+    uint8_t *ok_s = sm + OFF_SEQOK;
     for (int e = tid; e <= p.n_seq; e += kThreads) cu_s[e] = __ldg(p.cu + e);
+    for (int e = tid; e < p.n_seq; e += kThreads) {
+      const int32_t slot = __ldg(p.idx + e);
+      ok_s[e] = slot >= 0 && slot < p.num_slots;
+    }
     cu = cu_s;
+    seq_ok = ok_s;
   }
   if (tid == 0) {
     mbar_init(&bars.kq, kProdThreads);
@@ -317,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
       const int64_t s = it / p.Hk;
       const int g = (int)(it % p.Hk);
       Located L;
-      if (!locate(cu, p.n_seq, p.total_tokens, s, p.idx, p.num_slots, L)) continue;
+      if (!locate(cu, seq_ok, p.n_seq, p.total_tokens, s, p.idx, p.num_slots, L)) continue;
       // this thread's 4 x 4 blocks: tokens 4a..4a+3, channels 4b..4b+3 with
       // a = al + 8 ah, b = bl + 4 pw + 16 bh
       float4 kr[2][2][4], qr[2][2][4];
@@ -389,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
       const int64_t s = it / p.Hk;
       const int g = (int)(it % p.Hk);
       Located L;
-      if (!locate(cu, p.n_seq, p.total_tokens, s, p.idx, p.num_slots, L)) continue;
+      if (!locate(cu, seq_ok, p.n_seq, p.total_tokens, s, p.idx, p.num_slots, L)) continue;
       // the first head's gates in flight while the Gram product is awaited
       GateIn gin;
       if (r < 32 && grp < p.group) gin = load_gates(p, g * p.group + grp, L, lane);
@@ -432,14 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
           }
         }
         group_sync(bar_id);
-        // two of the group's warps invert, one per SM sub-partition pair
-        // (group 0: its warps 0 and 2, group 1: its warps 1 and 3)
-        if (((warp ^ grp) & 1) == 0) invert_unit_lower(Ap, Tp, 32 * ((warp & 3) >> 1) + lane, 2 * ((warp & 3) >> 1));
+        invert_unit_lower(Ap, Tp, r, bar_id);
         group_sync(bar_id);
         {
           // T' = T diag(b): row r / 2, columns 32 (r % 2) .. + 31
           const int tt = r >> 1, j0 = 32 * (r & 1);
-          const float *trow = Tp + tt * kC;
+          const float *trow = Tp + tt * kTs;
           float *dst = rec + kRecT;
 #pragma unroll 1
           for (int j4 = j0; j4 < j0 + 32; j4 += 4) {
