@@ -28,10 +28,11 @@
 // so every round keeps the lower half and sends the upper one, with no
 // lane-dependent selects.
 //
-// Tokens go in pairs (a, b): one pass over the state forms both tokens' dot
-// products against the state before the pair, and b's are corrected with the
-// pair's Gram scalars (true state S = gamma Shat; gamma_a' = alpha_a gamma,
-// gamma_b' = alpha_b gamma_a'):
+// Tokens go in pairs (a, b): both tokens' dot products are formed against the
+// state before the pair (one token after the other, so that the 64 state
+// registers, one token's inputs and its 16 products fit in 128 registers with
+// nothing spilled), and b's are corrected with the pair's Gram scalars (true
+// state S = gamma Shat; gamma_a' = alpha_a gamma, gamma_b' = alpha_b gamma_a'):
 //   d_a = beta_a (v_a - gamma_a' Shat.k_a),  o_a = gamma_a' Shat.q_a + d_a (k_a.q_a)
 //   u_b = gamma_a' Shat.k_b + d_a (k_a.k_b), d_b = beta_b (v_b - alpha_b u_b)
 //   o_b = gamma_b' Shat.q_b + alpha_b d_a (k_a.q_b) + d_b (k_b.q_b)
@@ -129,7 +130,10 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent128_kernel(const __grid_
   const bool odd = (lc & 1) != 0;
 
   uint64_t S[8][4];  // [slot][pair]: columns 4lc..4lc+3, then 64+4lc..64+4lc+3
-  TS *Sg = reinterpret_cast<TS *>(p.layer + (int64_t)slot * p.page + p.ssm_off) + (int64_t)h * dv * kDK;
+  auto state_ptr = [&]() {  // formed where used, so that no register holds it across the token loop
+    return reinterpret_cast<TS *>(p.layer + (int64_t)slot * p.page + p.ssm_off) + (int64_t)h * dv * kDK;
+  };
+  const TS *Sg = state_ptr();
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const int row = row0 + (r ^ rb);
@@ -265,29 +269,34 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent128_kernel(const __grid_
       xa[0] = a0.x; xa[1] = a0.y; xa[2] = a1.x; xa[3] = a1.y;
       xb[0] = b0.x; xb[1] = b0.y; xb[2] = b1.x; xb[3] = b1.y;
     };
-    for (int pp = 0; pp < np; ++pp) {
-      const int ta = 2 * pp, tb2 = ta + 1;
-      uint64_t xaa[4], xba[4], xab[4], xbb[4];  // tokens a and b: slot products xa / xb
-      load_x(ta, xaa, xba);
-      load_x(tb2, xab, xbb);
-      // both tokens' dot products with the state before the pair
-      float va[16], vb[16];  // local index 2 slot + {0: xa, 1: xb}
+    // both tokens' dot products with the state before the pair, one token at
+    // a time (the state's 64 registers leave no room for both tokens' inputs
+    // and products at once); returns this lane's reduced value and the
+    // token's k columns
+    auto dots = [&](int tt, uint64_t *kc) {
+      uint64_t xa[4], xb[4];
+      load_x(tt, xa, xb);
+      float v[16];  // local index 2 slot + {0: xa, 1: xb}
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        va[2 * r] = dot8(S[r], xaa);
-        va[2 * r + 1] = dot8(S[r], xba);
-        vb[2 * r] = dot8(S[r], xab);
-        vb[2 * r + 1] = dot8(S[r], xbb);
+        v[2 * r] = dot8(S[r], xa);
+        v[2 * r + 1] = dot8(S[r], xb);
       }
-      float a8[8], a4[4], a2[2], a1[1], b8[8], b4[4], b2[2], b1[1];
-      reduce_half<16>(va, a8, 8);
-      reduce_half<16>(vb, b8, 8);
-      reduce_half<8>(a8, a4, 4);
-      reduce_half<8>(b8, b4, 4);
-      reduce_half<4>(a4, a2, 2);
-      reduce_half<4>(b4, b2, 2);
-      reduce_half<2>(a2, a1, 1);
-      reduce_half<2>(b2, b1, 1);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) kc[q] = odd ? xb[q] : xa[q];
+      float v8[8], v4[4], v2[2], v1[1];
+      reduce_half<16>(v, v8, 8);
+      reduce_half<8>(v8, v4, 4);
+      reduce_half<4>(v4, v2, 2);
+      reduce_half<2>(v2, v1, 1);
+      return v1[0];
+    };
+    for (int pp = 0; pp < np; ++pp) {
+      const int ta = 2 * pp, tb2 = ta + 1;
+      uint64_t ka[4], kb[4];  // k of tokens a and b
+      float a1[1], b1[1];
+      a1[0] = dots(ta, ka);
+      b1[0] = dots(tb2, kb);
       // even lanes: u-hat of my_row for a and b (b against the old state);
       // odd lanes: the w-hats
       const float4 c0 = sp[2 * pp], c1 = sp[2 * pp + 1];
@@ -313,12 +322,6 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent128_kernel(const __grid_
           for (int q = 0; q < 4; ++q) S[r][q] = f2_mul(S[r][q], g2);
       }
       const float ea = da * c1.y, eb = db * c1.z;
-      uint64_t ka[4], kb[4];  // k of tokens a and b
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        ka[q] = odd ? xba[q] : xaa[q];
-        kb[q] = odd ? xbb[q] : xab[q];
-      }
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         const int src = gbase + 2 * (r ^ rb);  // the lane holding slot r's row
@@ -338,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent128_kernel(const __grid_
   gam = s_gam;
 
   // final state = gamma * Shat
+  TS *Sd = state_ptr();
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const int row = row0 + (r ^ rb);
@@ -351,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent128_kernel(const __grid_
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float v = gam * f[e];
-        if constexpr (sizeof(TS) == 4) ((float *)Sg)[(int64_t)row * kDK + c0 + e] = v;
-        else ((uint16_t *)Sg)[(int64_t)row * kDK + c0 + e] = float_to_bf16_bits(v);
+        if constexpr (sizeof(TS) == 4) ((float *)Sd)[(int64_t)row * kDK + c0 + e] = v;
+        else ((uint16_t *)Sd)[(int64_t)row * kDK + c0 + e] = float_to_bf16_bits(v);
       }
     }
   }
