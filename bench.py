@@ -29,6 +29,7 @@ sys.path.insert(0, ROOT)
 METRIC = "restore & gather→GDN-step→scatter HBM GB/s (fraction of GB300 peak); rows/s"
 UNIT = "GB/s"
 FALLBACK_HBM = 6800.0
+DECODE_FLAGS = 1  # LSC_DECODE_EARLY_STATE
 
 
 def parse():
@@ -257,7 +258,11 @@ def run_lsc(args):
     A = torch.stack([torch.from_numpy(a) for a, _ in abs_]).cuda()               # [36, n, Hv]
     B = torch.stack([torch.from_numpy(b) for _, b in abs_]).cuda()
     OUT = torch.empty((n_gdn, n, w.num_v_heads, w.head_v_dim), device="cuda")
-    dargs = [L.decode_args(n, w.num_k_heads, idx, hs, X[g], CW[g], A[g], B[g], OUT[g]) for g in range(n_gdn)]
+    # each decode launch may stream its layer's first state tiles while the
+    # previous layer's launch finishes: no launch of the chain writes another
+    # layer's state, and the first one follows the restore's event
+    dargs = [L.decode_args(n, w.num_k_heads, idx, hs, X[g], CW[g], A[g], B[g], OUT[g], DECODE_FLAGS)
+             for g in range(n_gdn)]
 
     prep = torch.cuda.Stream()
     fwd = torch.cuda.current_stream()
@@ -344,6 +349,7 @@ def run_lsc(args):
         "config": {"workload": "c1-serving-step", "layers": "36 GDN + 12 attention", "num_slots": w.num_slots,
                    "rows": n, "restore": "64 rows all hits x 36 GDN layers",
                    "decode": "1 token x 64 restored rows x 36 GDN layers",
+                   "decode_flags": "LSC_DECODE_EARLY_STATE" if DECODE_FLAGS else "0",
                    "conv": "[8192,3] bf16", "ssm": "[32,128,128] f32", "page_bytes": w.page_bytes,
                    "l2": "inputs larger than L2 (9.9 GB restore, 9.9 GB decode per step)",
                    "parallelism": f"replicas x{world}"},
@@ -380,7 +386,8 @@ def e2e_serving(args, L, torch, pool, w, rows, ops, n, n_gdn, X, CW, A, B, step_
     dhs = torch.empty(n, dtype=torch.uint8, device="cuda")
     didx = torch.empty(n, dtype=torch.int32, device="cuda")
     dout = torch.empty((n_gdn, n, w.num_v_heads, w.head_v_dim), device="cuda")
-    dargs = [L.decode_args(n, w.num_k_heads, didx, dhs, dx[g], CW[g], da[g], db[g], dout[g]) for g in range(n_gdn)]
+    dargs = [L.decode_args(n, w.num_k_heads, didx, dhs, dx[g], CW[g], da[g], db[g], dout[g], DECODE_FLAGS)
+             for g in range(n_gdn)]
     prep = torch.cuda.Stream()
     d2h_stream = torch.cuda.Stream()
     fwd = torch.cuda.current_stream()
@@ -516,6 +523,46 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     del buf, tviews, hs
     torch.cuda.empty_cache()
 
+    # the serving step's decode chain (64 restored rows x 36 GDN layers, fp32
+    # state) with and without the early state start, on the same pool and rows
+    w = W.get("c1")
+    rows = W.restore_rows("c1", seed=0)
+    buf, pool, views = make_pool(L, W, w, seed=0)
+    n = len(rows.live)
+    idx = torch.from_numpy(rows.live.astype(np.int32)).cuda()
+    has = torch.ones(n, dtype=torch.uint8, device="cuda")
+    xs, abs_ = serving_step_inputs(W, w, rows)
+    bf = torch.bfloat16
+    X = torch.stack([torch.from_numpy(x) for x, _ in xs]).to(bf).cuda()
+    CW = torch.stack([torch.from_numpy(cw) for _, cw in xs]).to(bf).cuda()
+    A = torch.stack([torch.from_numpy(a) for a, _ in abs_]).cuda()
+    B = torch.stack([torch.from_numpy(b) for _, b in abs_]).cuda()
+    OUT = torch.empty((len(w.gdn_layers), n, w.num_v_heads, w.head_v_dim), device="cuda")
+    v = views[w.gdn_layers[0]]
+    bytes_ = decode_bytes(v, w, n)
+    chain = {}
+    for flags, key in ((0, "plain"), (1, "early_state")):
+        dargs = [L.decode_args(n, w.num_k_heads, idx, has, X[g], CW[g], A[g], B[g], OUT[g], flags)
+                 for g in range(len(w.gdn_layers))]
+
+        def dec_chain():
+            for g, l in enumerate(w.gdn_layers):
+                assert L.lsc_gdn_decode(pool, l, dargs[g], fwd) == L.LSC_OK
+
+        t = timed(dec_chain, 20) / len(w.gdn_layers)
+        chain[key] = {"launch_ms": round(t * 1e3, 4), "GB/s": round(bytes_ / t / 1e9, 1),
+                      "frac": round(bytes_ / t / 1e9 / hbm_peak, 4)}
+    parts["decode_c1_chain"] = {"workload": "c1 pool: 64 rows x 36 GDN layers, ssm f32, one launch per layer, "
+                                            "layers back to back (the serving step's decode without its restore)",
+                                "kernel": "decode_kernel<128,f32>", "bytes_per_launch": bytes_,
+                                "plain": chain["plain"],
+                                "early_state": chain["early_state"] | {
+                                    "flags": "LSC_DECODE_EARLY_STATE: rows and first state tiles read before the "
+                                             "wait for the previous layer's launch"}}
+    L.lsc_pool_destroy(pool)
+    del buf, X, CW, A, B, OUT
+    torch.cuda.empty_cache()
+
     # decode step at 256 rows, bf16 state, one launch per layer over 36 layers
     w = W.get("c2")
     buf, pool, views = make_pool(L, W, w, seed=0)
@@ -528,7 +575,7 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
     CW = torch.from_numpy(cw).to(torch.bfloat16).cuda()
     A, B = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
     out = torch.empty((n, w.num_v_heads, w.head_v_dim), device="cuda")
-    da = L.decode_args(n, w.num_k_heads, idx, has, X, CW, A, B, out)
+    da = L.decode_args(n, w.num_k_heads, idx, has, X, CW, A, B, out, DECODE_FLAGS)
 
     def dec_all():
         for l in w.gdn_layers:
@@ -1039,7 +1086,7 @@ def run_ncu_case(args):
         t = [torch.from_numpy(x).to(torch.bfloat16).cuda(), torch.from_numpy(cw).to(torch.bfloat16).cuda(),
              torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()]
         out = torch.empty((n, w.num_v_heads, w.head_v_dim), device="cuda")
-        da = L.decode_args(n, w.num_k_heads, idx, has, *t, out)
+        da = L.decode_args(n, w.num_k_heads, idx, has, *t, out, DECODE_FLAGS)
 
         def launch(i):
             assert L.lsc_gdn_decode(pool, w.gdn_layers[i % 2], da, fwd) == L.LSC_OK

@@ -248,7 +248,20 @@ typedef struct {
   const float *alpha;       /* device [n, Hv]: gate, already activated */
   const float *beta;        /* device [n, Hv]: write strength, already activated */
   float *out;               /* device [n, Hv, dv] */
+  uint32_t flags;           /* 0 or LSC_DECODE_EARLY_STATE; other bits: INVALID_ARG */
 } lsc_gdn_decode_args;
+
+/* Flag of lsc_gdn_decode_args.  The decode kernel is launched with programmatic
+ * stream serialisation: its CTAs may start on SMs that the previous kernel of
+ * the stream has left, and wait for that kernel to complete before reading any
+ * input.  With this flag they read idx, has_init and the first state tiles of
+ * the layer's rows before that wait, so the state stream of this layer overlaps
+ * the end of the previous kernel.  Set it only when the kernel enqueued just
+ * before the call on the stream (with no event wait or copy between them)
+ * writes none of idx, has_init and the layer's ssm state of those rows -- for
+ * example the decode of another layer.  All other inputs are read after the
+ * wait, as without the flag. */
+#define LSC_DECODE_EARLY_STATE 1u
 
 /*
  * One decode token for n rows of GDN layer `layer`, in one fused kernel that

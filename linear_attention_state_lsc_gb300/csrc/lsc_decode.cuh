@@ -180,55 +180,72 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
     }
     fence_mbar_init();
   }
+
+  // rows of this CTA's items: slot (or -1) and warm, loaded once
+  auto load_rows = [&]() {
+    for (int k = tid; k < my_items; k += kDecodeBlock) {
+      const int i = (b + k * grid) / Hk;
+      const int32_t slot = p.idx[i];
+      const bool ok = slot >= 0 && slot < p.num_slots;
+      if (slot >= p.num_slots) report(p.status, LSC_ERR_OUT_OF_RANGE);
+      info_slot[k] = ok ? slot : -1;
+      info_warm[k] = ok && (p.has_init == nullptr || p.has_init[i] != 0);
+    }
+    __syncthreads();
+  };
+
+  // producer state, shared by the early start below and the producer loop
+  int issued_tiles = 0;
+  auto tile_addr = [&](int t, uint32_t &bytes, bool &live, bool &load) -> uint8_t * {
+    const int k = t / D.TPG, rem = t % D.TPG, hl = rem / D.TPH, rb = rem % D.TPH;
+    const int g = (b + k * grid) % Hk;
+    const int rows = min(D.TR, dv - rb * D.TR);
+    bytes = (uint32_t)rows * DK * Sh::ES;
+    const int32_t slot = info_slot[k];
+    live = slot >= 0;
+    load = live && info_warm[k] != 0;
+    if (!live) return nullptr;
+    return p.layer + (int64_t)slot * p.page + p.ssm_off +
+           (((int64_t)(g * G + hl) * dv + (int64_t)rb * D.TR) * DK) * Sh::ES;
+  };
+  // the state is read and written once per launch: evict it from L2 first
+  // (3 % faster on the fp32 serving-step decode than the default policy)
+  auto issue_tile = [&](int t, uint64_t l2_once) {
+    if (t >= my_tiles) return;
+    uint32_t bytes;
+    bool live, load;
+    const uint8_t *src = tile_addr(t, bytes, live, load);
+    mbar_arrive_expect_tx(&full[t % NS], load ? bytes : 0u);
+    if (load) bulk_g2s(smem + (int64_t)(t % NS) * D.stage_stride, src, bytes, &full[t % NS], l2_once);
+    issued_tiles = t + 1;
+  };
+
+  // Early start (the caller vouches that the previous kernel of the stream
+  // writes neither idx, has_init nor this layer's ssm state): read the rows and
+  // fill the ring with the first state tiles while that kernel finishes; every
+  // other input is read after griddep_wait() as usual.
+  const bool early = p.early_state != 0;
+  if (early) {
+    load_rows();
+    if (tid == kProducer)
+      for (int t = 0; t < NS; ++t) issue_tile(t, l2_evict_first_policy());
+  }
   // the previous kernel of the stream may still be running until here
   griddep_wait();
   if (tid == 0) griddep_launch_dependents();
-
-  // rows of this CTA's items: slot (or -1) and warm, loaded once
-  for (int k = tid; k < my_items; k += kDecodeBlock) {
-    const int i = (b + k * grid) / Hk;
-    const int32_t slot = p.idx[i];
-    const bool ok = slot >= 0 && slot < p.num_slots;
-    if (slot >= p.num_slots) report(p.status, LSC_ERR_OUT_OF_RANGE);
-    info_slot[k] = ok ? slot : -1;
-    info_warm[k] = ok && (p.has_init == nullptr || p.has_init[i] != 0);
-  }
-  __syncthreads();
+  if (!early) load_rows();
 
   if (tid >= kProducer) {
     // ------------------------------------------------------------ producer
     if (tid != kProducer) return;
-    int issued_tiles = 0;
-    auto tile_addr = [&](int t, uint32_t &bytes, bool &live, bool &load) -> uint8_t * {
-      const int k = t / D.TPG, rem = t % D.TPG, hl = rem / D.TPH, rb = rem % D.TPH;
-      const int g = (b + k * grid) % Hk;
-      const int rows = min(D.TR, dv - rb * D.TR);
-      bytes = (uint32_t)rows * DK * Sh::ES;
-      const int32_t slot = info_slot[k];
-      live = slot >= 0;
-      load = live && info_warm[k] != 0;
-      if (!live) return nullptr;
-      return p.layer + (int64_t)slot * p.page + p.ssm_off +
-             (((int64_t)(g * G + hl) * dv + (int64_t)rb * D.TR) * DK) * Sh::ES;
-    };
-    // the state is read and written once per launch: evict it from L2 first
-    // (3 % faster on the fp32 serving-step decode than the default policy)
     const uint64_t l2_once = l2_evict_first_policy();
-    auto issue_tile = [&](int t) {
-      if (t >= my_tiles) return;
-      uint32_t bytes;
-      bool live, load;
-      const uint8_t *src = tile_addr(t, bytes, live, load);
-      mbar_arrive_expect_tx(&full[t % NS], load ? bytes : 0u);
-      if (load) bulk_g2s(smem + (int64_t)(t % NS) * D.stage_stride, src, bytes, &full[t % NS], l2_once);
-      issued_tiles = t + 1;
-    };
     auto drain = [&](int t_from) {
       report(p.status, LSC_ERR_DEV_TIMEOUT);
       for (int tt = t_from; tt < issued_tiles; ++tt) mbar_wait_bounded(&full[tt % NS], (tt / NS) & 1, p.drain_limit_ns);
       bulk_wait_read_all();
     };
-    for (int t = 0; t < NS; ++t) issue_tile(t);
+    if (!early)
+      for (int t = 0; t < NS; ++t) issue_tile(t, l2_once);
     for (int t = 0; t < my_tiles; ++t) {
       if (!mbar_wait_bounded(&empty[t % NS], (t / NS) & 1, p.wait_limit_ns)) {
         drain(t);
@@ -242,7 +259,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
       // refill the previous tile's stage once its store has left shared memory
       if (t >= 1 && t - 1 + NS < my_tiles) {
         bulk_wait_read_one();
-        issue_tile(t - 1 + NS);
+        issue_tile(t - 1 + NS, l2_once);
       }
     }
     bulk_wait_read_all();

@@ -492,6 +492,7 @@ int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, voi
     return LSC_ERR_INVALID_ARG;
   if (a->n > 0 && (!a->idx || !a->x || !a->conv_weight || !a->alpha || !a->beta || !a->out))
     return LSC_ERR_INVALID_ARG;
+  if ((a->flags & ~LSC_DECODE_EARLY_STATE) != 0) return LSC_ERR_INVALID_ARG;
   if (g.conv_dtype == LSC_F16 || g.ssm_dtype == LSC_F16) return LSC_ERR_UNSUPPORTED;
   if (g.conv_width > 8 || g.Hv / Hk > 8 || a->n > 65535) return LSC_ERR_UNSUPPORTED;
   if (!all_aligned({a->x, a->conv_weight}, (uintptr_t)esize(g.conv_dtype)) ||
@@ -533,6 +534,7 @@ int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, voi
   d.wait_limit_ns = fault("timeout0") ? 0 : kWaitLimitNs;
   d.drain_limit_ns = kWaitLimitNs;
   d.num_sms = p->num_sms;
+  d.early_state = (a->flags & LSC_DECODE_EARLY_STATE) != 0;
   return lsc::launch_decode(d, g.dk, g.ssm_dtype, (cudaStream_t)stream);
 }
 

@@ -160,6 +160,7 @@ struct DecodeParams {
   uint64_t drain_limit_ns;  // bound of the wait for in-flight copies after a timeout
   int32_t num_sms;
   int32_t stages;           // set by the launcher: shared-memory ring depth
+  int32_t early_state;      // LSC_DECODE_EARLY_STATE: rows and first state tiles read before griddep_wait()
 };
 // returns LSC_OK, LSC_ERR_UNSUPPORTED or LSC_ERR_CUDA
 int launch_decode(const DecodeParams &p, int dk, int ssm_dtype, cudaStream_t stream);

@@ -41,6 +41,7 @@ LSC_SLOT_FREE, LSC_SLOT_LIVE, LSC_SLOT_CHECKPOINT, LSC_SLOT_RESERVED = 0, 1, 2, 
 
 LSC_LAYER_ATTENTION, LSC_LAYER_GDN = 0, 1
 LSC_RECURRENT_AUTO, LSC_RECURRENT_TOKEN, LSC_RECURRENT_CHUNKED = 0, 1, 2
+LSC_DECODE_EARLY_STATE = 1
 LSC_F32, LSC_BF16, LSC_F16 = 0, 1, 2
 
 
@@ -89,7 +90,7 @@ class lsc_restore_report(C.Structure):
 class lsc_gdn_decode_args(C.Structure):
     _fields_ = [("n", C.c_int32), ("num_k_heads", C.c_int32), ("idx", C.c_void_p),
                 ("has_init", C.c_void_p), ("x", C.c_void_p), ("conv_weight", C.c_void_p),
-                ("alpha", C.c_void_p), ("beta", C.c_void_p), ("out", C.c_void_p)]
+                ("alpha", C.c_void_p), ("beta", C.c_void_p), ("out", C.c_void_p), ("flags", C.c_uint32)]
 
 
 class lsc_gdn_recurrent_args(C.Structure):
@@ -322,9 +323,9 @@ def lsc_scatter(pool, layer, idx, n, conv_dense, ssm_dense, stream=None):
                               _stream(stream))
 
 
-def decode_args(n, num_k_heads, idx, has_init, x, conv_weight, alpha, beta, out):
+def decode_args(n, num_k_heads, idx, has_init, x, conv_weight, alpha, beta, out, flags=0):
     return lsc_gdn_decode_args(n, num_k_heads, ptr(idx), ptr(has_init), ptr(x), ptr(conv_weight),
-                               ptr(alpha), ptr(beta), ptr(out))
+                               ptr(alpha), ptr(beta), ptr(out), flags)
 
 
 def lsc_gdn_decode(pool, layer, args, stream=None):

@@ -324,3 +324,36 @@ def test_algorithmic_bytes_of_the_bench(lsc):
     assert bench.decode_bytes(v1, w1, 64) == 64 * 4_325_637 + 65_536               # 276.9 MB per serving-step decode
     w2, v2 = views["c2"]
     assert bench.decode_bytes(v2, w2, 256) == 256 * 2_228_485 + 65_536              # 570.56 MB per c2 decode launch
+
+
+def test_binding_structs_and_constants_match_the_headers(tmp_path):
+    """Every ctypes structure of the binding has the size and field offsets of
+    the C struct of the same name, and every LSC_ constant the binding defines
+    has the value of the header's macro, as a C compiler sees them."""
+    structs = [getattr(L, n) for n in dir(L)
+               if isinstance(getattr(L, n), type) and issubclass(getattr(L, n), ctypes.Structure)]
+    assert len(structs) >= 12
+    consts = {n: getattr(L, n) for n in dir(L) if n.startswith("LSC_") and isinstance(getattr(L, n), int)}
+    lines = []
+    for s in structs:
+        lines.append(f'  printf("%s %zu\\n", "{s.__name__}", sizeof({s.__name__}));')
+        for f in s._fields_:
+            lines.append(f'  printf("%s %zu\\n", "{s.__name__}.{f[0]}", offsetof({s.__name__}, {f[0]}));')
+    for n in consts:
+        lines.append(f'  printf("%s %lld\\n", "{n}", (long long)({n}));')
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"lsc.h\"\n#include \"lsc_kv.h\"\n"
+                   "#include \"lsc_prefix_cache.h\"\n#include \"lsc_store.h\"\nint main(void) {\n"
+                   + "\n".join(lines) + "\n  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    cc = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                         "-o", str(exe)], capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    got = dict(l.rsplit(" ", 1) for l in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                         check=True).stdout.splitlines())
+    for s in structs:
+        assert int(got[s.__name__]) == ctypes.sizeof(s), s.__name__
+        for f in s._fields_:
+            assert int(got[f"{s.__name__}.{f[0]}"]) == getattr(s, f[0]).offset, (s.__name__, f[0])
+    for n, v in consts.items():
+        assert int(got[n]) == v, n

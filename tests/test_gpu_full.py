@@ -111,12 +111,16 @@ def test_c4_resume_prefill_sampled_sequences(lsc, algorithm):
         assert P.status() == L.LSC_OK
 
 
-def test_c1_serving_step_back_to_back(lsc):
+@pytest.mark.parametrize("flags", [0, L.LSC_DECODE_EARLY_STATE])
+def test_c1_serving_step_back_to_back(lsc, flags):
     """The benchmarked step as the benchmark issues it: lsc_restore of the 64
     c1 rows on a prepare stream, an event, then 36 lsc_gdn_decode launches back
     to back on the forward stream with no host sync, then a second token (36
     more launches).  Hit rows, has_initial_state, both tokens' outputs and the
-    final states of three sampled layers against the oracle."""
+    final states of three sampled layers against the oracle.  With the early
+    state flag each launch streams its layer's first state tiles while the
+    previous layer's launch finishes (the first launch of each token follows
+    the event or the other layer's decode, neither writing its rows)."""
     w = W.get("c1")
     rows = W.restore_rows("c1")
     n = len(rows.live)
@@ -148,7 +152,7 @@ def test_c1_serving_step_back_to_back(lsc):
         for tok in range(2):
             for l in P.gdn_layers:
                 args = L.decode_args(n, w.num_k_heads, idx, hs, dx[tok, l], dw[l], da[tok, l], db[tok, l],
-                                     out[tok, l])
+                                     out[tok, l], flags)
                 assert L.lsc_gdn_decode(P.pool, l, args, fwd) == L.LSC_OK
         torch.cuda.synchronize()
         hs_o = rows.hs_prefill.copy()

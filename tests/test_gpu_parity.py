@@ -232,14 +232,14 @@ def decode_case(w, seed, n=None, cold_frac=0.25, pad_row=True, has_init_null=Fal
     return idx, has, x, cw, a, b
 
 
-def run_decode(P, l, w, idx, has, x, cw, a, b, stream=None):
+def run_decode(P, l, w, idx, has, x, cw, a, b, stream=None, flags=0):
     n = len(idx)
     out = torch.full((n, w.num_v_heads, w.head_v_dim), float("nan"), device="cuda")
     dx, dw = conv_bytes_dev(x, w.conv_dtype), conv_bytes_dev(cw, w.conv_dtype)
     di = dev(idx)
     dh = dev(has) if has is not None else None
     da, db = dev(a), dev(b)
-    args = L.decode_args(n, w.num_k_heads, di, dh, dx, dw, da, db, out)
+    args = L.decode_args(n, w.num_k_heads, di, dh, dx, dw, da, db, out, flags)
     rc = L.lsc_gdn_decode(P.pool, l, args, stream)
     torch.cuda.synchronize()
     return rc, out.cpu().numpy()
@@ -300,7 +300,8 @@ def test_decode_more_items_than_one_launch_holds(lsc):
         assert P.status() == L.LSC_OK
 
 
-def test_decode_fp32_dk128_ring_wraps(lsc):
+@pytest.mark.parametrize("flags", [0, L.LSC_DECODE_EARLY_STATE])
+def test_decode_fp32_dk128_ring_wraps(lsc, flags):
     """The benchmarked decode instantiation (head_k_dim 128, fp32 state, bf16
     conv, width 4) with 512 rows of two q/k heads: 1024 work items, so each CTA
     holds six or seven items of four 32 KiB tiles and its ring of stages wraps
@@ -311,9 +312,39 @@ def test_decode_fp32_dk128_ring_wraps(lsc):
         pre = P.host[l].copy()
         idx, has, x, cw, a, b = decode_case(w, seed=42, n=512, cold_frac=0.1)
         assert len(idx) * w.num_k_heads >= 6 * torch.cuda.get_device_properties(0).multi_processor_count
-        rc, out = run_decode(P, l, w, idx, has, x, cw, a, b, torch.cuda.current_stream())
+        rc, out = run_decode(P, l, w, idx, has, x, cw, a, b, torch.cuda.current_stream(), flags)
         assert rc == L.LSC_OK, L.lsc_error_string(rc)
         check_decode(w, P, l, pre, idx, has, x, cw, a, b, out)
+        assert P.status() == L.LSC_OK
+
+
+@pytest.mark.parametrize("name", ["c0p", "s1", "s3", "s4"])
+def test_decode_early_state_chain_of_layers(lsc, name):
+    """Every GDN layer of the pool decoded back to back on one stream with the
+    early state flag and no host sync in between (each launch may read its
+    rows and first state tiles while the previous layer's launch runs), then
+    each layer against the oracle.  Covers the vector and the channel-by-channel
+    conv paths, cold rows and a padding row."""
+    w = workload(name, layers=[W.GDN, W.ATTN, W.GDN, W.GDN, W.ATTN, W.GDN])
+    with DevPool(w, seed=23, random_padding=True) as P:
+        s = torch.cuda.Stream()
+        keep, cases = [], {}
+        for l in P.gdn_layers:
+            idx, has, x, cw, a, b = decode_case(w, seed=100 + l)
+            n = len(idx)
+            out = torch.full((n, w.num_v_heads, w.head_v_dim), float("nan"), device="cuda")
+            t = [dev(idx), dev(has), conv_bytes_dev(x, w.conv_dtype), conv_bytes_dev(cw, w.conv_dtype), dev(a),
+                 dev(b), out]
+            keep.append(t)
+            cases[l] = (idx, has, x, cw, a, b, out)
+        torch.cuda.synchronize()
+        for l, t in zip(P.gdn_layers, keep):
+            args = L.decode_args(len(cases[l][0]), w.num_k_heads, *t, flags=L.LSC_DECODE_EARLY_STATE)
+            assert L.lsc_gdn_decode(P.pool, l, args, s) == L.LSC_OK
+        torch.cuda.synchronize()
+        for l in P.gdn_layers:
+            idx, has, x, cw, a, b, out = cases[l]
+            check_decode(w, P, l, P.host[l].copy(), idx, has, x, cw, a, b, out.cpu().numpy())
         assert P.status() == L.LSC_OK
 
 
@@ -386,6 +417,9 @@ def test_decode_rejects(lsc):
         assert L.lsc_gdn_decode(P.pool, 1, args) == L.LSC_ERR_STATELESS_LAYER
         args = L.decode_args(0, 1, None, None, None, None, None, None, None)
         assert L.lsc_gdn_decode(P.pool, 0, args) == L.LSC_OK
+        for bad in (2, 0x80000000, L.LSC_DECODE_EARLY_STATE | 4):  # flag bits the call does not define
+            args = L.decode_args(2, 1, 256, 256, 256, 256, 256, 256, 256, bad)
+            assert L.lsc_gdn_decode(P.pool, 0, args) == L.LSC_ERR_INVALID_ARG
     w = workload("c0", head_k_dim=24, conv_dim=2 * 24 + 2 * 16, ssm_dtype=W.F32)
     with DevPool(w) as P:
         # aligned stand-in addresses (never dereferenced: the shape is refused first)
