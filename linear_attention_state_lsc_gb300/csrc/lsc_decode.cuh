@@ -222,13 +222,24 @@ __global__ void __launch_bounds__(kDecodeBlock, 1) decode_kernel(const __grid_co
 
   // Early start (the caller vouches that the previous kernel of the stream
   // writes neither idx, has_init nor this layer's ssm state): read the rows and
-  // fill the ring with the first state tiles while that kernel finishes; every
-  // other input is read after griddep_wait() as usual.
+  // fill the ring with the first state tiles while that kernel finishes; when
+  // the ring holds less than two items, the next item's tiles are prefetched
+  // into L2 as well (serving-step decode, fp32 state: 47.6 -> 46.2 us per
+  // launch; with a ring of three bf16 items it cost 1 %).  Every other input is
+  // read after griddep_wait() as usual.
   const bool early = p.early_state != 0;
   if (early) {
     load_rows();
-    if (tid == kProducer)
+    if (tid == kProducer) {
       for (int t = 0; t < NS; ++t) issue_tile(t, l2_evict_first_policy());
+      const int l2_end = NS < 2 * D.TPG ? min(my_tiles, NS + D.TPG) : NS;
+      for (int t = NS; t < l2_end; ++t) {
+        uint32_t bytes;
+        bool live, load;
+        const uint8_t *src = tile_addr(t, bytes, live, load);
+        if (load) bulk_prefetch_l2(src, bytes);
+      }
+    }
   }
   // the previous kernel of the stream may still be running until here
   griddep_wait();

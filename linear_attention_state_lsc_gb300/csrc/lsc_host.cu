@@ -523,12 +523,14 @@ int lsc_gdn_decode(lsc_pool *p, int32_t layer, const lsc_gdn_decode_args *a, voi
   d.out = a->out;
   d.status = g.status;
   // The vector conv path reads and writes 8-channel groups of the conv state,
-  // x and the weights with 16-byte accesses: every segment (q/k/v channel
-  // ranges) must be 16-byte aligned in start and length.
+  // x and the weights with 16-byte accesses: a work item's channels (q and k of
+  // one q/k head, the v channels of its Hv/Hk heads) must be whole groups, and
+  // every segment 16-byte aligned in start and length.
   const int64_t esc = g.conv_dtype == LSC_BF16 ? 2 : 4, W = g.conv_width;
   const int64_t units[] = {g.dk * (W - 1) * esc, (int64_t)g.dv * (W - 1) * esc, g.dk * esc, (int64_t)g.dv * esc,
                            (int64_t)g.conv_dim * esc, g.dk * W * esc, (int64_t)g.dv * W * esc};
-  bool tma = ((uintptr_t)a->x % 16) == 0 && ((uintptr_t)a->conv_weight % 16) == 0;
+  bool tma = ((uintptr_t)a->x % 16) == 0 && ((uintptr_t)a->conv_weight % 16) == 0 && g.dk % 8 == 0 &&
+             ((int64_t)(g.Hv / Hk) * g.dv) % 8 == 0;
   for (int64_t u : units) tma = tma && (u % 16) == 0;
   d.conv_vec = tma ? 1 : 0;
   d.wait_limit_ns = fault("timeout0") ? 0 : kWaitLimitNs;

@@ -218,6 +218,9 @@ DECODE_CASES = [
     ("s1", {"num_k_heads": 4, "conv_dim": 2 * 4 * 32 + 4 * 32}),
     # dk = 64 with fp32 state
     ("s3", {"head_k_dim": 64, "head_v_dim": 96, "conv_dim": 2 * 2 * 64 + 4 * 96}),
+    # fp32 conv, width 4, 16-byte aligned segments, but a work item of 2*16 + 3*12 = 68
+    # channels: not whole 8-channel groups, so the channel-by-channel conv path
+    ("s4", {"conv_dtype": W.F32}),
 ]
 
 
