@@ -52,7 +52,8 @@ def test_c3_restore_storm(lsc):
     assert (rep.n_hit, rep.n_miss, rep.n_noop) == (205, 154, 153)
 
 
-def test_c2_decode_full_layer(lsc):
+@pytest.mark.parametrize("flags", [0, L.LSC_DECODE_EARLY_STATE])
+def test_c2_decode_full_layer(lsc, flags):
     w = W.get("c2")
     with DevPool(w, seed=0, device_fill=True) as P:
         rng = np.random.default_rng(2)
@@ -62,7 +63,7 @@ def test_c2_decode_full_layer(lsc):
             idx = rng.permutation(w.num_slots)[:n].astype(np.int32)
             has = np.ones(n, np.uint8)
             x, cw, a, b = W.decode_inputs(w, n, seed=0, layer=l)
-            rc, out = run_decode(P, l, w, idx, has, x, cw, a, b)
+            rc, out = run_decode(P, l, w, idx, has, x, cw, a, b, flags=flags)
             assert rc == L.LSC_OK
             check_decode(w, P, l, pre, idx, has, x, cw, a, b, out)
         assert P.status() == L.LSC_OK

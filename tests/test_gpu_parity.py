@@ -351,6 +351,52 @@ def test_decode_early_state_chain_of_layers(lsc, name):
         assert P.status() == L.LSC_OK
 
 
+def test_decode_early_state_same_layer_disjoint_rows(lsc):
+    """Two decodes of one layer back to back on one stream, on disjoint row
+    sets, the second with the early state flag: the first writes none of the
+    second's rows, which is what the flag asks of the kernel before it.  Both
+    against the oracle applied in order."""
+    w = workload("s3", num_slots=600)
+    with DevPool(w, seed=31, random_padding=True) as P:
+        l = P.gdn_layers[0]
+        pre = P.host[l].copy()
+        rng = np.random.default_rng(32)
+        perm = rng.permutation(w.num_slots).astype(np.int32)
+        calls = []
+        for h, flags in ((0, 0), (1, L.LSC_DECODE_EARLY_STATE)):
+            idx = perm[h * 300:(h + 1) * 300].copy()
+            idx[7] = -1
+            has = (rng.random(300) >= 0.2).astype(np.uint8)
+            x, cw, a, b = W.decode_inputs(w, 300, seed=40 + h, layer=0)
+            out = torch.full((300, w.num_v_heads, w.head_v_dim), float("nan"), device="cuda")
+            t = [dev(idx), dev(has), conv_bytes_dev(x, w.conv_dtype), conv_bytes_dev(cw, w.conv_dtype), dev(a), dev(b),
+                 out]
+            calls.append((idx, has, x, cw, a, b, out, t, flags))
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        for idx, has, x, cw, a, b, out, t, flags in calls:
+            args = L.decode_args(len(idx), w.num_k_heads, *t, flags=flags)
+            assert L.lsc_gdn_decode(P.pool, l, args, s) == L.LSC_OK
+        torch.cuda.synchronize()
+        reg = pre.copy()
+        for idx, has, x, cw, a, b, out, t, flags in calls:
+            rc, o = oracle.gdn_decode(oracle_pool(w), reg, idx, has, W.to_dtype_bytes(x, w.conv_dtype),
+                                      W.to_dtype_bytes(cw, w.conv_dtype), w.num_k_heads, a, b)
+            assert rc == oracle.OK
+            np.testing.assert_allclose(out.cpu().numpy(), o, **tol(w.ssm_dtype))
+        got = P.download(l).reshape(w.num_slots, -1)
+        Lo = oracle_layout(w)
+        exp = reg.reshape(w.num_slots, -1)
+        np.testing.assert_array_equal(got[:, :Lo["conv_bytes"]], exp[:, :Lo["conv_bytes"]])
+        ssm = slice(Lo["ssm_offset"], Lo["ssm_offset"] + Lo["ssm_bytes"])
+        np.testing.assert_allclose(W.from_dtype_bytes(np.ascontiguousarray(got[:, ssm]), w.ssm_dtype),
+                                   W.from_dtype_bytes(np.ascontiguousarray(exp[:, ssm]), w.ssm_dtype),
+                                   **tol(w.ssm_dtype))
+        mask = ~payload_mask(w, Lo)
+        np.testing.assert_array_equal(got[:, mask], pre.reshape(w.num_slots, -1)[:, mask])
+        assert P.status() == L.LSC_OK
+
+
 def test_decode_two_steps_all_warm(lsc):
     """Two consecutive tokens on the same slots (the second reads what the first
     wrote), has_init NULL."""
