@@ -552,16 +552,36 @@ def measure_parts(L, W, torch, hbm_peak, reps=5):
         t = timed(dec_chain, 20) / len(w.gdn_layers)
         chain[key] = {"launch_ms": round(t * 1e3, 4), "GB/s": round(bytes_ / t / 1e9, 1),
                       "frac": round(bytes_ / t / 1e9 / hbm_peak, 4)}
+    L.lsc_pool_destroy(pool)
+    del buf, X, CW, A, B, OUT
+    torch.cuda.empty_cache()
+    # yardstick: the peak's own method (a torch copy) at the decode's launch
+    # size -- 36 back-to-back copies of half the launch's bytes each, distinct
+    # buffers per layer (10 GB in all, larger than L2)
+    half = bytes_ // 2 // 16 * 16
+    srcs = [torch.empty(half, dtype=torch.uint8, device="cuda") for _ in w.gdn_layers]
+    dsts = [torch.empty(half, dtype=torch.uint8, device="cuda") for _ in w.gdn_layers]
+    for t_ in srcs:
+        t_.fill_(1)
+
+    def copy_chain():
+        for a_, b_ in zip(dsts, srcs):
+            a_.copy_(b_)
+
+    t = timed(copy_chain, 20) / len(w.gdn_layers)
+    del srcs, dsts
+    torch.cuda.empty_cache()
     parts["decode_c1_chain"] = {"workload": "c1 pool: 64 rows x 36 GDN layers, ssm f32, one launch per layer, "
                                             "layers back to back (the serving step's decode without its restore)",
                                 "kernel": "decode_kernel<128,f32>", "bytes_per_launch": bytes_,
                                 "plain": chain["plain"],
                                 "early_state": chain["early_state"] | {
                                     "flags": "LSC_DECODE_EARLY_STATE: rows and first state tiles read before the "
-                                             "wait for the previous layer's launch"}}
-    L.lsc_pool_destroy(pool)
-    del buf, X, CW, A, B, OUT
-    torch.cuda.empty_cache()
+                                             "wait for the previous layer's launch"},
+                                "copy_yardstick": {"what": "torch copy_ (the measured peak's method) of the same "
+                                                           "bytes per launch, 36 back to back", "launch_ms":
+                                                   round(t * 1e3, 4), "GB/s": round(2 * half / t / 1e9, 1),
+                                                   "frac": round(2 * half / t / 1e9 / hbm_peak, 4)}}
 
     # decode step at 256 rows, bf16 state, one launch per layer over 36 layers
     w = W.get("c2")
