@@ -27,6 +27,15 @@ __device__ __forceinline__ void report(int32_t *status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Every copy kernel is launched with programmatic stream serialisation
+// (launch_pdl): its CTAs may be placed while the previous kernel of the stream
+// runs, and wait here, before any global access, until that kernel has
+// completed; then they let the next such kernel be placed early in turn.
+__device__ __forceinline__ void pdl_enter() {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+}
+
 // Block-cooperative copy of nvec 16 B vectors: every thread issues kUnroll
 // loads before its stores, so a CTA keeps kThreads * kUnroll * 16 B in flight.
 __device__ __forceinline__ void copy_vec16(uint4 *__restrict__ d, const uint4 *__restrict__ s,
@@ -77,6 +86,7 @@ __device__ __forceinline__ void zero_span(uint8_t *dst, int64_t len) {
 // Consecutive units are consecutive chunks of one page, so at any moment the
 // grid streams a contiguous stretch of each source page.
 __global__ void __launch_bounds__(kThreads) restore_kernel(const __grid_constant__ RestorePlan p) {
+  pdl_enter();
   const int gthreads = gridDim.x * blockDim.x;
   for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < p.n_hs; j += gthreads) {
     const int32_t e = p.hs_ops[j];
@@ -114,6 +124,7 @@ constexpr uint64_t kBulkWaitNs = 1000000000ull;
 __global__ void __launch_bounds__(32) restore_bulk_kernel(const __grid_constant__ RestorePlan p) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint64_t full[kBulkStages];
+  pdl_enter();
   const int gthreads = gridDim.x * blockDim.x;
   for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < p.n_hs; j += gthreads) {
     const int32_t e = p.hs_ops[j];
@@ -176,6 +187,7 @@ __global__ void __launch_bounds__(32) restore_bulk_kernel(const __grid_constant_
 // copy_prefix: unit = (op, attention layer, lane, chunk of the op's rows);
 // the rows [0, n) of a block are one contiguous span of n * row_bytes bytes.
 __global__ void __launch_bounds__(kThreads) kv_copy_kernel(const __grid_constant__ KvPlan p) {
+  pdl_enter();
   const int64_t per_op = (int64_t)p.num_layers * 2 * p.chunks_per_op;
   const int64_t total = (int64_t)p.n_ops * per_op;
   for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
@@ -197,6 +209,7 @@ __global__ void __launch_bounds__(kThreads) kv_copy_kernel(const __grid_constant
 
 // Gather: unit = (row, chunk of the conv view or of the ssm view).
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ AccessParams p) {
+  pdl_enter();
   const int cps = p.conv_chunks + p.ssm_chunks;
   const int64_t total = (int64_t)p.n * cps;
   for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
@@ -228,6 +241,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
 
 // Scatter: the inverse; negative or out-of-range indices write nothing.
 __global__ void __launch_bounds__(kThreads) scatter_kernel(const __grid_constant__ AccessParams p) {
+  pdl_enter();
   const int cps = p.conv_chunks + p.ssm_chunks;
   const int64_t total = (int64_t)p.n * cps;
   for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
@@ -288,34 +302,38 @@ int restore_bulk_grid(int num_sms) { return 2 * num_sms; }
 SmemLimit g_bulk_smem;
 
 cudaError_t launch_restore(const RestorePlan &plan, int grid, cudaStream_t stream) {
+  cudaError_t e;
   if (plan.bulk) {
     const int smem = kBulkStages * (int)kBulkChunk;
-    cudaError_t e = g_bulk_smem.ensure((const void *)restore_bulk_kernel, smem);
+    e = g_bulk_smem.ensure((const void *)restore_bulk_kernel, smem);
     if (e != cudaSuccess) return e;
-    restore_bulk_kernel<<<grid, 32, smem, stream>>>(plan);
+    e = launch_pdl(restore_bulk_kernel, grid, 32, smem, stream, plan);
   } else {
-    restore_kernel<<<grid, kThreads, 0, stream>>>(plan);
+    e = launch_pdl(restore_kernel, grid, kThreads, 0, stream, plan);
   }
-  return cudaGetLastError();
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_gather(const AccessParams &p, int num_sms, cudaStream_t stream) {
   const int64_t units = (int64_t)p.n * (p.conv_chunks + p.ssm_chunks);
-  gather_kernel<<<grid_for((const void *)gather_kernel, num_sms, units), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(gather_kernel, grid_for((const void *)gather_kernel, num_sms, units), kThreads, 0,
+                                   stream, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_kv_copy(const KvPlan &p, int num_sms, cudaStream_t stream) {
   const int64_t units = (int64_t)p.n_ops * p.num_layers * 2 * p.chunks_per_op;
   if (units == 0) return cudaSuccess;
-  kv_copy_kernel<<<grid_for((const void *)kv_copy_kernel, num_sms, units), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(kv_copy_kernel, grid_for((const void *)kv_copy_kernel, num_sms, units), kThreads,
+                                   0, stream, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_scatter(const AccessParams &p, int num_sms, cudaStream_t stream) {
   const int64_t units = (int64_t)p.n * (p.conv_chunks + p.ssm_chunks);
-  scatter_kernel<<<grid_for((const void *)scatter_kernel, num_sms, units), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(scatter_kernel, grid_for((const void *)scatter_kernel, num_sms, units), kThreads,
+                                   0, stream, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace lsc

@@ -23,6 +23,25 @@ struct TraceRange {
   TraceRange &operator=(const TraceRange &) = delete;
 };
 
+// Launch with programmatic stream serialisation: the grid's CTAs may be placed
+// while the previous kernel of the stream still runs; the kernel itself waits
+// (griddepcontrol.wait) for that kernel's completion before any global access
+// it does not own, and may let the next such kernel be placed early.
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, A &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<A &&>(args)...);
+}
+
 // ---- per-device launch state -------------------------------------------------
 // A kernel's dynamic shared-memory limit (cudaFuncSetAttribute) and figures
 // such as its occupancy belong to the device that is current at the call, and

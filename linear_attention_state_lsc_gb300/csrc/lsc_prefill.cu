@@ -150,8 +150,17 @@ __device__ __forceinline__ bool tokens_rotated(F &tok, int &t, int end) {
   }
 }
 
+// Every kernel of this file is launched with programmatic stream
+// serialisation (launch_pdl): it waits here, before any global access, for the
+// kernel before it on the stream to complete, then lets the next be placed.
+__device__ __forceinline__ void pdl_enter() {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+}
+
 template <typename TC, int CW>
 __global__ void __launch_bounds__(kPrefillThreads, CW ? 3 : 1) prefill_conv_vec_kernel(const __grid_constant__ PrefillConvParams p) {
+  pdl_enter();
   constexpr int WW = CW ? CW : kMaxTaps;  // register window, W <= WW
   constexpr int H = WW - 1;               // window inputs before the current token
   constexpr int esc = (int)sizeof(TC);
@@ -358,6 +367,7 @@ __global__ void __launch_bounds__(kPrefillThreads, CW ? 3 : 1) prefill_conv_vec_
 // ---------------------------------------------------------------- any shape
 template <typename TC>
 __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_scalar_kernel(const __grid_constant__ PrefillConvParams p) {
+  pdl_enter();
   using E = Elem<TC>;
   const int W = p.conv_width, C = p.conv_dim;
   const int c = blockIdx.x * kPrefillThreads + threadIdx.x;
@@ -413,6 +423,7 @@ __global__ void __launch_bounds__(kPrefillThreads) prefill_conv_scalar_kernel(co
 // q and k of every (token, head) divided by sqrt(sum of squares + 1e-6): one
 // warp per (token, head).
 __global__ void __launch_bounds__(kPrefillThreads) qk_norm_kernel(const __grid_constant__ PrefillConvParams p) {
+  pdl_enter();
   const int64_t wid = (int64_t)blockIdx.x * (kPrefillThreads / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   const int64_t n = (int64_t)p.total_tokens * p.Hk * 2;
@@ -431,6 +442,7 @@ __global__ void __launch_bounds__(kPrefillThreads) qk_norm_kernel(const __grid_c
 // copied bit for bit.  One thread per (sequence, channel).
 template <typename TB>  // raw element bits: uint16_t (bf16) or uint32_t (f32)
 __global__ void __launch_bounds__(kPrefillThreads) prefill_state_kernel(const __grid_constant__ PrefillConvParams p) {
+  pdl_enter();  // the conv kernel before it has read every old conv state
   const int W = p.conv_width, C = p.conv_dim;
   const int c = blockIdx.x * kPrefillThreads + threadIdx.x;
   const int s = blockIdx.y;
@@ -464,24 +476,31 @@ template <typename TC>
 int launch_prefill_t(const PrefillConvParams &p, cudaStream_t s) {
   const int tiles = (p.total_tokens + kPrefillTile - 1) / kPrefillTile;
   if (tiles > 0) {
+    cudaError_t e;
     if (p.vec) {
       const dim3 grid((p.conv_dim / 8 + kPrefillThreads - 1) / kPrefillThreads, tiles);
-      if (p.conv_width == 4) prefill_conv_vec_kernel<TC, 4><<<grid, kPrefillThreads, 0, s>>>(p);
-      else prefill_conv_vec_kernel<TC, 0><<<grid, kPrefillThreads, 0, s>>>(p);
+      e = p.conv_width == 4 ? launch_pdl(prefill_conv_vec_kernel<TC, 4>, grid, kPrefillThreads, 0, s, p)
+                            : launch_pdl(prefill_conv_vec_kernel<TC, 0>, grid, kPrefillThreads, 0, s, p);
     } else {
       const dim3 grid((p.conv_dim + kPrefillThreads - 1) / kPrefillThreads, tiles);
-      prefill_conv_scalar_kernel<TC><<<grid, kPrefillThreads, 0, s>>>(p);
+      e = launch_pdl(prefill_conv_scalar_kernel<TC>, grid, kPrefillThreads, 0, s, p);
       const int64_t warps = (int64_t)p.total_tokens * p.Hk * 2;
       const int64_t blocks = (warps + kPrefillThreads / 32 - 1) / (kPrefillThreads / 32);
-      if (blocks > 0) qk_norm_kernel<<<(unsigned)blocks, kPrefillThreads, 0, s>>>(p);
+      if (e == cudaSuccess && blocks > 0) e = launch_pdl(qk_norm_kernel, dim3((unsigned)blocks), kPrefillThreads, 0, s, p);
     }
-    if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
+      cudaGetLastError();
+      return LSC_ERR_CUDA;
+    }
   }
   if (p.n_seq > 0) {
     const dim3 grid((p.conv_dim + kPrefillThreads - 1) / kPrefillThreads, p.n_seq);
-    if (sizeof(TC) == 2) prefill_state_kernel<uint16_t><<<grid, kPrefillThreads, 0, s>>>(p);
-    else prefill_state_kernel<uint32_t><<<grid, kPrefillThreads, 0, s>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return LSC_ERR_CUDA;
+    const cudaError_t e = sizeof(TC) == 2 ? launch_pdl(prefill_state_kernel<uint16_t>, grid, kPrefillThreads, 0, s, p)
+                                          : launch_pdl(prefill_state_kernel<uint32_t>, grid, kPrefillThreads, 0, s, p);
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
+      cudaGetLastError();
+      return LSC_ERR_CUDA;
+    }
   }
   return LSC_OK;
 }
