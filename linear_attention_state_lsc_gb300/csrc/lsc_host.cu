@@ -410,6 +410,12 @@ int lsc_restore(lsc_pool *p, const LinearStateCacheOp *ops, int32_t n_rows, cons
       if (hit && g.num_gdn > 0) P.hit[P.n_hits++] = make_int2(ops[i].linear_state_id, ops[i].restore_src_slot_id);
     }
     if (P.n_hs == 0) continue;
+    {  // does a source slot feed more than one hit of this launch
+      std::vector<int32_t> src(P.n_hits);
+      for (int32_t h = 0; h < P.n_hits; ++h) src[h] = P.hit[h].y;
+      std::sort(src.begin(), src.end());
+      P.src_reuse = std::adjacent_find(src.begin(), src.end()) != src.end() ? 1 : 0;
+    }
     cudaError_t e = lsc::launch_restore(P, grid, stream);
     if (e != cudaSuccess) { cudaGetLastError(); return LSC_ERR_CUDA; }
     launches++;

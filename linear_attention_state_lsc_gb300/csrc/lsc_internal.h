@@ -136,6 +136,7 @@ struct RestorePlan {
   int32_t n_hits;
   int32_t n_hs;
   int32_t bulk;            // 1: copy through shared memory with 1-D TMA bulk copies
+  int32_t src_reuse;       // 1: a source slot feeds several hits (its loads keep L2 priority)
   int32_t *status;         // device error word (bulk copies: a bounded wait gave up)
   int2 hit[kPlanMaxHits];  // (dst slot, src slot)
   int32_t hs_ops[kPlanMaxHs];  // (row << 1) | value

@@ -75,6 +75,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// The default priority, for data that will be read again soon.
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`, under
 // an L2 cache policy (l2_evict_first_policy).  Both addresses 16-byte aligned,

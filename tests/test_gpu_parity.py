@@ -285,7 +285,8 @@ def test_decode_matches_oracle(lsc, name, kw):
 
 
 @pytest.mark.big
-def test_decode_more_items_than_one_launch_holds(lsc):
+@pytest.mark.parametrize("flags", [0, L.LSC_DECODE_EARLY_STATE])
+def test_decode_more_items_than_one_launch_holds(lsc, flags):
     """A CTA holds at most 512 work items per launch, so more than 512 x SMs /
     Hk rows are split over several launches; the result is the same."""
     w0 = W.small("s1")   # Hk = 2: the split happens below the 65535-row limit
@@ -297,7 +298,7 @@ def test_decode_more_items_than_one_launch_holds(lsc):
         l = P.gdn_layers[0]
         pre = P.host[l].copy()
         idx, has, x, cw, a, b = decode_case(w, seed=19, n=n)
-        rc, out = run_decode(P, l, w, idx, has, x, cw, a, b)
+        rc, out = run_decode(P, l, w, idx, has, x, cw, a, b, flags=flags)
         assert rc == L.LSC_OK
         check_decode(w, P, l, pre, idx, has, x, cw, a, b, out)
         assert P.status() == L.LSC_OK
