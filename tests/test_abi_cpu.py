@@ -357,3 +357,29 @@ def test_binding_structs_and_constants_match_the_headers(tmp_path):
             assert int(got[f"{s.__name__}.{f[0]}"]) == getattr(s, f[0]).offset, (s.__name__, f[0])
     for n, v in consts.items():
         assert int(got[n]) == v, n
+
+
+def test_recurrent_workspace_query_host_only():
+    """The chunked order's scratch is one record of (2 * 64 * 64 + 64 + 64 + 16)
+    floats per (chunk slot, v head), with (T + 63) / 64 + n_seq chunk slots
+    (sequence i's chunks start at slot floor(cu_i / 64) + i); the token order,
+    and AUTO below head_k_dim 128, need none.  The query needs no GPU."""
+    L.load()
+    rec = (2 * 64 * 64 + 64 + 64 + 16) * 4
+    assert rec == 33344
+    for name, dk, n_seq, T in (("c4", 128, 64, 60840), ("c4", 128, 1, 1), ("c4", 128, 3, 0), ("s1", 32, 5, 300)):
+        w = W.get(name) if name.startswith("c") else W.small(name)
+        pool = host_pool(w)
+        try:
+            for algo in (L.LSC_RECURRENT_AUTO, L.LSC_RECURRENT_TOKEN, L.LSC_RECURRENT_CHUNKED):
+                args = L.recurrent_args(n_seq, w.num_k_heads, T, None, None, None, None, None, None, None, None,
+                                        None, algorithm=algo)
+                rc, n = L.lsc_gdn_recurrent_workspace_bytes(pool, args)
+                assert rc == L.LSC_OK
+                chunked = algo == L.LSC_RECURRENT_CHUNKED or (algo == L.LSC_RECURRENT_AUTO and dk == 128)
+                slots = (T + 63) // 64 + n_seq
+                assert n == (slots * w.num_v_heads * rec if chunked else 0), (name, algo, n)
+            bad = L.recurrent_args(-1, w.num_k_heads, T, None, None, None, None, None, None, None, None, None)
+            assert L.lsc_gdn_recurrent_workspace_bytes(pool, bad)[0] == L.LSC_ERR_INVALID_ARG
+        finally:
+            L.lsc_pool_destroy(pool)
