@@ -383,3 +383,19 @@ def test_recurrent_workspace_query_host_only():
             assert L.lsc_gdn_recurrent_workspace_bytes(pool, bad)[0] == L.LSC_ERR_INVALID_ARG
         finally:
             L.lsc_pool_destroy(pool)
+
+
+def test_decode_flags_validated_before_any_device_work():
+    """lsc_gdn_decode refuses flag bits it does not define with INVALID_ARG,
+    checked on the host before the device is touched (the stand-in pointers
+    are never dereferenced)."""
+    L.load()
+    w = W.get("c0")
+    pool = host_pool(w)
+    try:
+        l = w.gdn_layers[0]
+        for bad in (2, 0x80000000, L.LSC_DECODE_EARLY_STATE | 8):
+            args = L.decode_args(2, 1, 256, 256, 256, 256, 256, 256, 256, bad)
+            assert L.lsc_gdn_decode(pool, l, args) == L.LSC_ERR_INVALID_ARG
+    finally:
+        L.lsc_pool_destroy(pool)
