@@ -83,3 +83,15 @@ def lib_desc(w: W.Workload, layers=None):
 def ops_of(rows):
     from linear_attention_state_lsc_gb300 import lsc
     return lsc.ops_array(rows.live, rows.src, rows.restore_hash, rows.save_hash, rows.save_slot)
+
+
+def gpu_present():
+    """True when a CUDA device is visible.  Tests that build host-only pools on
+    a stand-in base address make a valid (enqueuing) call only when this is
+    False: with a device present the pool would be a device pool and the
+    stand-in address would be dereferenced."""
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False

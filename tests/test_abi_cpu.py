@@ -15,7 +15,7 @@ import oracle
 from linear_attention_state_lsc_gb300 import lsc as L
 from linear_attention_state_lsc_gb300 import workloads as W
 
-from _util import lib_desc, oracle_layout, oracle_pool, ops_of
+from _util import gpu_present, lib_desc, oracle_layout, oracle_pool, ops_of
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
@@ -192,13 +192,15 @@ def test_validation_matches_oracle(lsc, case):
 
 def test_restore_rejects_before_touching_the_device(lsc):
     """On a host-only pool a valid call fails with LSC_ERR_CUDA (it would have to
-    enqueue), an invalid one with its validation error: validation runs first."""
+    enqueue), an invalid one with its validation error: validation runs first.
+    (The valid call is made only where no GPU is visible.)"""
     w = W.get("c0")
     pool = host_pool(w)
     rows = W.restore_rows("c0")
     ops = ops_of(rows)
-    rc, _ = L.lsc_restore(pool, ops, rows.nkv, 16, rows.initialized, FAKE_BASE)
-    assert rc == L.LSC_ERR_CUDA
+    if not gpu_present():
+        rc, _ = L.lsc_restore(pool, ops, rows.nkv, 16, rows.initialized, FAKE_BASE)
+        assert rc == L.LSC_ERR_CUDA
     ops2 = ops.copy()
     ops2["linear_state_id"][3] = ops2["linear_state_id"][0]
     assert L.lsc_restore(pool, ops2, rows.nkv, 16, rows.initialized, FAKE_BASE)[0] == L.LSC_ERR_DUP_DST
