@@ -983,7 +983,38 @@ def oracle_sample(n_rows=None, seed=0):
     return run, step_bytes, n_rows, min(n_rows, oracle.num_threads())
 
 
-def cpu_baseline(budget_s=12.0):
+def oracle_recurrent_sample(n_seq=None, tokens=128, seed=0):
+    """A bounded sample of the c4 resume prefill on the host: n_seq sequences
+    (one per host thread by default) of `tokens` tokens on one GDN layer of c4's
+    shapes, all warm; returns (run, token_layers per run, flops per run)."""
+    import oracle
+    from linear_attention_state_lsc_gb300 import workloads as W
+    if n_seq is None:
+        n_seq = max(1, min(16, oracle.num_threads()))
+    w = W.get("c4")
+    w.num_slots = n_seq
+    pool = oracle.Pool([oracle.GDN], n_seq, w.conv_dim, w.conv_width, oracle.BF16, w.num_v_heads, w.head_v_dim,
+                       w.head_k_dim, oracle.F32, w.page_bytes)
+    _, Lo = oracle.layout(pool)
+    rng = np.random.default_rng(seed)
+    region = np.zeros(n_seq * w.page_bytes, np.uint8)
+    pages = region.reshape(n_seq, w.page_bytes)
+    vals = rng.standard_normal((n_seq, Lo["ssm_elems"]), dtype=np.float32)
+    pages[:, Lo["ssm_offset"]:Lo["ssm_offset"] + Lo["ssm_bytes"]] = vals.view(np.uint8).reshape(n_seq, -1)
+    lengths = np.full(n_seq, tokens, np.int32)
+    cu, q, k, v, a, b = W.recurrent_inputs(w, lengths, seed=seed, layer=0)
+    idx = np.arange(n_seq, dtype=np.int32)
+    has = np.ones(n_seq, np.uint8)
+    T = int(cu[-1])
+
+    def run():
+        rc, _ = oracle.gdn_recurrent(pool, region, idx, has, cu, w.num_k_heads, q, k, v, a, b)
+        assert rc == oracle.OK
+
+    return run, T, T * w.num_v_heads * 6 * w.head_k_dim * w.head_v_dim, n_seq
+
+
+def cpu_baseline(budget_s=12.0, recurrent_budget_s=3.0):
     import oracle.build as ob
     ob.build()
     run, step_bytes, n_rows, threads = oracle_sample()
@@ -994,10 +1025,25 @@ def cpu_baseline(budget_s=12.0):
         run()
         k += 1
     el = time.perf_counter() - t
-    return {"value": round(step_bytes * k / el / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+    line = {"value": round(step_bytes * k / el / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
             "rows_per_s": round(n_rows * k / el, 3),
             "sample": f"c1 serving step on {n_rows} rows (restore x 36 GDN layers + 36 decode layers), "
                       f"{k} repetitions in {el:.1f} s, OpenMP over rows"}
+    # the resume-prefill recurrence (c4 shapes) on the same host cores
+    run, tl, flops, n_seq = oracle_recurrent_sample()
+    run()
+    t = time.perf_counter()
+    k = 0
+    while time.perf_counter() - t < recurrent_budget_s:
+        run()
+        k += 1
+    el = time.perf_counter() - t
+    line["recurrent_c4"] = {"token_layers_per_s": round(tl * k / el, 1), "GFLOP/s": round(flops * k / el / 1e9, 2),
+                            "flops_basis": "6 dk dv per (token, v head), as the GPU line",
+                            "sample": f"{n_seq} warm sequences x {tl // n_seq} tokens on one c4 layer "
+                                      f"(state [32,128,128] f32), {k} repetitions in {el:.1f} s, "
+                                      f"double precision, OpenMP over (sequence, head)"}
+    return line
 
 
 def run_reference(args):
